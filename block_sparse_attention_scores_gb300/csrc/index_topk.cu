@@ -1,0 +1,315 @@
+// Index branch of MiniMax Sparse Attention: scores, block max-pool and top-k.
+//
+// itinai.ru "How to solve the memory problem with MiniMax Sparse Attention",
+// section "How the indexer works": score every visible token with the
+// group's index query against the shared index key, max-pool per block, keep
+// the top-k blocks with the query's own block always included; section
+// "Kernel optimisations": selection runs on the raw scores (softmax keeps the
+// order, so no exp or sum is needed). dothoosh.com "how Flash-MSA cuts
+// million-token training cost", "Kernel design and execution": the proxy pass
+// accumulates no output, only scores and the running top-k.
+//
+// GB300 design. One work item = 128 consecutive queries (one query block qb)
+// of one (b, g). Its 128 index-query rows (128 x 64 bf16) are the UMMA A
+// operand; every earlier KV block c < qb of k_idx (128 x 64) is a B operand.
+// Because Bk = 128 = UMMA N, the 128 fp32 columns of one accumulator are
+// exactly one block, so each epilogue thread (one TMEM lane = one query) takes
+// its block max with 127 fmax and inserts (max, c) into a register top-(k-1).
+// The own block needs no score: it is always kept.
+//
+// Warp roles (192 threads, 2 CTAs per SM, persistent over work items handed
+// out largest-qb-first by an atomic counter):
+//   warp 0      TMA producer: q tile per item, k_idx tiles into a 4-stage ring
+//   warp 1      TMEM owner and UMMA issuer (one thread), 2 accumulators
+//   warps 2..5  epilogue: tcgen05.ld, block max, running top-k, output
+#include "msa_internal.h"
+#include "sm100.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kStages = 4;
+constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
+
+struct TopkArgs {
+  int B, T, G, n, k;
+  int num_items;
+  int32_t* block_idx;
+  int* counter;
+  int* err;
+};
+
+struct TopkShared {
+  uint64_t q_full[2], q_empty[2];
+  uint64_t k_full[kStages], k_empty[kStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t it_full[2], it_empty[2];
+  int item[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void decode_item(int item, int B, int G, int n, int& b, int& g, int& qb) {
+  const int BG = B * G;
+  qb = n - 1 - item / BG;
+  const int bg = item % BG;
+  b = bg / G;
+  g = bg % G;
+}
+
+// Insert (v, c) into a list sorted by (value desc, id asc). Ids arrive in
+// increasing order, so an equal value never displaces an earlier entry.
+template <int CAP>
+__device__ __forceinline__ void topk_insert(float (&val)[CAP], int (&idx)[CAP], float v, int c) {
+  if (!(v > val[CAP - 1])) return;
+  float cv = v;
+  int ci = c;
+#pragma unroll
+  for (int i = 0; i < CAP; ++i) {
+    const bool sw = cv > val[i];
+    const float tv = val[i];
+    const int ti = idx[i];
+    val[i] = sw ? cv : tv;
+    idx[i] = sw ? ci : ti;
+    cv = sw ? tv : cv;
+    ci = sw ? ti : ci;
+  }
+}
+
+template <int CAP>
+__global__ void __launch_bounds__(kThreads, 2)
+    index_topk_kernel(TopkArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;                   // 2 x 16 KB
+  uint8_t* sK = smem + 2 * kTileBytes;  // kStages x 16 KB
+  __shared__ TopkShared sh;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.q_full[i], 1);
+      mbar_init(&sh.q_empty[i], 1);
+      mbar_init(&sh.acc_full[i], 1);
+      mbar_init(&sh.acc_empty[i], 4);
+      mbar_init(&sh.it_full[i], 1);
+      mbar_init(&sh.it_empty[i], 5);
+    }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_empty[i], 1);
+    }
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_k);
+      uint32_t kc = 0;
+      for (int it = 0;; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 101)) { *abort_flag = 1; break; }
+        int item = atomicAdd(a.counter, 1);
+        if (item >= a.num_items || *abort_flag) item = -1;
+        sh.item[s] = item;
+        mbar_arrive(&sh.it_full[s]);
+        if (item < 0) break;
+        int b, g, qb;
+        decode_item(item, a.B, a.G, a.n, b, g, qb);
+        if (!mbar_wait(&sh.q_empty[s], ph ^ 1, a.err, 102)) { *abort_flag = 1; break; }
+        mbar_arrive_expect_tx(&sh.q_full[s], kTileBytes);
+        tma_load_3d(sQ + s * kTileBytes, &map_q, &sh.q_full[s], 0, g, b * a.T + qb * 128);
+        bool ok = true;
+        for (int c = 0; c < qb; ++c, ++kc) {
+          const int st = kc % kStages;
+          if (!mbar_wait(&sh.k_empty[st], ((kc / kStages) & 1) ^ 1, a.err, 103)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sh.k_full[st], kTileBytes);
+          tma_load_2d(sK + st * kTileBytes, &map_k, &sh.k_full[st], 0, b * a.T + c * 128);
+        }
+        if (!ok) { *abort_flag = 1; break; }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- UMMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+      uint32_t kc = 0, ac = 0;
+      for (int it = 0;; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 111)) { *abort_flag = 1; break; }
+        const int item = sh.item[s];
+        mbar_arrive(&sh.it_empty[s]);
+        if (item < 0) break;
+        int b, g, qb;
+        decode_item(item, a.B, a.G, a.n, b, g, qb);
+        if (!mbar_wait(&sh.q_full[s], ph, a.err, 112)) { *abort_flag = 1; break; }
+        tc_fence_after();
+        const uint32_t qaddr = smem_u32(sQ + s * kTileBytes);
+        bool ok = true;
+        for (int c = 0; c < qb; ++c, ++kc, ++ac) {
+          const int st = kc % kStages;
+          const int ab = ac & 1;
+          if (!mbar_wait(&sh.k_full[st], (kc / kStages) & 1, a.err, 113)) { ok = false; break; }
+          if (!mbar_wait(&sh.acc_empty[ab], ((ac >> 1) & 1) ^ 1, a.err, 114)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kaddr = smem_u32(sK + st * kTileBytes);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t ad = make_sdesc(qaddr + ks * 32, 16, 1024, kSw128);
+            const uint64_t bd = make_sdesc(kaddr + ks * 32, 16, 1024, kSw128);
+            umma_bf16_ss(tmem + ab * 128, ad, bd, idesc, ks > 0);
+          }
+          umma_commit(&sh.k_empty[st]);
+          umma_commit(&sh.acc_full[ab]);
+        }
+        umma_commit(&sh.q_empty[s]);
+        if (!ok) { *abort_flag = 1; break; }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint32_t ac = 0;
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 121)) { *abort_flag = 1; break; }
+      const int item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item < 0) break;
+      int b, g, qb;
+      decode_item(item, a.B, a.G, a.n, b, g, qb);
+      float val[CAP];
+      int idx[CAP];
+#pragma unroll
+      for (int i = 0; i < CAP; ++i) {
+        val[i] = -INFINITY;
+        idx[i] = -1;
+      }
+      bool ok = true;
+      for (int c = 0; c < qb; ++c, ++ac) {
+        const int ab = ac & 1;
+        if (!mbar_wait(&sh.acc_full[ab], (ac >> 1) & 1, a.err, 122)) { ok = false; break; }
+        tc_fence_after();
+        float m0 = -INFINITY, m1 = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float v0[32], v1[32];
+          tmem_ld32(lane_addr + ab * 128 + h * 64, v0);
+          tmem_ld32(lane_addr + ab * 128 + h * 64 + 32, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            m0 = fmaxf(m0, fmaxf(v0[i], v0[i + 1]));
+            m1 = fmaxf(m1, fmaxf(v1[i], v1[i + 1]));
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);
+        topk_insert<CAP>(val, idx, fmaxf(m0, m1), c);
+      }
+      if (!ok) { *abort_flag = 1; break; }
+      // keep the best k-1, order them by block id, append the own block
+      const int nsel = min(a.k - 1, qb);
+#pragma unroll
+      for (int i = 0; i < CAP; ++i)
+        if (i >= nsel) idx[i] = 0x7fffffff;
+#pragma unroll
+      for (int pass = 0; pass < CAP; ++pass) {
+#pragma unroll
+        for (int i = pass & 1; i + 1 < CAP; i += 2) {
+          const int lo = min(idx[i], idx[i + 1]), hi = max(idx[i], idx[i + 1]);
+          idx[i] = lo;
+          idx[i + 1] = hi;
+        }
+      }
+      const int t = qb * 128 + row;
+      int32_t* dst = a.block_idx + (((size_t)b * a.G + g) * a.T + t) * a.k;
+#pragma unroll
+      for (int i = 0; i <= CAP; ++i) {
+        if (i < a.k) {
+          const int v = i < nsel ? idx[i < CAP ? i : 0] : (i == nsel ? qb : -1);
+          dst[i] = v;
+        }
+      }
+      for (int i = CAP + 1; i < a.k; ++i) dst[i] = -1;
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+template <int CAP>
+cudaError_t launch_cap(const Prob& p, const TopkArgs& args, const CUtensorMap& mq, const CUtensorMap& mk,
+                       cudaStream_t st) {
+  auto kern = index_topk_kernel<CAP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int grid = min(args.num_items, 2 * num_sms());
+  kern<<<grid, kThreads, kSmemBytes, st>>>(args, mq, mk);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
+                              const WsLayout& L, cudaStream_t st) {
+  CUtensorMap mq, mk;
+  {
+    const uint64_t dims[3] = {(uint64_t)p.E, (uint64_t)p.G, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {(uint64_t)p.E * 2, (uint64_t)p.G * p.E * 2};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap(&mq, const_cast<void*>(q_idx), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)p.E, (uint64_t)p.BT()};
+    const uint64_t strides[1] = {(uint64_t)p.E * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap(&mk, const_cast<void*>(k_idx), 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  TopkArgs args;
+  args.B = p.B;
+  args.T = p.T;
+  args.G = p.G;
+  args.n = p.n;
+  args.k = p.k;
+  args.num_items = p.B * p.G * p.n;
+  args.block_idx = block_idx;
+  args.counter = reinterpret_cast<int*>(w + L.counters);
+  args.err = reinterpret_cast<int*>(w + L.err);
+  cudaError_t e = cudaMemsetAsync(args.counter, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const int need = p.k - 1;
+  if (need <= 4) return launch_cap<4>(p, args, mq, mk, st);
+  if (need <= 16) return launch_cap<16>(p, args, mq, mk, st);
+  if (need <= 32) return launch_cap<32>(p, args, mq, mk, st);
+  return launch_cap<64>(p, args, mq, mk, st);
+}
+
+}  // namespace msa

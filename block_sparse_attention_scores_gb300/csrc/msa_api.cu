@@ -1,0 +1,262 @@
+// C ABI of the MSA hot path: argument validation, workspace carving and
+// kernel launch order. See include/msa.h for the contract of each call.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "msa_internal.h"
+#include "sm100.cuh"
+
+namespace msa {
+
+static thread_local char g_err[512];
+
+static msa_status fail(msa_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                 const uint32_t* box, CUtensorMapSwizzle swz) {
+  typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                               const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                               CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return false;
+    fn = reinterpret_cast<EncodeFn>(p);
+  }
+  cuuint64_t d[5], s[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+    if (i + 1 < rank) s[i] = strides_bytes[i];
+  }
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int max_work_items(const Prob& p, int tiles_per_item, int rows_per_tile) {
+  // each list of length L gives ceil(ceil(L / rows) / tiles) items; the sum is
+  // bounded by total_tiles / tiles + lists, total_tiles <= entries / rows + lists
+  const long long lists = (long long)p.B * p.G * p.n;
+  const long long entries = (long long)p.B * p.G * p.T * p.k;
+  const long long tiles = entries / rows_per_tile + lists;
+  return (int)(tiles / tiles_per_item + lists + 1);
+}
+
+WsLayout ws_layout(const Prob& p, int which) {
+  WsLayout L;
+  size_t off = 256;  // header: error word + counters
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  const size_t lists = (size_t)p.B * p.G * p.n;
+  const size_t rows = (size_t)p.B * p.T;
+  if (which >= MSA_WS_FWD) {
+    L.list_count = take(lists * 4);
+    L.list_off = take((lists + 1) * 4);
+    L.list_cursor = take(lists * 4);
+    L.entries = take(rows * p.G * p.k * 4);
+    L.max_items = max_work_items(p, 1, 16);
+    L.items = take((size_t)L.max_items * 16);
+    L.n_items = take(16);
+  }
+  if (which == MSA_WS_FWD) {
+    L.o_part = take(rows * p.G * p.k * p.hg * p.d * 2);
+    L.lse_part = take(rows * p.G * p.k * p.hg * 4);
+  }
+  if (which == MSA_WS_BWD) {
+    // the forward's partial buffers alias the backward's larger ones
+    L.drow = take(rows * p.Hq * 4);
+    L.px_part = take(rows * p.G * p.k * 4);
+    L.lse_px = take(rows * p.G * 4);
+    L.dq_part = take(rows * p.G * p.k * p.hg * p.d * 2);
+    L.dqi_part = take(rows * p.G * p.k * p.E * 4);
+    L.kl_part = take(rows * p.G * p.k * 4);
+    L.dki_part = take((size_t)p.B * p.G * p.T * p.E * 4);
+    L.o_part = L.dq_part;
+    L.lse_part = take(rows * p.G * p.k * p.hg * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+static msa_status validate(const msa_shape* s, Prob* p) {
+  if (!s) return fail(MSA_ERR_INVALID_ARG, "shape is NULL");
+  if (s->B < 1 || s->T < 1 || s->Hq < 1 || s->G < 1 || s->d < 1 || s->d_idx < 1 || s->Bk < 1 || s->k < 1)
+    return fail(MSA_ERR_INVALID_ARG, "shape fields must be positive (B=%d T=%d Hq=%d G=%d d=%d d_idx=%d Bk=%d k=%d)",
+                s->B, s->T, s->Hq, s->G, s->d, s->d_idx, s->Bk, s->k);
+  if (s->Hq % s->G) return fail(MSA_ERR_INVALID_ARG, "Hq=%d is not a multiple of G=%d", s->Hq, s->G);
+  const int hg = s->Hq / s->G;
+  if (s->d != 128) return fail(MSA_ERR_UNSUPPORTED, "d=%d: only head dim 128 is supported", s->d);
+  if (s->d_idx != 64) return fail(MSA_ERR_UNSUPPORTED, "d_idx=%d: only index dim 64 is supported", s->d_idx);
+  if (s->Bk != 128) return fail(MSA_ERR_UNSUPPORTED, "Bk=%d: only 128-token blocks are supported", s->Bk);
+  if (!(hg == 1 || hg == 2 || hg == 4 || hg == 8))
+    return fail(MSA_ERR_UNSUPPORTED, "Hq/G=%d: heads per group must be 1, 2, 4 or 8", hg);
+  if (s->T % 128) return fail(MSA_ERR_UNSUPPORTED, "T=%d is not a multiple of 128", s->T);
+  if (s->T > (1 << 20)) return fail(MSA_ERR_UNSUPPORTED, "T=%d exceeds 2^20", s->T);
+  if (s->k > 64) return fail(MSA_ERR_UNSUPPORTED, "k=%d exceeds 64", s->k);
+  if ((long long)s->B * s->T > (1LL << 30)) return fail(MSA_ERR_UNSUPPORTED, "B*T too large");
+  const float sc = s->scale > 0 ? s->scale : 1.0f / sqrtf((float)s->d);
+  const float sci = s->scale_idx > 0 ? s->scale_idx : 1.0f / sqrtf((float)s->d_idx);
+  if (!(sc > 0) || !isfinite(sc) || !(sci > 0) || !isfinite(sci))
+    return fail(MSA_ERR_INVALID_ARG, "scales must be finite");
+  p->B = s->B;
+  p->T = s->T;
+  p->Hq = s->Hq;
+  p->G = s->G;
+  p->d = s->d;
+  p->E = s->d_idx;
+  p->Bk = s->Bk;
+  p->k = s->k;
+  p->hg = hg;
+  p->n = s->T / s->Bk;
+  p->scale = sc;
+  p->scale_idx = sci;
+  return MSA_OK;
+}
+
+static msa_status check_ptr(const void* ptr, const char* name, size_t align) {
+  if (!ptr) return fail(MSA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (reinterpret_cast<uintptr_t>(ptr) % align)
+    return fail(MSA_ERR_INVALID_ARG, "%s is not %zu-byte aligned", name, align);
+  return MSA_OK;
+}
+
+static msa_status check_ws(const Prob& p, int which, void* ws, size_t bytes, WsLayout* L) {
+  *L = ws_layout(p, which);
+  if (!ws) return fail(MSA_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(MSA_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (bytes < L->total)
+    return fail(MSA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", bytes, L->total);
+  return MSA_OK;
+}
+
+static msa_status check_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MSA_ERR_UNSUPPORTED, "no CUDA device");
+  int major = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (major != 10) return fail(MSA_ERR_UNSUPPORTED, "device %d has compute capability %d.x, sm_10x needed", dev, major);
+  return MSA_OK;
+}
+
+static msa_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MSA_OK;
+  cudaGetLastError();
+  return fail(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" {
+
+int32_t msa_version(void) { return (1 << 16) | 0; }
+
+const char* msa_last_error(void) { return g_err; }
+
+size_t msa_workspace_size(const msa_shape* shape, int which) {
+  Prob p;
+  if (which < MSA_WS_TOPK || which > MSA_WS_BWD) return 0;
+  if (validate(shape, &p) != MSA_OK) return 0;
+  return ws_layout(p, which).total;
+}
+
+msa_status msa_index_topk(const msa_shape* shape, const void* q_idx, const void* k_idx, int32_t* block_idx,
+                          void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Prob p;
+  WsLayout L;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_ptr(q_idx, "q_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(k_idx, "k_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(block_idx, "block_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ws(p, MSA_WS_TOPK, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_index_topk(p, q_idx, k_idx, block_idx, workspace, L, st), "index top-k launch");
+}
+
+msa_status msa_sparse_fwd(const msa_shape* shape, const void* Q, const void* K, const void* V,
+                          const int32_t* block_idx, void* O, float* LSE, void* workspace, size_t workspace_bytes,
+                          msa_stream_t stream) {
+  Prob p;
+  WsLayout L;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_ptr(Q, "Q", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(K, "K", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(V, "V", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(block_idx, "block_idx", 4)) != MSA_OK) return s;
+  if ((s = check_ptr(O, "O", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(LSE, "LSE", 4)) != MSA_OK) return s;
+  if ((s = check_ws(p, MSA_WS_FWD, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_sparse_fwd(p, Q, K, V, block_idx, O, LSE, w, L, st), "sparse forward launch");
+}
+
+msa_status msa_bwd(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
+                   float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
+                   void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Prob p;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  return fail(MSA_ERR_UNSUPPORTED, "msa_bwd: not built yet");
+}
+
+msa_status msa_check_device_status(const void* workspace, msa_stream_t stream) {
+  if (!workspace) return fail(MSA_ERR_INVALID_ARG, "workspace is NULL");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  msa_status s;
+  if ((s = cuda_status(cudaStreamSynchronize(st), "stream synchronize")) != MSA_OK) return s;
+  int word = 0;
+  if ((s = cuda_status(cudaMemcpy(&word, workspace, sizeof word, cudaMemcpyDeviceToHost), "reading error word")) !=
+      MSA_OK)
+    return s;
+  if (word == 0) return MSA_OK;
+  cudaMemset(const_cast<void*>(workspace), 0, sizeof word);
+  const int code = word / 65536, where = word % 65536;
+  return fail(MSA_ERR_DEVICE, "device error %s at site %d",
+              code == kDevTimeout ? "timeout (a bounded wait ran out)"
+                                  : (code == kDevBadIndex ? "block id out of range" : "unknown"),
+              where);
+}
+
+}  // extern "C"

@@ -1,0 +1,71 @@
+// Host-side internals shared by the MSA entry points and kernel launchers:
+// validated problem description, workspace layout, tensor-map encoding.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+// Validated, defaulted shape.
+struct Prob {
+  int B, T, Hq, G, d, E, Bk, k;  // E = d_idx
+  int hg;                        // heads per group
+  int n;                         // KV blocks = T / Bk
+  float scale, scale_idx;
+  long long BT() const { return (long long)B * T; }
+};
+
+// Workspace regions (byte offsets from the workspace base, 256-aligned).
+struct WsLayout {
+  size_t err = 0;           // int32 error word
+  size_t counters = 64;     // int32 work counters [16]
+  size_t list_count = 0;    // int32 [B*G*n]   selections per KV block
+  size_t list_off = 0;      // int32 [B*G*n+1] exclusive prefix of list_count
+  size_t list_cursor = 0;   // int32 [B*G*n]   scatter cursors
+  size_t entries = 0;       // int32 [B*G*T*k] (t << 8 | slot), grouped by list
+  size_t items = 0;         // int4  [max_items] work items (list, tile range)
+  size_t n_items = 0;       // int32 [4]       number of work items per kernel
+  size_t o_part = 0;        // bf16  [B,T,G,k,hg,d] forward partial outputs (normalised)
+  size_t lse_part = 0;      // fp32  [B,T,G,k,hg]   forward partial log-sum-exp
+  size_t drow = 0;          // fp32  [B,T,Hq]       rowsum(dO * O)
+  size_t px_part = 0;       // fp32  [B,T,G,k]      index-branch partial LSE per slot
+  size_t lse_px = 0;        // fp32  [B,T,G]        index-branch LSE over S(g,t)
+  size_t dq_part = 0;       // bf16  [B,T,G,k,hg,d] dQ partials per slot
+  size_t dqi_part = 0;      // fp32  [B,T,G,k,E]    dq_idx partials per slot
+  size_t kl_part = 0;       // fp32  [B,T,G,k]      KL partials per slot
+  size_t dki_part = 0;      // fp32  [B,G,T,E]      dk_idx per group
+  size_t total = 256;
+  int max_items = 0;
+};
+
+WsLayout ws_layout(const Prob& p, int which);
+
+// Maximum work-item count of the sparse kernels for a problem.
+int max_work_items(const Prob& p, int tiles_per_item, int rows_per_tile);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
+                 const uint32_t* box, CUtensorMapSwizzle swz);
+
+int num_sms();
+
+// Launchers (return cudaSuccess or the launch error).
+cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
+                              const WsLayout& L, cudaStream_t st);
+
+// Inverted block -> query lists and work items (rows_per_tile * tiles_per_item
+// entries per item).
+cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L,
+                            int rows_per_tile, int tiles_per_item, cudaStream_t st);
+
+cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
+                              void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st);
+
+}  // namespace msa

@@ -1,0 +1,449 @@
+// Main-branch forward of MiniMax Sparse Attention: exact causal softmax
+// attention over the selected KV blocks, with the LSE kept for the backward.
+//
+// itinai.ru "How to solve the memory problem with MiniMax Sparse Attention",
+// "Two-stage process": ordinary scaled dot-product softmax, but only over the
+// selected tokens; "Kernel optimisations": iterate over KV blocks (KV-outer)
+// and pack ceil(128 / heads-per-group) query positions x heads-per-group
+// heads into one 128 x 128 MMA. dothoosh.com "how FlashAttention cuts GPU
+// memory traffic", "Online-softmax trick": partial results (m, l, a) of
+// different KV blocks merge exactly.
+//
+// GB300 design. A work item is a run of up to 32 tiles from the inverted list
+// of one (b, g, KV block c). K_c and V_c (128 x 128 bf16 each) are staged once
+// per item by TMA; each tile gathers the Q rows of 128 / hg selecting queries
+// (hg heads each, 256 B per head row) with cp.async into a 128 x 128 K-major
+// SW128 tile. Per tile, tcgen05 computes S = Q K_c^T into TMEM; the softmax
+// warps (one TMEM lane = one (query, head) row) mask keys past the query,
+// exponentiate, write P (bf16) to shared memory; tcgen05 computes O = P V_c
+// into TMEM; the same warps write the normalised partial O and its partial
+// LSE for (query, slot). Two S and two O accumulators (512 TMEM columns) let
+// the tensor core work on one tile while the softmax warps work on the other.
+// A second kernel merges the k partials of every (query, head):
+// LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) O_s.
+//
+// Warp roles (192 threads, one CTA per SM, persistent):
+//   warp 0      item fetch, K/V TMA, Q-row gathers (cp.async, all 32 lanes)
+//   warp 1      TMEM owner, UMMA issuer (one thread)
+//   warps 2..5  softmax + partial-output epilogue
+#include "msa_internal.h"
+#include "sm100.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kQStages = 2;
+constexpr int kTile = 32768;  // 128 rows x 128 bf16, as two 64-column SW128 chunks
+constexpr int kChunk = 16384;
+constexpr int kSmemBytes = (2 + kQStages + 2) * kTile + 1024;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct FwdArgs {
+  const __nv_bfloat16* Q;
+  const int32_t* entries;
+  const int4* items;
+  const int* n_items;
+  int* counter;
+  int* err;
+  __nv_bfloat16* o_part;
+  float* lse_part;
+  int B, T, Hq, G, hg, n, k;
+  int pos_per_tile;
+  float scale_log2;  // softmax scale * log2(e)
+};
+
+struct FwdShared {
+  uint64_t it_full[2], it_empty[2];
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[kQStages], q_empty[kQStages];
+  uint64_t s_full[2], s_empty[2];
+  uint64_t p_full[2], p_free[2];
+  uint64_t o_full[2], o_empty[2];
+  int4 item[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + kTile;
+  uint8_t* sQ = smem + 2 * kTile;                // kQStages tiles
+  uint8_t* sP = smem + (2 + kQStages) * kTile;   // 2 tiles
+  __shared__ FwdShared sh;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.it_full[i], 1);
+      mbar_init(&sh.it_empty[i], 5);
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.s_empty[i], 4);
+      mbar_init(&sh.p_full[i], 4);
+      mbar_init(&sh.p_free[i], 1);
+      mbar_init(&sh.o_full[i], 1);
+      mbar_init(&sh.o_empty[i], 4);
+    }
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&sh.q_full[i], 32);
+      mbar_init(&sh.q_empty[i], 1);
+    }
+    mbar_init(&sh.kv_full, 1);
+    mbar_init(&sh.kv_empty, 1);
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort;
+  const int P = a.pos_per_tile;
+  const int n_items = *a.n_items;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&map_k);
+      tma_prefetch_desc(&map_v);
+    }
+    uint32_t tj = 0;
+    const int chunk = lane & 15;  // 16-byte chunk of a 256-byte head row
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      int4 item = make_int4(-1, 0, 0, 0);
+      if (lane == 0) {
+        if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 301)) *abort_flag = 1;
+        int id = atomicAdd(a.counter, 1);
+        if (id < n_items && !*abort_flag) item = a.items[id];
+        sh.item[s] = item;
+        mbar_arrive(&sh.it_full[s]);
+      }
+      item.x = __shfl_sync(0xffffffffu, item.x, 0);
+      item.y = __shfl_sync(0xffffffffu, item.y, 0);
+      item.z = __shfl_sync(0xffffffffu, item.z, 0);
+      if (item.x < 0) break;
+      const int bg = item.x / a.n, c = item.x % a.n;
+      const int b = bg / a.G, g = bg % a.G;
+      if (lane == 0) {
+        bool ok = mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 302);
+        if (ok) {
+          mbar_arrive_expect_tx(&sh.kv_full, 2 * kTile);
+          const int row0 = b * a.T + c * 128;
+          tma_load_3d(sK, &map_k, &sh.kv_full, 0, g, row0);
+          tma_load_3d(sK + kChunk, &map_k, &sh.kv_full, 64, g, row0);
+          tma_load_3d(sV, &map_v, &sh.kv_full, 0, g, row0);
+          tma_load_3d(sV + kChunk, &map_v, &sh.kv_full, 64, g, row0);
+        } else {
+          *abort_flag = 1;
+        }
+      }
+      __syncwarp();
+      if (*abort_flag) break;
+      const int ntiles = (item.z + P - 1) / P;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int qs = tj % kQStages;
+        if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 303)) { ok = false; break; }
+        const uint32_t dst0 = smem_u32(sQ + qs * kTile) + (chunk >> 3) * kChunk;
+        for (int i = 0; i < 64; ++i) {
+          const int r = 2 * i + (lane >> 4);
+          const int p = r / a.hg, h = r - p * a.hg;
+          const int idx = j * P + p;
+          const bool valid = idx < item.z;
+          const int t = valid ? (a.entries[item.y + idx] >> 8) : 0;
+          const __nv_bfloat16* src =
+              a.Q + ((((size_t)b * a.T + t) * a.Hq + g * a.hg + h) * 128 + chunk * 8);
+          cp_async_16_zfill(dst0 + sw128_off(r, chunk & 7), src, valid);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.q_full[qs]);
+      }
+      if (!ok) { *abort_flag = 1; break; }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc_o = make_idesc_bf16(128, 128, false, true);
+      const uint32_t k0 = smem_u32(sK), v0 = smem_u32(sV);
+      uint32_t tj = 0;
+      bool ok = true;
+      auto issue_o = [&](uint32_t u) -> bool {
+        const int sb = u & 1;
+        if (!mbar_wait(&sh.p_full[sb], (u >> 1) & 1, a.err, 311)) return false;
+        if (!mbar_wait(&sh.o_empty[sb], ((u >> 1) & 1) ^ 1, a.err, 312)) return false;
+        tc_fence_after();
+        const uint32_t p0 = smem_u32(sP + sb * kTile);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = make_sdesc(p0 + (ks >> 2) * kChunk + (ks & 3) * 32, 16, 1024, kSw128);
+          const uint64_t bd = make_sdesc(v0 + ks * 2048, kChunk, 1024, kSw128);
+          umma_bf16_ss(tmem + 256 + sb * 128, ad, bd, idesc_o, ks > 0);
+        }
+        umma_commit(&sh.o_full[sb]);
+        umma_commit(&sh.p_free[sb]);
+        return true;
+      };
+      for (int it = 0; ok; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 313)) { ok = false; break; }
+        const int4 item = sh.item[s];
+        mbar_arrive(&sh.it_empty[s]);
+        if (item.x < 0) break;
+        const int ntiles = (item.z + P - 1) / P;
+        if (!mbar_wait(&sh.kv_full, it & 1, a.err, 314)) { ok = false; break; }
+        for (int j = 0; j < ntiles && ok; ++j, ++tj) {
+          const int sb = tj & 1, qs = tj % kQStages;
+          if (!mbar_wait(&sh.q_full[qs], (tj / kQStages) & 1, a.err, 315)) { ok = false; break; }
+          if (!mbar_wait(&sh.s_empty[sb], ((tj >> 1) & 1) ^ 1, a.err, 316)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t q0 = smem_u32(sQ + qs * kTile);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * kChunk + (ks & 3) * 32;
+            umma_bf16_ss(tmem + sb * 128, make_sdesc(q0 + off, 16, 1024, kSw128),
+                         make_sdesc(k0 + off, 16, 1024, kSw128), idesc_s, ks > 0);
+          }
+          umma_commit(&sh.s_full[sb]);
+          umma_commit(&sh.q_empty[qs]);
+          if (j > 0 && !issue_o(tj - 1)) { ok = false; break; }
+        }
+        if (ok && ntiles > 0 && !issue_o(tj - 1)) ok = false;
+        umma_commit(&sh.kv_empty);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const int p_in_tile = row / a.hg, h = row - (row / a.hg) * a.hg;
+    uint32_t tj = 0;
+    bool ok = true;
+    // pending tile (softmax done, output not yet written)
+    float pm = 0.f, pl = 0.f;
+    int pentry = -1;
+    int pb = 0, pg = 0;
+    auto epilogue = [&](uint32_t u) -> bool {
+      const int sb = u & 1;
+      if (!mbar_wait(&sh.o_full[sb], (u >> 1) & 1, a.err, 321)) return false;
+      tc_fence_after();
+      float o[128];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + 256 + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(o + q * 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.o_empty[sb]);
+      if (pentry >= 0) {
+        const int t = pentry >> 8, slot = pentry & 255;
+        const float inv = 1.f / pl;
+        const size_t rowid = ((((size_t)pb * a.T + t) * a.G + pg) * a.k + slot) * a.hg + h;
+        uint4* dst = reinterpret_cast<uint4*>(a.o_part + rowid * 128);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          uint4 v;
+          v.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+          v.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+          v.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+          v.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+          dst[q] = v;
+        }
+        a.lse_part[rowid] = (pm + __log2f(pl)) * kLn2;
+      }
+      return true;
+    };
+    for (int it = 0; ok; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 322)) { ok = false; break; }
+      const int4 item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item.x < 0) break;
+      const int bg = item.x / a.n, c = item.x % a.n;
+      const int b = bg / a.G, g = bg % a.G;
+      const int ntiles = (item.z + P - 1) / P;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int sb = tj & 1;
+        const int idx = j * P + p_in_tile;
+        const int entry = idx < item.z ? a.entries[item.y + idx] : -1;
+        const int lim = entry >= 0 ? (entry >> 8) - c * 128 : -1;  // last visible key column
+        if (!mbar_wait(&sh.s_full[sb], (tj >> 1) & 1, a.err, 323)) { ok = false; break; }
+        tc_fence_after();
+        float x[128];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(x + q * 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          x[i] = (i <= lim) ? x[i] * a.scale_log2 : -INFINITY;
+          m = fmaxf(m, x[i]);
+        }
+        const float mm = (m == -INFINITY) ? 0.f : m;
+        float l = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          x[i] = fast_exp2(x[i] - mm);
+          l += x[i];
+        }
+        // P[sb] is free once the O MMA of tile tj-2 has read it
+        if (!mbar_wait(&sh.p_free[sb], ((tj >> 1) & 1) ^ 1, a.err, 324)) { ok = false; break; }
+        uint8_t* prow = sP + sb * kTile;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          uint4 v;
+          v.x = pack_bf16(x[8 * q + 0], x[8 * q + 1]);
+          v.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
+          v.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
+          v.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
+          *reinterpret_cast<uint4*>(prow + (q >> 3) * kChunk + sw128_off(row, q & 7)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_full[sb]);
+        if (j > 0 || tj > 0) {
+          if (tj > 0 && !epilogue(tj - 1)) { ok = false; break; }
+        }
+        pm = mm;
+        pl = l;
+        pentry = entry;
+        pb = b;
+        pg = g;
+      }
+      // the last tile of the item is finished at the start of the next item's
+      // first tile, or after the loop ends
+    }
+    if (ok && tj > 0) ok = epilogue(tj - 1);
+    if (!ok) *abort_flag = 1;
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// One warp per (b, t, g): merge the k partials of each of the hg heads.
+__global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const __nv_bfloat16* __restrict__ o_part,
+                                 const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ O,
+                                 float* __restrict__ LSE, int B, int T, int Hq, int G, int hg, int k) {
+  const long long rows = (long long)B * T * G;
+  const int lane = threadIdx.x & 31;
+  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int g = (int)(w % G);
+    const long long bt = w / G;
+    const int t = (int)(bt % T), b = (int)(bt / T);
+    const int32_t* sel = block_idx + (((size_t)b * G + g) * T + t) * k;
+    for (int h = 0; h < hg; ++h) {
+      float mx = -INFINITY;
+      for (int s = 0; s < k; ++s)
+        if (sel[s] >= 0) mx = fmaxf(mx, lse_part[((size_t)w * k + s) * hg + h]);
+      float z = 0.f;
+      for (int s = 0; s < k; ++s)
+        if (sel[s] >= 0) z += expf(lse_part[((size_t)w * k + s) * hg + h] - mx);
+      const float lse = mx + logf(z);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < k; ++s) {
+        if (sel[s] < 0) continue;
+        const size_t rid = ((size_t)w * k + s) * hg + h;
+        const float wgt = expf(lse_part[rid] - lse);
+        const uint2 raw = *reinterpret_cast<const uint2*>(o_part + rid * 128 + lane * 4);
+        const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
+        acc[0] += wgt * f0.x;
+        acc[1] += wgt * f0.y;
+        acc[2] += wgt * f1.x;
+        acc[3] += wgt * f1.y;
+      }
+      const size_t orow = ((size_t)b * T + t) * Hq + g * hg + h;
+      uint2 out;
+      out.x = pack_bf16(acc[0], acc[1]);
+      out.y = pack_bf16(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(O + orow * 128 + lane * 4) = out;
+      if (lane == 0) LSE[orow] = lse;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
+                              void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st) {
+  const int pos_per_tile = 128 / p.hg;
+  cudaError_t e = build_block_map(p, block_idx, ws, L, pos_per_tile, 32, st);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mk, mv;
+  const uint64_t dims[3] = {(uint64_t)p.d, (uint64_t)p.G, (uint64_t)p.BT()};
+  const uint64_t strides[2] = {(uint64_t)p.d * 2, (uint64_t)p.G * p.d * 2};
+  const uint32_t box[3] = {64, 1, 128};
+  if (!encode_tmap(&mk, const_cast<void*>(K), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  FwdArgs a;
+  a.Q = static_cast<const __nv_bfloat16*>(Q);
+  a.entries = reinterpret_cast<const int32_t*>(ws + L.entries);
+  a.items = reinterpret_cast<const int4*>(ws + L.items);
+  a.n_items = reinterpret_cast<const int*>(ws + L.n_items);
+  a.counter = reinterpret_cast<int*>(ws + L.counters) + 1;
+  a.err = reinterpret_cast<int*>(ws + L.err);
+  a.o_part = reinterpret_cast<__nv_bfloat16*>(ws + L.o_part);
+  a.lse_part = reinterpret_cast<float*>(ws + L.lse_part);
+  a.B = p.B;
+  a.T = p.T;
+  a.Hq = p.Hq;
+  a.G = p.G;
+  a.hg = p.hg;
+  a.n = p.n;
+  a.k = p.k;
+  a.pos_per_tile = pos_per_tile;
+  a.scale_log2 = p.scale * kLog2e;
+  if ((e = cudaMemsetAsync(a.counter, 0, sizeof(int), st)) != cudaSuccess) return e;
+  static bool attr = false;
+  if (!attr) {
+    if ((e = cudaFuncSetAttribute(sparse_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
+        cudaSuccess)
+      return e;
+    attr = true;
+  }
+  sparse_fwd_kernel<<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const long long rows = (long long)p.B * p.T * p.G;
+  const int grid = (int)std::min<long long>((rows * 32 + 255) / 256, 16LL * num_sms());
+  fwd_merge_kernel<<<grid, 256, 0, st>>>(block_idx, a.o_part, a.lse_part, static_cast<__nv_bfloat16*>(O), LSE, p.B,
+                                         p.T, p.Hq, p.G, p.hg, p.k);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -1,0 +1,182 @@
+/*
+ * msa.h -- C ABI of the GB300 (sm_103a) MiniMax Sparse Attention (MSA)
+ * training hot path on one GQA layer.
+ *
+ * The method (itinai.ru "How to solve the memory problem with MiniMax Sparse
+ * Attention", sections "Two-stage process", "How the indexer works" and
+ * "Training sparse attention"; dothoosh.com "how Flash-MSA cuts
+ * million-token training cost", sections "Block-sparsity mechanism",
+ * "Kernel design and execution" and "Fixing the KL-divergence bottleneck"):
+ *
+ *   1. msa_index_topk  -- index branch: every causally visible token is scored
+ *      with the group's index query against the shared index key, scores are
+ *      max-pooled over Bk-token KV blocks, and each (group, query) keeps k
+ *      blocks: its own block plus the best k-1 earlier ones.
+ *   2. msa_sparse_fwd  -- main branch: exact causal softmax attention over the
+ *      selected blocks only; writes O and the log-sum-exp kept for the backward.
+ *   3. msa_bwd         -- fused backward: dQ, dK, dV of the main branch and the
+ *      KL-alignment gradient of the index branch, whose score gradient is
+ *      p_px - p_main (index softmax over the selected tokens minus the
+ *      head-averaged, detached main softmax), giving dq_idx and dk_idx.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *   never allocates device memory. Scratch comes from the caller's workspace,
+ *   sized by msa_workspace_size() (256-byte aligned base required).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *   stream). Host-side argument checks run before anything is enqueued; on a
+ *   non-OK status nothing was launched and msa_last_error() describes why.
+ * - bf16 tensors are passed as `void*` holding IEEE bfloat16 values.
+ * - Layouts (row-major, innermost last):
+ *     Q, O, dO, dQ        [B, T, Hq, d]      bf16
+ *     K, V, dK, dV        [B, T, G, d]       bf16   (one KV head per group)
+ *     q_idx, dq_idx       [B, T, G, d_idx]   bf16
+ *     k_idx, dk_idx       [B, T, d_idx]      bf16   (shared by all groups)
+ *     block_idx           [B, G, T, k]       int32  (ascending ids, -1 padded)
+ *     LSE                 [B, T, Hq]         fp32   (natural log, scaled scores)
+ *     KL                  [B, G, T]          fp32   (one KL term per query)
+ *   Head h belongs to group h / (Hq / G).
+ * - Supported shapes (MSA_ERR_UNSUPPORTED otherwise): d = 128, d_idx = 64,
+ *   Bk = 128, Hq / G in {1, 2, 4, 8} with Hq % G == 0, T % 128 == 0,
+ *   1 <= T <= 2^20, 1 <= k <= 64, B >= 1, scale and scale_idx > 0 after
+ *   defaulting. Kernels need an sm_100-family GPU (built for sm_103a).
+ * - Device-side checks (bounded waits, block ids out of range) write an error
+ *   word in the workspace; msa_check_device_status() reads it.
+ */
+#ifndef MSA_H
+#define MSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define MSA_API __attribute__((visibility("default")))
+#else
+#define MSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *msa_stream_t;
+
+typedef enum msa_status {
+  MSA_OK = 0,
+  MSA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad enum       */
+  MSA_ERR_UNSUPPORTED = 2, /* shape outside the supported set above, or no GPU */
+  MSA_ERR_WORKSPACE = 3,   /* workspace missing, misaligned or too small      */
+  MSA_ERR_CUDA = 4,        /* a CUDA runtime call failed (see msa_last_error) */
+  MSA_ERR_DEVICE = 5       /* a kernel reported a timeout or a bad block id   */
+} msa_status;
+
+typedef struct msa_shape {
+  int32_t B;       /* batch                                                 */
+  int32_t T;       /* sequence length                                       */
+  int32_t Hq;      /* query heads                                           */
+  int32_t G;       /* GQA groups = KV heads = index queries per position    */
+  int32_t d;       /* head dim of Q/K/V                                     */
+  int32_t d_idx;   /* index dim of q_idx/k_idx                              */
+  int32_t Bk;      /* tokens per KV block                                   */
+  int32_t k;       /* blocks kept per (group, query), own block included    */
+  float scale;     /* main softmax scale; <= 0 selects 1/sqrt(d)            */
+  float scale_idx; /* index score scale; <= 0 selects 1/sqrt(d_idx)         */
+} msa_shape;
+
+/* Which entry point a workspace is sized for. */
+enum { MSA_WS_TOPK = 0, MSA_WS_FWD = 1, MSA_WS_BWD = 2 };
+
+/* Bytes of device workspace the entry point `which` needs for `shape`
+ * (0 if the shape is invalid or unsupported). A workspace sized for
+ * MSA_WS_BWD also serves the other two. */
+MSA_API size_t msa_workspace_size(const msa_shape *shape, int which);
+
+/*
+ * Index branch (itinai.ru "How the indexer works"; dothoosh.com Flash-MSA,
+ * "Block-sparsity mechanism" and "Kernel design and execution": the proxy
+ * pass accumulates no output, only scores and the running top-k).
+ *
+ * For every (b, g, t) with own block c_t = t / Bk:
+ *   s[j]  = <q_idx[b,t,g,:], k_idx[b,j,:]>            for j <= t (fp32 sums of
+ *           exact bf16 products; the positive scale_idx does not change order)
+ *   pool[c] = max_{j in block c} s[j]                  for c < c_t
+ *   block_idx[b,g,t,:] = {c_t} U top-(k-1) of pool under (score descending,
+ *           block id ascending), written in ascending order, then -1 padding.
+ * No T x T (or T x n_blocks) tensor is materialised.
+ *
+ * q_idx: [B,T,G,d_idx] bf16, k_idx: [B,T,d_idx] bf16 (both 16-byte aligned).
+ * block_idx: [B,G,T,k] int32, fully written.
+ */
+MSA_API msa_status msa_index_topk(const msa_shape *shape, const void *q_idx, const void *k_idx, int32_t *block_idx,
+                          void *workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/*
+ * Main branch forward (itinai.ru "Two-stage process": exact softmax over the
+ * selected tokens only; dothoosh.com Flash-MSA, "Kernel design and
+ * execution": keep the LSE for the backward; dothoosh.com "how FlashAttention
+ * cuts GPU memory traffic", "Online-softmax trick": the (m, l, a) merge).
+ *
+ * For head h in group g and query t, over S(g,t) = { j <= t : j / Bk listed in
+ * block_idx[b,g,t,:] }:
+ *   s_j = scale * <Q[b,t,h,:], K[b,j,g,:]>,  LSE = ln sum_j exp(s_j),
+ *   O[b,t,h,:] = sum_j exp(s_j - LSE) V[b,j,g,:].
+ * block_idx may come from msa_index_topk or from anywhere else, but every row
+ * must hold distinct ids in [0, t / Bk] in ascending order followed by -1s
+ * and must include t / Bk (violations set the device error word and the
+ * offending row's outputs are unspecified).
+ *
+ * O: [B,T,Hq,d] bf16, LSE: [B,T,Hq] fp32, both fully written.
+ */
+MSA_API msa_status msa_sparse_fwd(const msa_shape *shape, const void *Q, const void *K, const void *V,
+                          const int32_t *block_idx, void *O, float *LSE, void *workspace,
+                          size_t workspace_bytes, msa_stream_t stream);
+
+/*
+ * Fused backward (dothoosh.com Flash-MSA, "Kernel design and execution": one
+ * backward over proxy and main branch, scheduled through the inverted
+ * block -> query map; "Fixing the KL-divergence bottleneck": d KL / d s_px =
+ * p_px - p_main; itinai.ru "Training sparse attention": KL alignment to the
+ * head-averaged main softmax, gradient detached from the backbone;
+ * dothoosh.com FlashAttention page, "Training and the backward pass").
+ *
+ * Main branch, with P = exp(s - LSE) rebuilt from the saved LSE:
+ *   D = rowsum(dO * O), dP = dO V^T, dS = P (dP - D),
+ *   dQ = scale dS K, dK = scale dS^T Q, dV = P^T dO.
+ * Index branch, per (b, g, t) over S(g,t):
+ *   p_main_j = mean over the group's heads of P_h,j (detached),
+ *   p_px_j   = softmax_j(scale_idx <q_idx[b,t,g,:], k_idx[b,j,:]>),
+ *   KL[b,g,t] = sum_j p_main_j (ln p_main_j - ln p_px_j),
+ *   gs_j = kl_weight (p_px_j - p_main_j),
+ *   dq_idx[b,t,g,:] = scale_idx sum_j gs_j k_idx[b,j,:],
+ *   dk_idx[b,j,:]  += scale_idx sum_{g,t} gs_j q_idx[b,t,g,:].
+ * The loss is kl_weight * sum over rows of KL (pass 1/(B*G*T) for a mean).
+ * No KL gradient reaches Q, K, V and no dO gradient reaches q_idx, k_idx.
+ *
+ * Inputs as in msa_sparse_fwd; O and LSE are the forward's outputs for the
+ * same block_idx. Outputs dQ, dK, dV, dq_idx, dk_idx (bf16) and KL (fp32) are
+ * fully written (positions that no query selected get zero dK/dV/dk_idx).
+ */
+MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K, const void *V, const void *O,
+                   const void *dO, const float *LSE, const void *q_idx, const void *k_idx,
+                   const int32_t *block_idx, float kl_weight, void *dQ, void *dK, void *dV, void *dq_idx,
+                   void *dk_idx, float *KL, void *workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* Message describing the last non-OK status returned on this thread. */
+MSA_API const char *msa_last_error(void);
+
+/* Synchronises `stream`, then reads and clears the device error word of
+ * `workspace` (the one the last call on it used). MSA_ERR_DEVICE if a kernel
+ * gave up on a wait or met a block id out of range; msa_last_error() says
+ * which kernel and where. */
+MSA_API msa_status msa_check_device_status(const void *workspace, msa_stream_t stream);
+
+/* ABI version: (major << 16) | minor. */
+MSA_API int32_t msa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSA_H */
