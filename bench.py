@@ -1,0 +1,424 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA training hot path (index top-k -> sparse forward -> fused backward).
+
+One step = msa_index_topk + msa_sparse_fwd + msa_bwd over one batch of
+synthetic inputs already resident in HBM. Default workload: B=1, T=131072,
+Hq=32, G=8, d=128, d_idx=64, Bk=128, k=16. Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config ID] [--impl gb300|reference]
+
+--impl reference times the fp64 CPU oracle (as it stands) on a bounded sample
+of the same workload, per step, on the host cores.
+
+Multi-GPU: launched with torch.distributed.run, one process per GPU; every rank
+runs its own batch (the path shards over the batch with no collective:
+weak scaling); a barrier brackets the timed region and rank 0 reports the
+max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MSA fwd+bwd tokens/s and achieved TFLOP/s vs GB300 BF16 peak (k=16, Bk=128)"
+
+
+def n_selected(w) -> int:
+    """Selected, causally visible (query, key) pairs per (b, g) when every
+    query keeps min(k, visible) blocks: the own block's t-c*Bk+1 keys plus
+    Bk keys for each of min(k-1, c) earlier blocks."""
+    Bk = w.Bk
+    tot = 0
+    for c in range(w.n_blocks):
+        tot += Bk * (Bk + 1) // 2 + Bk * Bk * min(c, w.k - 1)
+    return tot
+
+
+def counted_flops(w):
+    """Counted FLOPs: full causal index branch + selected-block main fwd/bwd + KL bwd."""
+    ns = n_selected(w) * w.B * w.G
+    hg = w.Hq // w.G
+    idx = w.d_idx * w.B * w.G * w.T * (w.T + 1)
+    fwd = 4 * w.d * hg * ns
+    bwd = 10 * w.d * hg * ns
+    kl = 6 * w.d_idx * ns
+    return dict(index=idx, fwd=fwd, bwd=bwd + kl, total=idx + fwd + bwd + kl)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.strip().split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def traffic_record(kernel_file: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it still matches the source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f)
+    src = os.path.join(ROOT, "block_sparse_attention_scores_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    r = rec.get(kernel_file)
+    if not r or r.get("source_sha") != sha:
+        return None
+    return r
+
+
+# ----------------------------------------------------------------------------- multi-rank helpers
+def dist_max(value: float, device=None) -> float:
+    """Max of a per-rank value over all ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_workload(w, rank: int):
+    """Each rank runs its own batch: same shapes, its own seed (weak scaling)."""
+    return w.with_(seed=w.seed + 1000 * rank)
+
+
+def aggregate_tokens_per_s(w, world: int, max_ms_per_step: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's step time."""
+    return w.B * w.T * world / (max_ms_per_step * 1e-3)
+
+
+# ----------------------------------------------------------------------------- CPU oracle baseline
+def oracle_sample(w, seconds: float, seed: int = 0):
+    """Time the fp64 oracle on a bounded sample of the workload and extrapolate.
+
+    Sample: R query rows (b, g, t) drawn uniformly, run through the oracle's
+    index top-k, forward (all heads of the group) and per-query backward; plus
+    one KV block through the per-block backward (dK, dV, dk_idx), whose cost
+    scales with the number of (row, block) selections. Whole-step oracle time =
+    (B*G*T / R) * t_rows + (B*G*T*k / E) * t_block, E = selections of that block.
+    Returns (tokens_per_s, description, threads).
+    """
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    s = oracle.shape_of(w)
+    # inputs: only what the sample touches must be right, but the oracle reads
+    # whole tensors, so draw them all (seeded, same generator as the GPU arm)
+    inp = synth.make_inputs(w)
+    bi = synth.synthetic_block_idx(w)
+    hg = w.Hq // w.G
+    R = 8
+    t0 = time.perf_counter()
+    t_rows = 0.0
+    rows_done = 0
+    while True:
+        b = rng.integers(0, w.B, R)
+        g = rng.integers(0, w.G, R)
+        t = rng.integers(0, w.T, R)
+        rows = (b * w.G + g) * w.T + t
+        a = time.perf_counter()
+        oracle.index_topk(s, inp["q_idx"], inp["k_idx"], rows=rows)
+        hrows = ((b * w.T + t)[:, None] * w.Hq + (g * hg)[:, None] + np.arange(hg)[None, :]).ravel()
+        oracle.sparse_fwd(s, inp["Q"], inp["K"], inp["V"], bi, rows=hrows)
+        oracle.bwd_rows(s, *[inp[n] for n in ("Q", "K", "V", "dO", "q_idx", "k_idx")], bi, rows=rows)
+        t_rows += time.perf_counter() - a
+        rows_done += R
+        if time.perf_counter() - t0 > 0.6 * seconds:
+            break
+    c = int(rng.integers(0, w.n_blocks))
+    b0 = int(rng.integers(0, w.B))
+    a = time.perf_counter()
+    oracle.bwd_blocks(s, *[inp[n] for n in ("Q", "K", "V", "dO", "q_idx", "k_idx")], bi, blocks=[b0 * w.n_blocks + c])
+    t_block = time.perf_counter() - a
+    E = int((bi[b0] == c).sum())
+    total = (w.B * w.G * w.T / rows_done) * t_rows + (w.B * w.G * w.T * w.k / max(E, 1)) * t_block
+    desc = (f"{rows_done} random queries (b,g,t) through index top-k + forward + per-query backward, and KV block "
+            f"{c} (selected {E} times) through the per-block backward; whole step extrapolated by row and "
+            f"selection counts ({t_rows + t_block:.1f} s measured)")
+    return w.B * w.T / total, desc, oracle.num_threads()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    vals = []
+    desc, cores = "", 0
+    seconds = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        v, desc, cores = oracle_sample(w, seconds, seed=i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": w.B * w.T / value * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, args.gpus),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def config_dict(w, n):
+    return {"workload": w.name, "B": w.B, "T": w.T, "Hq": w.Hq, "G": w.G, "d": w.d, "d_idx": w.d_idx, "Bk": w.Bk,
+            "k": w.k, "global_batch": w.B * n, "seq_len": w.T, "parallelism": f"batch-sharded x{n}, no collective",
+            "l2": "inputs larger than L2 (Q and dO are 1 GiB each at T=131072)"}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, w):
+    import numpy as np
+    import torch
+
+    import block_sparse_attention_scores_gb300 as msa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, d=w.d, d_idx=w.d_idx, Bk=w.Bk, k=w.k)
+    # inputs: seeded synthetic data (each rank its own batch), built on the host once
+    ww = rank_workload(w, rank)
+    host = synth.make_inputs(ww)
+
+    def pinned(x):
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    h_in = {n: pinned(host[n]) for n in ("Q", "K", "V", "dO", "q_idx", "k_idx")}
+    d_in = {n: h_in[n].to(dev, non_blocking=False) for n in h_in}
+    ws = msa.alloc_workspace(s, msa.MSA_WS_BWD, dev)
+    bi = torch.empty((w.B, w.G, w.T, w.k), dtype=torch.int32, device=dev)
+    O = torch.empty_like(d_in["Q"])
+    LSE = torch.empty((w.B, w.T, w.Hq), dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(dQ=torch.empty(d_in["Q"].shape, **f32), dK=torch.empty(d_in["K"].shape, **f32),
+               dV=torch.empty(d_in["V"].shape, **f32), dq_idx=torch.empty(d_in["q_idx"].shape, **f32),
+               dk_idx=torch.empty(d_in["k_idx"].shape, **f32), KL=torch.empty((w.B, w.G, w.T), **f32))
+    stream = torch.cuda.current_stream(dev)
+    ev = {}
+
+    def step(d, record=False):
+        if record:
+            ev["a"].record(stream)
+        msa.msa_index_topk(s, d["q_idx"], d["k_idx"], bi, ws, stream)
+        if record:
+            ev["b"].record(stream)
+        msa.msa_sparse_fwd(s, d["Q"], d["K"], d["V"], bi, O, LSE, ws, stream)
+        if record:
+            ev["c"].record(stream)
+        msa.msa_bwd(s, d["Q"], d["K"], d["V"], O, d["dO"], LSE, d["q_idx"], d["k_idx"], bi, 1.0, out["dQ"],
+                    out["dK"], out["dV"], out["dq_idx"], out["dk_idx"], out["KL"], ws, stream)
+        if record:
+            ev["d"].record(stream)
+
+    for _ in range(args.warmup):
+        step(d_in)
+    msa.msa_check_device_status(ws, stream)
+    torch.cuda.synchronize()
+
+    # ---- device-resident timing, per-phase events inside the timed region
+    phase = {"index_topk": [], "sparse_fwd": [], "bwd": []}
+    clocks = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.5)
+    launches0 = msa.msa_kernel_launches()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    steps_ev = []
+    e0.record(stream)
+    for _ in range(args.steps):
+        ev = {k: torch.cuda.Event(enable_timing=True) for k in "abcd"}
+        step(d_in, record=True)
+        steps_ev.append(ev)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    launches = msa.msa_kernel_launches() - launches0
+    clk = clocks.stop() if clocks else None
+    total_ms = e0.elapsed_time(e1)
+    for ev in steps_ev:
+        phase["index_topk"].append(ev["a"].elapsed_time(ev["b"]))
+        phase["sparse_fwd"].append(ev["b"].elapsed_time(ev["c"]))
+        phase["bwd"].append(ev["c"].elapsed_time(ev["d"]))
+    msa.msa_check_device_status(ws, stream)
+    total_ms = dist_max(total_ms, dev)
+    ms_step = total_ms / args.steps
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    h_out = {n: torch.empty(out[n].shape, dtype=out[n].dtype, pin_memory=True) for n in out}
+    h_O = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in h_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values()) + h_O.numel() * h_O.element_size()
+    d_e2e = {n: torch.empty_like(d_in[n]) for n in d_in}
+
+    def e2e_step():
+        for n in h_in:
+            d_e2e[n].copy_(h_in[n], non_blocking=True)
+        step(d_e2e)
+        for n in out:
+            h_out[n].copy_(out[n], non_blocking=True)
+        h_O.copy_(O, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(f0.elapsed_time(f1) / args.steps, dev)
+    msa.msa_check_device_status(ws, stream)
+
+    if rank == 0:
+        fl = counted_flops(w)
+        peaks, src = measured_peaks()
+        tokens = w.B * w.T * world
+        tflops = fl["total"] / (ms_step * 1e-3) / 1e12
+        pm = {k: statistics.mean(v) for k, v in phase.items()}
+        peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+        # dominant entry point of the step
+        dom = max(pm, key=pm.get)
+        dom_flops = {"index_topk": fl["index"], "sparse_fwd": fl["fwd"], "bwd": fl["bwd"]}[dom]
+        dom_file = {"index_topk": "index_topk.cu", "sparse_fwd": "sparse_fwd.cu", "bwd": "sparse_bwd.cu"}[dom]
+        achieved = dom_flops / (pm[dom] * 1e-3) / 1e12
+        tr = traffic_record(dom_file)
+        line = {
+            "metric": METRIC, "value": aggregate_tokens_per_s(w, world, ms_step), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": config_dict(w, world),
+            "tflops": tflops, "frac_bf16_peak": tflops / peak_sus,
+            "fwd_tokens_per_s": tokens / ((pm["index_topk"] + pm["sparse_fwd"]) * 1e-3),
+            "phases_ms": pm,
+            "counted_flops_per_step": fl["total"] * world,
+            "roofline": {"kernel": f"{dom} entry point ({dom_file})", "bound": "tensor", "achieved": achieved,
+                         "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
+                         "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json)" if src == "measured"
+                         else "fallback 1.7 PFLOP/s sustained",
+                         "traffic": tr["bytes_per_launch"] if tr else None},
+            "e2e": {"value": aggregate_tokens_per_s(w, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "clocks": clk,
+            "gpu_launches": launches,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            v, desc, cores = oracle_sample(w, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", type=int, default=3, help="workload preset 0-4 (default 3: T=131072)")
+    ap.add_argument("--seq", type=int, default=0, help="override the preset's sequence length (profiling cases)")
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    w = synth.CONFIGS[args.config]
+    if args.seq:
+        w = w.with_(T=args.seq, name=f"{w.name.split('_t')[0]}_t{args.seq}_{w.name.split('_', 3)[-1]}")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

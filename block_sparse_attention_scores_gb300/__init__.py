@@ -31,7 +31,7 @@ MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUD
 MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD = 0, 1, 2
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
-            "msa_check_device_status", "msa_version")
+            "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version")
 
 
 class MsaError(RuntimeError):
@@ -88,6 +88,9 @@ def load_library():
     lib.msa_check_device_status.argtypes = [P, P]
     lib.msa_check_device_status.restype = ctypes.c_int
     lib.msa_version.restype = ctypes.c_int32
+    lib.msa_kernel_launches.restype = ctypes.c_int64
+    lib.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_int32, P]
+    lib.msa_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -131,6 +134,11 @@ def msa_version() -> int:
     return load_library().msa_version()
 
 
+def msa_kernel_launches() -> int:
+    """Kernels the library has launched in this process so far."""
+    return int(load_library().msa_kernel_launches())
+
+
 def msa_workspace_size(shape, which: int) -> int:
     return int(load_library().msa_workspace_size(ctypes.byref(_shape(shape)), which))
 
@@ -154,6 +162,10 @@ def msa_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, 
                                   _ptr(LSE), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), float(kl_weight), _ptr(dQ),
                                   _ptr(dK), _ptr(dV), _ptr(dq_idx), _ptr(dk_idx), _ptr(KL), _ptr(workspace), wb,
                                   _stream(stream)))
+
+
+def msa_selftest_wait_timeout(workspace, limit_us: int, stream=None) -> None:
+    _check(load_library().msa_selftest_wait_timeout(_ptr(workspace), int(limit_us), _stream(stream)))
 
 
 def msa_check_device_status(workspace, stream=None) -> None:
@@ -192,13 +204,14 @@ def sparse_fwd(shape: Shape, Q, K, V, block_idx, workspace=None, stream=None):
 
 
 def bwd(shape: Shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight=1.0, workspace=None, stream=None):
-    """Allocate the gradients and KL and run msa_bwd. Returns a dict."""
+    """Allocate the fp32 gradients and KL and run msa_bwd. Returns a dict."""
     import torch
 
     ws = workspace if workspace is not None else alloc_workspace(shape, MSA_WS_BWD, Q.device)
-    out = dict(dQ=torch.empty_like(Q), dK=torch.empty_like(K), dV=torch.empty_like(V), dq_idx=torch.empty_like(q_idx),
-               dk_idx=torch.empty_like(k_idx),
-               KL=torch.empty((shape.B, shape.G, shape.T), dtype=torch.float32, device=Q.device))
+    f32 = dict(dtype=torch.float32, device=Q.device)
+    out = dict(dQ=torch.empty(Q.shape, **f32), dK=torch.empty(K.shape, **f32), dV=torch.empty(V.shape, **f32),
+               dq_idx=torch.empty(q_idx.shape, **f32), dk_idx=torch.empty(k_idx.shape, **f32),
+               KL=torch.empty((shape.B, shape.G, shape.T), **f32))
     msa_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, out["dQ"], out["dK"], out["dV"],
             out["dq_idx"], out["dk_idx"], out["KL"], ws, stream)
     return out

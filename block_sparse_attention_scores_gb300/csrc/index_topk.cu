@@ -270,6 +270,7 @@ cudaError_t launch_cap(const Prob& p, const TopkArgs& args, const CUtensorMap& m
   if (e != cudaSuccess) return e;
   const int grid = min(args.num_items, 2 * num_sms());
   kern<<<grid, kThreads, kSmemBytes, st>>>(args, mq, mk);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
+
 #include "msa_internal.h"
 #include "sm100.cuh"
 
@@ -19,6 +21,10 @@ static msa_status fail(msa_status s, const char* fmt, ...) {
   va_end(ap);
   return s;
 }
+
+static std::atomic<long long> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -184,6 +190,8 @@ extern "C" {
 
 int32_t msa_version(void) { return (1 << 16) | 0; }
 
+int64_t msa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
 const char* msa_last_error(void) { return g_err; }
 
 size_t msa_workspace_size(const msa_shape* shape, int which) {
@@ -233,12 +241,39 @@ msa_status msa_sparse_fwd(const msa_shape* shape, const void* Q, const void* K, 
 
 msa_status msa_bwd(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
                    const void* dO, const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
-                   float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
+                   float kl_weight, float* dQ, float* dK, float* dV, float* dq_idx, float* dk_idx, float* KL,
                    void* workspace, size_t workspace_bytes, msa_stream_t stream) {
   Prob p;
+  WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
-  return fail(MSA_ERR_UNSUPPORTED, "msa_bwd: not built yet");
+  const void* in16[] = {Q, K, V, O, dO, q_idx, k_idx, dQ, dK, dV, dq_idx, dk_idx};
+  const char* names16[] = {"Q", "K", "V", "O", "dO", "q_idx", "k_idx", "dQ", "dK", "dV", "dq_idx", "dk_idx"};
+  for (int i = 0; i < 12; ++i)
+    if ((s = check_ptr(in16[i], names16[i], 16)) != MSA_OK) return s;
+  if ((s = check_ptr(LSE, "LSE", 4)) != MSA_OK) return s;
+  if ((s = check_ptr(block_idx, "block_idx", 4)) != MSA_OK) return s;
+  if ((s = check_ptr(KL, "KL", 4)) != MSA_OK) return s;
+  if (!isfinite(kl_weight)) return fail(MSA_ERR_INVALID_ARG, "kl_weight must be finite");
+  if ((s = check_ws(p, MSA_WS_BWD, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_bwd(p, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, dK, dV, dq_idx,
+                                dk_idx, KL, w, L, st),
+                     "backward launch");
+}
+
+msa_status msa_selftest_wait_timeout(void* workspace, int32_t limit_us, msa_stream_t stream) {
+  msa_status s;
+  if ((s = check_ptr(workspace, "workspace", 256)) != MSA_OK) return s;
+  if (limit_us < 1 || limit_us > 1000000) return fail(MSA_ERR_INVALID_ARG, "limit_us=%d outside [1, 1e6]", limit_us);
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if ((s = cuda_status(cudaMemsetAsync(workspace, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_selftest_wait_timeout(static_cast<int*>(workspace), (long long)limit_us * 1000, st),
+                     "self-test launch");
 }
 
 msa_status msa_check_device_status(const void* workspace, msa_stream_t stream) {

@@ -56,6 +56,9 @@ bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, c
 
 int num_sms();
 
+// Count of kernels launched by the library (msa_kernel_launches).
+void count_launches(int n);
+
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
                               const WsLayout& L, cudaStream_t st);
@@ -67,5 +70,12 @@ cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws
 
 cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
                               void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st);
+
+cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                       const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
+                       float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
+                       uint8_t* ws, const WsLayout& L, cudaStream_t st);
+
+cudaError_t launch_selftest_wait_timeout(int* err, long long limit_ns, cudaStream_t st);
 
 }  // namespace msa

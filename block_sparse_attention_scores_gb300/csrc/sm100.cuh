@@ -21,6 +21,7 @@ enum : int {
   kDevOk = 0,
   kDevTimeout = 1,   // an mbarrier wait ran past kWaitLimitNs
   kDevBadIndex = 2,  // a block index out of range reached a kernel
+  kDevSmemAlign = 3, // dynamic shared memory not 1024-byte aligned
 };
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per wait
 
@@ -68,27 +69,37 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete. Bounded: false on timeout.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int where) {
+// Wait for the phase with the given parity to complete. Bounded: false on
+// timeout (after limit_ns), with the site recorded in the error word.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int where,
+                                         unsigned long long limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_test(a, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_test(a, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+    if ((i & 255u) == 0 && global_ns() - t0 > limit_ns) {
       dev_fail(err, kDevTimeout, where);
       return false;
     }
   }
 }
 
+// Bounded rendezvous of the warps that share `bar` (initialised with one
+// arrival per warp). Every warp must call it the same number of times; `phase`
+// is per-thread state starting at 0. Returns false on timeout.
+__device__ __forceinline__ bool warps_sync(uint64_t* bar, uint32_t& phase, int* err, int where) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait(bar, phase, err, where);
+  phase ^= 1u;
+  __syncwarp();
+  return ok;
+}
+
 // ------------------------------------------------------------------ proxies
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void named_barrier(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ------------------------------------------------------------------ TMA

@@ -1,0 +1,948 @@
+// Fused backward of MiniMax Sparse Attention: main-branch dQ/dK/dV and the
+// KL-alignment gradient of the index branch in one pass over the selected
+// blocks.
+//
+// dothoosh.com "how Flash-MSA cuts million-token training cost", "Kernel
+// design and execution": the backward fuses proxy and main attention because
+// the proxy's training signal needs both distributions at once, and inverting
+// the block-index map schedules the query chunks of each sparse KV block so
+// the block is reused from shared memory; "Fixing the KL-divergence
+// bottleneck": d KL / d s_px = p_px - p_main, so no full KL distribution is
+// materialised. itinai.ru "How to solve the memory problem with MiniMax
+// Sparse Attention", "Training sparse attention": the teacher is the main
+// softmax averaged over the group's heads, detached from the backbone.
+// dothoosh.com "how FlashAttention cuts GPU memory traffic", "Training and the
+// backward pass": P is rebuilt from the saved LSE; dV += P^T dO, dP = dO V^T.
+//
+// Kernels, in launch order:
+//   drow_kernel       D[b,t,h] = rowsum(dO * O)
+//   px_stats_kernel   index-branch log-sum-exp over S(g,t), per (query, slot):
+//                     tcgen05 S_px = q_idx rows x k_idx block^T, one query
+//                     per TMEM lane, 128 queries per tile
+//   px_merge_kernel   lse_px[b,t,g] from the k partials
+//   bwd_kernel        per KV block c of (b, g), over the tiles of queries that
+//                     selected it (keys on TMEM lanes, 64 (query, head) rows
+//                     per tile):
+//                       S^T = K_c Q^T, dP^T = V_c dO^T, X^T = KI_c QI^T
+//                       P = exp(s - LSE), dS = P (dP - D), p_main = head mean,
+//                       p_px = exp(x - lse_px), gs = w (p_px - p_main), KL terms
+//                       dV += P^T dO, dK += dS^T Q, dk_idx += gs^T QI (TMEM,
+//                       across all tiles of the block), dQ^T = K_c^T dS^T and
+//                       dq_idx^T = KI_c^T gs^T (per tile, to slot partials)
+//   bwd_merge_kernel  dQ, dq_idx, KL = sums of the slot partials
+//   dki_merge_kernel  dk_idx = sum over groups
+#include "msa_internal.h"
+#include "sm100.cuh"
+
+namespace msa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ void decode_list(int l, int n, int G, int& b, int& g, int& c) {
+  const int bg = l / n;
+  c = l - bg * n;
+  b = bg / G;
+  g = bg - b * G;
+}
+
+// ============================================================================ D
+__global__ void drow_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+                            float* __restrict__ drow, long long rows) {
+  const int lane = threadIdx.x & 31;
+  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const uint2 a = *reinterpret_cast<const uint2*>(O + r * 128 + lane * 4);
+    const uint2 b = *reinterpret_cast<const uint2*>(dO + r * 128 + lane * 4);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+    const float2 a0 = __bfloat1622float2(pa[0]), a1 = __bfloat1622float2(pa[1]);
+    const float2 b0 = __bfloat1622float2(pb[0]), b1 = __bfloat1622float2(pb[1]);
+    float s = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) drow[r] = s;
+  }
+}
+
+// ============================================================================ px stats
+// One CTA per SM, persistent over whole lists. 128 queries per tile.
+constexpr int kPxThreads = 192;
+constexpr int kPxTile = 16384;  // 128 rows x 64 bf16
+constexpr int kPxSmem = 3 * kPxTile + 1024;
+
+struct PxArgs {
+  const __nv_bfloat16* q_idx;
+  const int32_t* entries;
+  const int4* items;
+  const int* n_items;
+  int* counter;
+  int* err;
+  float* px_part;  // [B,T,G,k]
+  int B, T, G, n, k;
+  float scale_log2;
+};
+
+struct PxShared {
+  uint64_t it_full[2], it_empty[2];
+  uint64_t kv_full, kv_empty;
+  uint64_t q_full[2], q_empty[2];
+  uint64_t s_full[2], s_empty[2];
+  int4 item[2];
+  int tile_t[128];  // producer scratch: query of each tile position
+  uint32_t tmem_base;
+  int abort;
+};
+
+__global__ void __launch_bounds__(kPxThreads, 1)
+    px_stats_kernel(PxArgs a, const __grid_constant__ CUtensorMap map_ki) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sKI = smem;
+  uint8_t* sQ = smem + kPxTile;  // 2 tiles
+  __shared__ PxShared sh;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.it_full[i], 1);
+      mbar_init(&sh.it_empty[i], 5);
+      mbar_init(&sh.q_full[i], 32);
+      mbar_init(&sh.q_empty[i], 1);
+      mbar_init(&sh.s_full[i], 1);
+      mbar_init(&sh.s_empty[i], 4);
+    }
+    mbar_init(&sh.kv_full, 1);
+    mbar_init(&sh.kv_empty, 1);
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort;
+  const int n_items = *a.n_items;
+
+  if (warp == 0) {
+    uint32_t tj = 0;
+    const int chunk = lane & 7;
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      int4 item = make_int4(-1, 0, 0, 0);
+      if (lane == 0) {
+        if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 401)) *abort_flag = 1;
+        const int id = atomicAdd(a.counter, 1);
+        if (id < n_items && !*abort_flag) item = a.items[id];
+        sh.item[s] = item;
+        mbar_arrive(&sh.it_full[s]);
+      }
+      item.x = __shfl_sync(0xffffffffu, item.x, 0);
+      item.y = __shfl_sync(0xffffffffu, item.y, 0);
+      item.z = __shfl_sync(0xffffffffu, item.z, 0);
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      if (lane == 0) {
+        if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 402)) {
+          mbar_arrive_expect_tx(&sh.kv_full, kPxTile);
+          tma_load_2d(sKI, &map_ki, &sh.kv_full, 0, b * a.T + c * 128);
+        } else {
+          *abort_flag = 1;
+        }
+      }
+      __syncwarp();
+      if (*abort_flag) break;
+      const int ntiles = (item.z + 127) / 128;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int qs = tj & 1;
+        if (!mbar_wait(&sh.q_empty[qs], ((tj >> 1) & 1) ^ 1, a.err, 403)) { ok = false; break; }
+        const uint32_t dst0 = smem_u32(sQ + qs * kPxTile);
+        for (int p = lane; p < 128; p += 32) {
+          const int idx = j * 128 + p;
+          sh.tile_t[p] = idx < item.z ? (a.entries[item.y + idx] >> 8) : -1;
+        }
+        __syncwarp();
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+          const int r = 4 * i + (lane >> 3);
+          const int tq = sh.tile_t[r];
+          const bool valid = tq >= 0;
+          const __nv_bfloat16* src = a.q_idx + ((((size_t)b * a.T + (valid ? tq : 0)) * a.G + g) * 64 + chunk * 8);
+          cp_async_16_zfill(dst0 + sw128_off(r, chunk), src, valid);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.q_full[qs]);
+        __syncwarp();
+      }
+      if (!ok) { *abort_flag = 1; break; }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+      const uint32_t k0 = smem_u32(sKI);
+      uint32_t tj = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 411)) { ok = false; break; }
+        const int4 item = sh.item[s];
+        mbar_arrive(&sh.it_empty[s]);
+        if (item.x < 0) break;
+        const int ntiles = (item.z + 127) / 128;
+        if (!mbar_wait(&sh.kv_full, it & 1, a.err, 412)) { ok = false; break; }
+        for (int j = 0; j < ntiles; ++j, ++tj) {
+          const int sb = tj & 1;
+          if (!mbar_wait(&sh.q_full[sb], (tj >> 1) & 1, a.err, 413)) { ok = false; break; }
+          if (!mbar_wait(&sh.s_empty[sb], ((tj >> 1) & 1) ^ 1, a.err, 414)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t q0 = smem_u32(sQ + sb * kPxTile);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16_ss(tmem + sb * 128, make_sdesc(q0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(k0 + ks * 32, 16, 1024, kSw128), idesc, ks > 0);
+          umma_commit(&sh.s_full[sb]);
+          umma_commit(&sh.q_empty[sb]);
+        }
+        umma_commit(&sh.kv_empty);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint32_t tj = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 421)) { ok = false; break; }
+      const int4 item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      const int ntiles = (item.z + 127) / 128;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int sb = tj & 1;
+        const int idx = j * 128 + row;
+        const int entry = idx < item.z ? a.entries[item.y + idx] : -1;
+        const int lim = entry >= 0 ? (entry >> 8) - c * 128 : -1;
+        if (!mbar_wait(&sh.s_full[sb], (tj >> 1) & 1, a.err, 422)) { ok = false; break; }
+        tc_fence_after();
+        float x[128];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          tmem_ld32(tmem + lane_off + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(x + q * 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
+        float m = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) {
+          x[i] = (i <= lim) ? x[i] * a.scale_log2 : -INFINITY;
+          m = fmaxf(m, x[i]);
+        }
+        const float mm = (m == -INFINITY) ? 0.f : m;
+        float l = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; ++i) l += fast_exp2(x[i] - mm);
+        if (entry >= 0) {
+          const int t = entry >> 8, slot = entry & 255;
+          a.px_part[(((size_t)b * a.T + t) * a.G + g) * a.k + slot] = (mm + __log2f(l)) * kLn2;
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
+// lse_px[b,t,g] = ln sum_s exp(px_part[b,t,g,s]) over the valid slots.
+__global__ void px_merge_kernel(const int32_t* __restrict__ block_idx, const float* __restrict__ px_part,
+                                float* __restrict__ lse_px, int B, int T, int G, int k) {
+  const long long rows = (long long)B * T * G;
+  for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows;
+       r += (long long)gridDim.x * blockDim.x) {
+    const int g = (int)(r % G);
+    const long long bt = r / G;
+    const int t = (int)(bt % T), b = (int)(bt / T);
+    const int32_t* sel = block_idx + (((size_t)b * G + g) * T + t) * k;
+    float mx = -INFINITY;
+    for (int s = 0; s < k; ++s)
+      if (sel[s] >= 0) mx = fmaxf(mx, px_part[r * k + s]);
+    float z = 0.f;
+    for (int s = 0; s < k; ++s)
+      if (sel[s] >= 0) z += expf(px_part[r * k + s] - mx);
+    lse_px[r] = mx + logf(z);
+  }
+}
+
+// ============================================================================ fused backward
+constexpr int kBwdThreads = 192;
+constexpr int kRows = 64;                // (query, head) rows per tile
+constexpr int kKV = 32768;               // 128 keys x 128 d
+constexpr int kKIb = 16384;              // 128 keys x 64
+constexpr int kRowTile = kRows * 256;    // 64 rows x 128 d  (16 KB)
+constexpr int kRowChunk = kRows * 128;   // one 64-column chunk of it (8 KB)
+constexpr int kQIb = kRows * 128;        // 64 rows x 64     (8 KB)
+constexpr int kKeyRows = 128 * 128;      // 128 keys x 64 bf16 (16 KB)
+constexpr int kGather = 2 * kRowTile + kQIb;  // Q, dO, QI per tile
+// smem map (the dynamic base is 1024-aligned; checked at entry)
+constexpr int oK = 0, oV = kKV, oKI = 2 * kKV;
+constexpr int oG = 2 * kKV + kKIb;             // 2 gather buffers
+constexpr int oPT = oG + 2 * kGather;          // P^T (bf16 high part)
+constexpr int oPL = oPT + kKeyRows;            // P^T low part: P - bf16(P), for an exact-enough dV
+constexpr int oDST = oPL + kKeyRows;           // dS^T
+constexpr int oGST = oDST + kKeyRows;          // gs^T
+constexpr int oSh = oGST + kKeyRows;           // BwdShared
+// TMEM columns
+constexpr uint32_t cS = 0, cDP = 64, cX = 128, cDV = 192, cDK = 320, cKI = 448;
+
+struct RowMeta {
+  float lse2[kRows];   // LSE * log2(e)
+  float dval[kRows];   // D
+  float lsepx2[kRows]; // lse_px * log2(e) (per row of the query)
+  int entry[kRows];    // (t << 8 | slot), -1 for padding rows
+};
+
+struct BwdArgs {
+  const __nv_bfloat16* Q;
+  const __nv_bfloat16* dO;
+  const __nv_bfloat16* q_idx;
+  const float* LSE;
+  const float* drow;
+  const float* lse_px;
+  const int32_t* entries;
+  const int4* items;
+  const int* n_items;
+  int* counter;
+  int* err;
+  float* dK;
+  float* dV;
+  __nv_bfloat16* dq_part;  // [B,T,G,k,hg,d]
+  float* dqi_part;         // [B,T,G,k,E]
+  float* kl_part;          // [B,T,G,k]
+  float* dki_part;         // [B,G,T,E]
+  int B, T, Hq, G, hg, n, k;
+  float scale_log2, scale, scale_idx_log2, scale_idx, kl_weight;
+};
+
+struct BwdShared {
+  uint64_t it_full[2], it_empty[2];
+  uint64_t kv_full, kv_empty;
+  uint64_t g_full[2], g_empty[2];
+  uint64_t ph1_full, ph1_done, ph2_full, ph2_done;
+  uint64_t acc_free;
+  uint64_t epi_sync;  // rendezvous of the 4 epilogue warps
+  RowMeta meta[2];
+  float kl_acc[kRows];  // per-query KL partial of the current tile (summed over the 4 warps)
+  int4 item[2];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kBwdSmem = oSh + (int)sizeof(BwdShared);
+static_assert(kBwdSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
+
+template <int HG>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_kernel(BwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+               const __grid_constant__ CUtensorMap map_ki) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // uniform for the block: nothing started yet
+    if (threadIdx.x == 0) dev_fail(a.err, kDevSmemAlign, 500);
+    return;
+  }
+  BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + oSh);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRows; ++i) sh.kl_acc[i] = 0.f;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.it_full[i], 1);
+      mbar_init(&sh.it_empty[i], 5);
+      mbar_init(&sh.g_full[i], 32);
+      mbar_init(&sh.g_empty[i], 1 + 4);  // MMA commit + epilogue warps (meta)
+    }
+    mbar_init(&sh.kv_full, 1);
+    mbar_init(&sh.kv_empty, 1);
+    mbar_init(&sh.ph1_full, 1);
+    mbar_init(&sh.ph1_done, 4);
+    mbar_init(&sh.ph2_full, 1);
+    mbar_init(&sh.ph2_done, 4);
+    mbar_init(&sh.acc_free, 4);
+    mbar_init(&sh.epi_sync, 4);
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort;
+  const int n_items = *a.n_items;
+  constexpr int hg = HG;          // heads per group (compile time: static register indexing)
+  constexpr int npos = kRows / hg;  // queries per tile
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t tj = 0;
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      int4 item = make_int4(-1, 0, 0, 0);
+      if (lane == 0) {
+        if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 501)) *abort_flag = 1;
+        const int id = atomicAdd(a.counter, 1);
+        if (id < n_items && !*abort_flag) item = a.items[id];
+        sh.item[s] = item;
+        mbar_arrive(&sh.it_full[s]);
+      }
+      item.x = __shfl_sync(0xffffffffu, item.x, 0);
+      item.y = __shfl_sync(0xffffffffu, item.y, 0);
+      item.z = __shfl_sync(0xffffffffu, item.z, 0);
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      if (lane == 0) {
+        if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 502)) {
+          mbar_arrive_expect_tx(&sh.kv_full, 2 * kKV + kKIb);
+          const int row0 = b * a.T + c * 128;
+          tma_load_3d(smem + oK, &map_k, &sh.kv_full, 0, g, row0);
+          tma_load_3d(smem + oK + kKV / 2, &map_k, &sh.kv_full, 64, g, row0);
+          tma_load_3d(smem + oV, &map_v, &sh.kv_full, 0, g, row0);
+          tma_load_3d(smem + oV + kKV / 2, &map_v, &sh.kv_full, 64, g, row0);
+          tma_load_2d(smem + oKI, &map_ki, &sh.kv_full, 0, row0);
+        } else {
+          *abort_flag = 1;
+        }
+      }
+      __syncwarp();
+      if (*abort_flag) break;
+      const int ntiles = (item.z + npos - 1) / npos;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int gb = tj & 1;
+        if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503)) { ok = false; break; }
+        uint8_t* buf = smem + oG + gb * kGather;
+        const uint32_t q0 = smem_u32(buf), do0 = q0 + kRowTile, qi0 = q0 + 2 * kRowTile;
+        // row metadata first (independent loads), then the gathers read it
+        RowMeta& m = sh.meta[gb];
+        for (int r = lane; r < kRows; r += 32) {
+          const int p = r / hg, h = r - p * hg;
+          const int idx = j * npos + p;
+          if (idx < item.z) {
+            const int e = a.entries[item.y + idx];
+            const int t = e >> 8;
+            const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + h;
+            m.entry[r] = e;
+            m.lse2[r] = a.LSE[hr] * kLog2e;
+            m.dval[r] = a.drow[hr];
+            m.lsepx2[r] = a.lse_px[((size_t)b * a.T + t) * a.G + g] * kLog2e;
+          } else {
+            m.entry[r] = -1;
+            m.lse2[r] = 0.f;
+            m.dval[r] = 0.f;
+            m.lsepx2[r] = 0.f;
+          }
+        }
+        __syncwarp();
+        // Q and dO rows: 64 rows x 16 chunks each; lane -> (row half, chunk)
+        const int chunk = lane & 15;
+#pragma unroll 4
+        for (int i = 0; i < 32; ++i) {
+          const int r = 2 * i + (lane >> 4);
+          const int h = r % hg;
+          const int e = m.entry[r];
+          const bool valid = e >= 0;
+          const int t = valid ? (e >> 8) : 0;
+          const size_t off = (((size_t)b * a.T + t) * a.Hq + g * hg + h) * 128 + chunk * 8;
+          const uint32_t d = (chunk >> 3) * kRowChunk + sw128_off(r, chunk & 7);
+          cp_async_16_zfill(q0 + d, a.Q + off, valid);
+          cp_async_16_zfill(do0 + d, a.dO + off, valid);
+        }
+        // q_idx rows (replicated over the heads of a query): 64 rows x 8 chunks
+#pragma unroll 4
+        for (int i = 0; i < 16; ++i) {
+          const int r = 4 * i + (lane >> 3), ch = lane & 7;
+          const int e = m.entry[r];
+          const bool valid = e >= 0;
+          const int t = valid ? (e >> 8) : 0;
+          cp_async_16_zfill(qi0 + sw128_off(r, ch), a.q_idx + ((((size_t)b * a.T + t) * a.G + g) * 64 + ch * 8),
+                            valid);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.g_full[gb]);
+        __syncwarp();
+      }
+      if (!ok) { *abort_flag = 1; break; }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_sT = make_idesc_bf16(128, 64, false, false);   // K-major x K-major, N=64
+      constexpr uint32_t id_acc = make_idesc_bf16(128, 128, false, true);  // K-major A, MN-major B, N=128
+      constexpr uint32_t id_tr = make_idesc_bf16(128, 64, true, true);     // MN-major A and B, N=64
+      constexpr uint32_t id_ki = make_idesc_bf16(128, 64, false, true);    // K-major A, MN-major B, N=64
+      const uint32_t k0 = smem_u32(smem + oK), v0 = smem_u32(smem + oV), ki0 = smem_u32(smem + oKI);
+      const uint32_t pt0 = smem_u32(smem + oPT), pl0 = smem_u32(smem + oPL);
+      const uint32_t dst0 = smem_u32(smem + oDST), gst0 = smem_u32(smem + oGST);
+      uint32_t tj = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 511)) { ok = false; break; }
+        const int4 item = sh.item[s];
+        mbar_arrive(&sh.it_empty[s]);
+        if (item.x < 0) break;
+        const int ntiles = (item.z + npos - 1) / npos;
+        if (!mbar_wait(&sh.kv_full, it & 1, a.err, 512)) { ok = false; break; }
+        for (int j = 0; j < ntiles; ++j, ++tj) {
+          const int gb = tj & 1;
+          if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 513)) { ok = false; break; }
+          // the previous tile's epilogue has read dQ^T / dq_idx^T out of TMEM
+          if (!mbar_wait(&sh.ph2_done, (tj & 1) ^ 1, a.err, 514)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t g0 = smem_u32(smem + oG + gb * kGather);
+          const uint32_t gq = g0, gdo = g0 + kRowTile, gqi = g0 + 2 * kRowTile;
+          // phase 1: S^T = K Q^T, dP^T = V dO^T, X^T = KI QI^T
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = (ks >> 2) * (kKV / 2) + (ks & 3) * 32;
+            const uint32_t bo = (ks >> 2) * kRowChunk + (ks & 3) * 32;
+            umma_bf16_ss(tmem + cS, make_sdesc(k0 + ao, 16, 1024, kSw128), make_sdesc(gq + bo, 16, 1024, kSw128),
+                         id_sT, ks > 0);
+            umma_bf16_ss(tmem + cDP, make_sdesc(v0 + ao, 16, 1024, kSw128),
+                         make_sdesc(gdo + bo, 16, 1024, kSw128), id_sT, ks > 0);
+          }
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(gqi + ks * 32, 16, 1024, kSw128), id_sT, ks > 0);
+          umma_commit(&sh.ph1_full);
+          // phase 2 once P^T, dS^T, gs^T are in shared memory
+          if (!mbar_wait(&sh.ph1_done, tj & 1, a.err, 515)) { ok = false; break; }
+          if (j == 0 && !mbar_wait(&sh.acc_free, (it & 1) ^ 1, a.err, 516)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t acc = (j > 0) ? 1u : 0u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            // dV += P^T dO, dK += dS^T Q   (K = 64 rows, 16 per step)
+            umma_bf16_ss(tmem + cDV, make_sdesc(pt0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(gdo + ks * 2048, kRowChunk, 1024, kSw128), id_acc, acc | (ks > 0));
+            umma_bf16_ss(tmem + cDV, make_sdesc(pl0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(gdo + ks * 2048, kRowChunk, 1024, kSw128), id_acc, 1u);
+            umma_bf16_ss(tmem + cDK, make_sdesc(dst0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(gq + ks * 2048, kRowChunk, 1024, kSw128), id_acc, acc | (ks > 0));
+            // dk_idx += gs^T QI
+            umma_bf16_ss(tmem + cKI, make_sdesc(gst0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(gqi + ks * 2048, 16, 1024, kSw128), id_ki, acc | (ks > 0));
+          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            // dQ^T = K^T dS^T, dq_idx^T = KI^T gs^T   (K = 128 keys, 16 per step)
+            umma_bf16_ss(tmem + cS, make_sdesc(k0 + ks * 2048, kKV / 2, 1024, kSw128),
+                         make_sdesc(dst0 + ks * 2048, 16, 1024, kSw128), id_tr, ks > 0);
+            umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 2048, kKIb, 1024, kSw128),
+                         make_sdesc(gst0 + ks * 2048, 16, 1024, kSw128), id_tr, ks > 0);
+          }
+          umma_commit(&sh.ph2_full);
+          umma_commit(&sh.g_empty[gb]);
+        }
+        umma_commit(&sh.kv_empty);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (thread = key / d lane)
+    const int quarter = warp & 3;
+    const int kk = quarter * 32 + lane;  // TMEM lane: key in block c (phase 1), d (dQ^T), e (dq_idx^T)
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    uint32_t tj = 0, sync_phase = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 521)) { ok = false; break; }
+      const int4 item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      const int key = c * 128 + kk;
+      const int ntiles = (item.z + npos - 1) / npos;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int gb = tj & 1;
+        const RowMeta& m = sh.meta[gb];
+        if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 522)) { ok = false; break; }
+        if (!mbar_wait(&sh.ph1_full, tj & 1, a.err, 523)) { ok = false; break; }
+        tc_fence_after();
+        // ---- phase-1 epilogue: 64 rows, 16 at a time
+        for (int q = 0; q < 4; ++q) {
+          float sv[16], dp[16], xv[16];
+          tmem_ld16(tmem + lane_off + cS + q * 16, sv);
+          tmem_ld16(tmem + lane_off + cDP + q * 16, dp);
+          tmem_ld16(tmem + lane_off + cX + q * 16, xv);
+          tmem_wait_ld();
+          float pv[16], dsv[16], gv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int r = q * 16 + i;
+            const int e = m.entry[r];
+            const bool vis = e >= 0 && key <= (e >> 8);
+            pv[i] = vis ? fast_exp2(sv[i] * a.scale_log2 - m.lse2[r]) : 0.f;
+            dsv[i] = pv[i] * (dp[i] - m.dval[r]) * a.scale;
+          }
+          // index branch: one value per query (the first head row of each query)
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            gv[i] = 0.f;
+            xv[i] = xv[i] * a.scale_idx_log2;  // log2-domain index score
+          }
+#pragma unroll
+          for (int i0 = 0; i0 < 16; i0 += hg) {
+            const int r = q * 16 + i0;
+            const int e = m.entry[r];
+            const bool vis = e >= 0 && key <= (e >> 8);
+            float pm = 0.f;
+#pragma unroll
+            for (int h = 0; h < hg; ++h) pm += pv[i0 + h];
+            pm *= 1.f / (float)hg;
+            const float lpx2 = xv[i0] - m.lsepx2[r];  // log2 p_px
+            const float ppx = vis ? fast_exp2(lpx2) : 0.f;
+            gv[i0] = vis ? a.kl_weight * (ppx - pm) * a.scale_idx : 0.f;
+            float term = 0.f;
+            if (vis && pm > 0.f) term = pm * (__log2f(pm) - lpx2) * kLn2;
+            // reduce over the 128 keys: warp shuffle, then across the 4 warps
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
+            if (lane == 0) atomicAdd(&sh.kl_acc[r / hg], term);
+          }
+          // write the 16 columns of this chunk: two 16-byte pieces per image
+#pragma unroll
+          for (int hlf = 0; hlf < 2; ++hlf) {
+            const int c16 = q * 2 + hlf;
+            uint4 v;
+            float lo[8];
+#pragma unroll
+            for (int z = 0; z < 8; ++z) lo[z] = pv[8 * hlf + z] - __bfloat162float(__float2bfloat16_rn(pv[8 * hlf + z]));
+            v.x = pack_bf16(pv[8 * hlf + 0], pv[8 * hlf + 1]);
+            v.y = pack_bf16(pv[8 * hlf + 2], pv[8 * hlf + 3]);
+            v.z = pack_bf16(pv[8 * hlf + 4], pv[8 * hlf + 5]);
+            v.w = pack_bf16(pv[8 * hlf + 6], pv[8 * hlf + 7]);
+            *reinterpret_cast<uint4*>(smem + oPT + sw128_off(kk, c16)) = v;
+            v = make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
+                           pack_bf16(lo[6], lo[7]));
+            *reinterpret_cast<uint4*>(smem + oPL + sw128_off(kk, c16)) = v;
+            v.x = pack_bf16(dsv[8 * hlf + 0], dsv[8 * hlf + 1]);
+            v.y = pack_bf16(dsv[8 * hlf + 2], dsv[8 * hlf + 3]);
+            v.z = pack_bf16(dsv[8 * hlf + 4], dsv[8 * hlf + 5]);
+            v.w = pack_bf16(dsv[8 * hlf + 6], dsv[8 * hlf + 7]);
+            *reinterpret_cast<uint4*>(smem + oDST + sw128_off(kk, c16)) = v;
+            v.x = pack_bf16(gv[8 * hlf + 0], gv[8 * hlf + 1]);
+            v.y = pack_bf16(gv[8 * hlf + 2], gv[8 * hlf + 3]);
+            v.z = pack_bf16(gv[8 * hlf + 4], gv[8 * hlf + 5]);
+            v.w = pack_bf16(gv[8 * hlf + 6], gv[8 * hlf + 7]);
+            *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, c16)) = v;
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        if (!warps_sync(&sh.epi_sync, sync_phase, a.err, 525)) { ok = false; break; }
+        if (lane == 0) mbar_arrive(&sh.ph1_done);
+        // KL partial per query of the tile
+        if (kk < npos) {
+          const int r = kk * hg;
+          const int e = m.entry[r];
+          if (e >= 0) {
+            a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[kk];
+          }
+          sh.kl_acc[kk] = 0.f;  // next writers come after the phase-2 rendezvous
+        }
+        // ---- phase-2 epilogue: dQ^T (lane = d), dq_idx^T (lane = e < 64)
+        if (!mbar_wait(&sh.ph2_full, tj & 1, a.err, 524)) { ok = false; break; }
+        tc_fence_after();
+        {
+          float dq[32];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            tmem_ld32(tmem + lane_off + cS + q * 32, dq);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int r = q * 32 + i;
+              const int e = m.entry[r];
+              if (e >= 0) {
+                const int h = r % hg;
+                const size_t rowid = ((((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)) * hg + h;
+                a.dq_part[rowid * 128 + kk] = __float2bfloat16_rn(dq[i]);
+              }
+            }
+          }
+          if (quarter < 2) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              tmem_ld32(tmem + lane_off + cX + q * 32, dq);
+              tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int r = q * 32 + i;
+                const int e = m.entry[r];
+                if (e >= 0 && (r % hg) == 0)
+                  a.dqi_part[((((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)) * 64 + kk] = dq[i];
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        if (!warps_sync(&sh.epi_sync, sync_phase, a.err, 526)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive(&sh.ph2_done);
+          mbar_arrive(&sh.g_empty[gb]);
+        }
+      }
+      if (!ok) break;
+      // ---- list end: dV, dK, dk_idx accumulators (lane = key)
+      {
+        const size_t orow = ((size_t)b * a.T + key) * a.G + g;
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          tmem_ld32(tmem + lane_off + cDV + q * 32, v);
+          tmem_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(a.dV + orow * 128 + q * 32);
+#pragma unroll
+          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+          tmem_ld32(tmem + lane_off + cDK + q * 32, v);
+          tmem_wait_ld();
+          dst = reinterpret_cast<float4*>(a.dK + orow * 128 + q * 32);
+#pragma unroll
+          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+        }
+        float* dki = a.dki_part + (((size_t)b * a.G + g) * a.T + key) * 64;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          tmem_ld32(tmem + lane_off + cKI + q * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int z = 0; z < 8; ++z)
+            reinterpret_cast<float4*>(dki + q * 32)[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.acc_free);
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// One warp per (b, t, g): dQ rows of its heads, dq_idx and KL from the slots.
+__global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const __nv_bfloat16* __restrict__ dq_part,
+                                 const float* __restrict__ dqi_part, const float* __restrict__ kl_part,
+                                 float* __restrict__ dQ, float* __restrict__ dq_idx,
+                                 float* __restrict__ KL, int B, int T, int Hq, int G, int hg, int k) {
+  const long long rows = (long long)B * T * G;
+  const int lane = threadIdx.x & 31;
+  for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
+       w += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const int g = (int)(w % G);
+    const long long bt = w / G;
+    const int t = (int)(bt % T), b = (int)(bt / T);
+    const int32_t* sel = block_idx + (((size_t)b * G + g) * T + t) * k;
+    for (int h = 0; h < hg; ++h) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < k; ++s) {
+        if (sel[s] < 0) continue;
+        const uint2 raw = *reinterpret_cast<const uint2*>(dq_part + (((size_t)w * k + s) * hg + h) * 128 + lane * 4);
+        const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
+        acc[0] += f0.x;
+        acc[1] += f0.y;
+        acc[2] += f1.x;
+        acc[3] += f1.y;
+      }
+      *reinterpret_cast<float4*>(dQ + (((size_t)b * T + t) * Hq + g * hg + h) * 128 + lane * 4) =
+          make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+    float a0 = 0.f, a1 = 0.f, kl = 0.f;
+    for (int s = 0; s < k; ++s) {
+      if (sel[s] < 0) continue;
+      const float2 v = *reinterpret_cast<const float2*>(dqi_part + ((size_t)w * k + s) * 64 + lane * 2);
+      a0 += v.x;
+      a1 += v.y;
+      kl += kl_part[(size_t)w * k + s];
+    }
+    *reinterpret_cast<float2*>(dq_idx + (size_t)w * 64 + lane * 2) = make_float2(a0, a1);
+    if (lane == 0) KL[((size_t)b * G + g) * T + t] = kl;
+  }
+}
+
+// dk_idx[b,t,:] = sum_g dki_part[b,g,t,:]
+__global__ void dki_merge_kernel(const float* __restrict__ dki_part, float* __restrict__ dk_idx, int B,
+                                 int T, int G) {
+  const long long n2 = (long long)B * T * 32;  // pairs of elements
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n2; i += (long long)gridDim.x * blockDim.x) {
+    const long long bt = i / 32;
+    const int e2 = (int)(i % 32);
+    const int b = (int)(bt / T), t = (int)(bt % T);
+    float s0 = 0.f, s1 = 0.f;
+    for (int g = 0; g < G; ++g) {
+      const float2 v = *reinterpret_cast<const float2*>(dki_part + (((size_t)b * G + g) * T + t) * 64 + e2 * 2);
+      s0 += v.x;
+      s1 += v.y;
+    }
+    *reinterpret_cast<float2*>(dk_idx + bt * 64 + e2 * 2) = make_float2(s0, s1);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                       const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
+                       float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
+                       uint8_t* ws, const WsLayout& L, cudaStream_t st) {
+  cudaError_t e = build_block_map(p, block_idx, ws, L, 1, 1 << 30, st);
+  if (e != cudaSuccess) return e;
+  int* err = reinterpret_cast<int*>(ws + L.err);
+  int* counters = reinterpret_cast<int*>(ws + L.counters);
+  float* drow = reinterpret_cast<float*>(ws + L.drow);
+  float* px_part = reinterpret_cast<float*>(ws + L.px_part);
+  float* lse_px = reinterpret_cast<float*>(ws + L.lse_px);
+  const long long hrows = (long long)p.B * p.T * p.Hq;
+  const long long grows = (long long)p.B * p.T * p.G;
+  const int sms = num_sms();
+  drow_kernel<<<(int)std::min<long long>((hrows * 32 + 255) / 256, 16LL * sms), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), drow, hrows);
+  if ((e = cudaMemsetAsync(counters + 2, 0, 2 * sizeof(int), st)) != cudaSuccess) return e;
+
+  CUtensorMap mki, mk, mv;
+  {
+    const uint64_t dims[2] = {64, (uint64_t)p.BT()};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap(&mki, const_cast<void*>(k_idx), 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[3] = {128, (uint64_t)p.G, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {256, (uint64_t)p.G * 256};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap(&mk, const_cast<void*>(K), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  static bool attr = false;
+  if (!attr) {
+    if ((e = cudaFuncSetAttribute(px_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPxSmem)) !=
+        cudaSuccess)
+      return e;
+    for (auto f : {bwd_kernel<1>, bwd_kernel<2>, bwd_kernel<4>, bwd_kernel<8>})
+      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem)) != cudaSuccess)
+        return e;
+    attr = true;
+  }
+  PxArgs pa;
+  pa.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  pa.entries = reinterpret_cast<const int32_t*>(ws + L.entries);
+  pa.items = reinterpret_cast<const int4*>(ws + L.items);
+  pa.n_items = reinterpret_cast<const int*>(ws + L.n_items);
+  pa.counter = counters + 2;
+  pa.err = err;
+  pa.px_part = px_part;
+  pa.B = p.B;
+  pa.T = p.T;
+  pa.G = p.G;
+  pa.n = p.n;
+  pa.k = p.k;
+  pa.scale_log2 = p.scale_idx * kLog2e;
+  px_stats_kernel<<<sms, kPxThreads, kPxSmem, st>>>(pa, mki);
+  px_merge_kernel<<<(int)std::min<long long>((grows + 255) / 256, 16LL * sms), 256, 0, st>>>(
+      block_idx, px_part, lse_px, p.B, p.T, p.G, p.k);
+
+  BwdArgs ba;
+  ba.Q = static_cast<const __nv_bfloat16*>(Q);
+  ba.dO = static_cast<const __nv_bfloat16*>(dO);
+  ba.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  ba.LSE = LSE;
+  ba.drow = drow;
+  ba.lse_px = lse_px;
+  ba.entries = pa.entries;
+  ba.items = pa.items;
+  ba.n_items = pa.n_items;
+  ba.counter = counters + 3;
+  ba.err = err;
+  ba.dK = static_cast<float*>(dK);
+  ba.dV = static_cast<float*>(dV);
+  ba.dq_part = reinterpret_cast<__nv_bfloat16*>(ws + L.dq_part);
+  ba.dqi_part = reinterpret_cast<float*>(ws + L.dqi_part);
+  ba.kl_part = reinterpret_cast<float*>(ws + L.kl_part);
+  ba.dki_part = reinterpret_cast<float*>(ws + L.dki_part);
+  ba.B = p.B;
+  ba.T = p.T;
+  ba.Hq = p.Hq;
+  ba.G = p.G;
+  ba.hg = p.hg;
+  ba.n = p.n;
+  ba.k = p.k;
+  ba.scale_log2 = p.scale * kLog2e;
+  ba.scale = p.scale;
+  ba.scale_idx_log2 = p.scale_idx * kLog2e;
+  ba.scale_idx = p.scale_idx;
+  ba.kl_weight = kl_weight;
+  switch (p.hg) {
+    case 1: bwd_kernel<1><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
+    case 2: bwd_kernel<2><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
+    case 4: bwd_kernel<4><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
+    default: bwd_kernel<8><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
+  }
+  count_launches(6);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  bwd_merge_kernel<<<(int)std::min<long long>((grows * 32 + 255) / 256, 16LL * sms), 256, 0, st>>>(
+      block_idx, ba.dq_part, ba.dqi_part, ba.kl_part, static_cast<float*>(dQ), static_cast<float*>(dq_idx), KL,
+      p.B, p.T, p.Hq, p.G, p.hg, p.k);
+  const long long n2 = (long long)p.B * p.T * 32;
+  dki_merge_kernel<<<(int)std::min<long long>((n2 + 255) / 256, 16LL * sms), 256, 0, st>>>(
+      ba.dki_part, static_cast<float*>(dk_idx), p.B, p.T, p.G);
+  return cudaGetLastError();
+}
+
+}  // namespace msa

@@ -62,6 +62,7 @@ struct FwdShared {
   uint64_t p_full[2], p_free[2];
   uint64_t o_full[2], o_empty[2];
   int4 item[2];
+  int tile_t[128];  // producer scratch: query of each tile position
   uint32_t tmem_base;
   int abort;
 };
@@ -166,20 +167,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qs = tj % kQStages;
         if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 303)) { ok = false; break; }
         const uint32_t dst0 = smem_u32(sQ + qs * kTile) + (chunk >> 3) * kChunk;
+        // stage the tile's queries first: the loads are independent and overlap
+        for (int p = lane; p < P; p += 32) {
+          const int idx = j * P + p;
+          sh.tile_t[p] = idx < item.z ? (a.entries[item.y + idx] >> 8) : -1;
+        }
+        __syncwarp();
+#pragma unroll 8
         for (int i = 0; i < 64; ++i) {
           const int r = 2 * i + (lane >> 4);
           const int p = r / a.hg, h = r - p * a.hg;
-          const int idx = j * P + p;
-          const bool valid = idx < item.z;
-          const int t = valid ? (a.entries[item.y + idx] >> 8) : 0;
+          const int tq = sh.tile_t[p];
+          const bool valid = tq >= 0;
           const __nv_bfloat16* src =
-              a.Q + ((((size_t)b * a.T + t) * a.Hq + g * a.hg + h) * 128 + chunk * 8);
+              a.Q + ((((size_t)b * a.T + (valid ? tq : 0)) * a.Hq + g * a.hg + h) * 128 + chunk * 8);
           cp_async_16_zfill(dst0 + sw128_off(r, chunk & 7), src, valid);
         }
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
         mbar_arrive(&sh.q_full[qs]);
+        __syncwarp();
       }
       if (!ok) { *abort_flag = 1; break; }
     }
@@ -438,6 +446,7 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
     attr = true;
   }
   sparse_fwd_kernel<<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv);
+  count_launches(2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.T * p.G;
   const int grid = (int)std::min<long long>((rows * 32 + 255) / 256, 16LL * num_sms());

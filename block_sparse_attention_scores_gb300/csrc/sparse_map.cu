@@ -232,6 +232,7 @@ cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws
     attr_set = true;
   }
   map_sort_kernel<<<std::min(lists, 4 * num_sms()), 1024, kSortCap * 4, st>>>(off, lists, entries);
+  count_launches(4);
   return cudaGetLastError();
 }
 

@@ -27,12 +27,13 @@
  * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *   stream). Host-side argument checks run before anything is enqueued; on a
  *   non-OK status nothing was launched and msa_last_error() describes why.
- * - bf16 tensors are passed as `void*` holding IEEE bfloat16 values.
+ * - bf16 tensors are passed as `void*` holding IEEE bfloat16 values; the
+ *   backward's gradients are fp32 (`float*`), accumulated and written in fp32.
  * - Layouts (row-major, innermost last):
- *     Q, O, dO, dQ        [B, T, Hq, d]      bf16
- *     K, V, dK, dV        [B, T, G, d]       bf16   (one KV head per group)
- *     q_idx, dq_idx       [B, T, G, d_idx]   bf16
- *     k_idx, dk_idx       [B, T, d_idx]      bf16   (shared by all groups)
+ *     Q, O, dO            [B, T, Hq, d]      bf16      dQ      fp32
+ *     K, V                [B, T, G, d]       bf16      dK, dV  fp32 (one KV head per group)
+ *     q_idx               [B, T, G, d_idx]   bf16      dq_idx  fp32
+ *     k_idx               [B, T, d_idx]      bf16      dk_idx  fp32 (shared by all groups)
  *     block_idx           [B, G, T, k]       int32  (ascending ids, -1 padded)
  *     LSE                 [B, T, Hq]         fp32   (natural log, scaled scores)
  *     KL                  [B, G, T]          fp32   (one KL term per query)
@@ -155,13 +156,16 @@ MSA_API msa_status msa_sparse_fwd(const msa_shape *shape, const void *Q, const v
  * No KL gradient reaches Q, K, V and no dO gradient reaches q_idx, k_idx.
  *
  * Inputs as in msa_sparse_fwd; O and LSE are the forward's outputs for the
- * same block_idx. Outputs dQ, dK, dV, dq_idx, dk_idx (bf16) and KL (fp32) are
- * fully written (positions that no query selected get zero dK/dV/dk_idx).
+ * same block_idx. Outputs dQ, dK, dV, dq_idx, dk_idx and KL (all fp32) are
+ * fully written: every key block is selected at least by its own queries, so
+ * every dK/dV/dk_idx row receives its sum (rows of a block whose queries all
+ * had invalid block_idx rows are unspecified, as is everything else when the
+ * device error word is set).
  */
 MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K, const void *V, const void *O,
                    const void *dO, const float *LSE, const void *q_idx, const void *k_idx,
-                   const int32_t *block_idx, float kl_weight, void *dQ, void *dK, void *dV, void *dq_idx,
-                   void *dk_idx, float *KL, void *workspace, size_t workspace_bytes, msa_stream_t stream);
+                   const int32_t *block_idx, float kl_weight, float *dQ, float *dK, float *dV, float *dq_idx,
+                   float *dk_idx, float *KL, void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /* Message describing the last non-OK status returned on this thread. */
 MSA_API const char *msa_last_error(void);
@@ -171,6 +175,18 @@ MSA_API const char *msa_last_error(void);
  * gave up on a wait or met a block id out of range; msa_last_error() says
  * which kernel and where. */
 MSA_API msa_status msa_check_device_status(const void *workspace, msa_stream_t stream);
+
+/* Failure-detection self-test: launches one block whose wait on an mbarrier
+ * that nothing ever arrives at is bounded by `limit_us` microseconds
+ * (1..1000000). The wait runs out, the kernel records a timeout in the error
+ * word of `workspace` (>= 256 bytes, device memory) and returns; a following
+ * msa_check_device_status() reports MSA_ERR_DEVICE. Exercises the same bounded
+ * wait every kernel uses, without faulting or hanging the GPU. */
+MSA_API msa_status msa_selftest_wait_timeout(void *workspace, int32_t limit_us, msa_stream_t stream);
+
+/* Number of kernels this library has launched in the calling process since it
+ * was loaded (monotonic; for accounting in benchmarks and tests). */
+MSA_API int64_t msa_kernel_launches(void);
 
 /* ABI version: (major << 16) | minor. */
 MSA_API int32_t msa_version(void);
