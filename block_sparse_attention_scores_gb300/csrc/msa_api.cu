@@ -91,26 +91,30 @@ WsLayout ws_layout(const Prob& p, int which) {
     L.list_count = take(lists * 4);
     L.list_off = take((lists + 1) * 4);
     L.list_cursor = take(lists * 4);
+    L.list_poff = take((lists + 1) * 4);
     L.entries = take(rows * p.G * p.k * 4);
+    L.rev = take(rows * p.G * p.k * 4);
+    // lists are padded to whole tiles of at most 128 queries
+    L.max_padded = (long long)(rows * p.G * p.k) + (long long)lists * 128;
     L.max_items = max_work_items(p, 1, 16);
     L.items = take((size_t)L.max_items * 16);
     L.n_items = take(16);
   }
   if (which == MSA_WS_FWD) {
-    L.o_part = take(rows * p.G * p.k * p.hg * p.d * 2);
-    L.lse_part = take(rows * p.G * p.k * p.hg * 4);
+    L.o_part = take((size_t)L.max_padded * p.hg * p.d * 2);
+    L.lse_part = take((size_t)L.max_padded * p.hg * 4);
   }
   if (which == MSA_WS_BWD) {
     // the forward's partial buffers alias the backward's larger ones
     L.drow = take(rows * p.Hq * 4);
     L.px_part = take(rows * p.G * p.k * 4);
     L.lse_px = take(rows * p.G * 4);
-    L.dq_part = take(rows * p.G * p.k * p.hg * p.d * 2);
+    L.dq_part = take((size_t)L.max_padded * p.hg * p.d * 2);
     L.dqi_part = take(rows * p.G * p.k * p.E * 4);
     L.kl_part = take(rows * p.G * p.k * 4);
     L.dki_part = take((size_t)p.B * p.G * p.T * p.E * 4);
     L.o_part = L.dq_part;
-    L.lse_part = take(rows * p.G * p.k * p.hg * 4);
+    L.lse_part = take((size_t)L.max_padded * p.hg * 4);
   }
   L.total = off;
   return L;

@@ -29,11 +29,13 @@ struct WsLayout {
   size_t list_count = 0;    // int32 [B*G*n]   selections per KV block
   size_t list_off = 0;      // int32 [B*G*n+1] exclusive prefix of list_count
   size_t list_cursor = 0;   // int32 [B*G*n]   scatter cursors
+  size_t list_poff = 0;     // int32 [B*G*n+1] prefix of list lengths padded to whole tiles
+  size_t rev = 0;           // int32 [B*G*T*k] padded entry index of (b, g, t, slot)
   size_t entries = 0;       // int32 [B*G*T*k] (t << 8 | slot), grouped by list
   size_t items = 0;         // int4  [max_items] work items (list, tile range)
   size_t n_items = 0;       // int32 [4]       number of work items per kernel
-  size_t o_part = 0;        // bf16  [B,T,G,k,hg,d] forward partial outputs (normalised)
-  size_t lse_part = 0;      // fp32  [B,T,G,k,hg]   forward partial log-sum-exp
+  size_t o_part = 0;        // bf16  [padded entries, hg, d] forward partial outputs (normalised), tile order
+  size_t lse_part = 0;      // fp32  [padded entries, hg]    forward partial log-sum-exp
   size_t drow = 0;          // fp32  [B,T,Hq]       rowsum(dO * O)
   size_t px_part = 0;       // fp32  [B,T,G,k]      index-branch partial LSE per slot
   size_t lse_px = 0;        // fp32  [B,T,G]        index-branch LSE over S(g,t)
@@ -43,6 +45,7 @@ struct WsLayout {
   size_t dki_part = 0;      // fp32  [B,G,T,E]      dk_idx per group
   size_t total = 256;
   int max_items = 0;
+  long long max_padded = 0;  // capacity in padded entries (queries x slots, tile-padded per list)
 };
 
 WsLayout ws_layout(const Prob& p, int which);

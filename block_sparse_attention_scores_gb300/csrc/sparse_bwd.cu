@@ -455,24 +455,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503)) { ok = false; break; }
         uint8_t* buf = smem + oG + gb * kGather;
         const uint32_t q0 = smem_u32(buf), do0 = q0 + kRowTile, qi0 = q0 + 2 * kRowTile;
-        // row metadata first (independent loads), then the gathers read it
+        // row metadata first, then the gathers read it. Each lane owns rows
+        // lane and lane + 32: both entry loads go out together, then all six
+        // dependent loads together (two memory round trips per tile).
         RowMeta& m = sh.meta[gb];
-        for (int r = lane; r < kRows; r += 32) {
-          const int p = r / hg, h = r - p * hg;
-          const int idx = j * npos + p;
-          if (idx < item.z) {
-            const int e = a.entries[item.y + idx];
-            const int t = e >> 8;
-            const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + h;
-            m.entry[r] = e;
-            m.lse2[r] = a.LSE[hr] * kLog2e;
-            m.dval[r] = a.drow[hr];
-            m.lsepx2[r] = a.lse_px[((size_t)b * a.T + t) * a.G + g] * kLog2e;
-          } else {
-            m.entry[r] = -1;
-            m.lse2[r] = 0.f;
-            m.dval[r] = 0.f;
-            m.lsepx2[r] = 0.f;
+        {
+          int e2[2], t2[2], h2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int r = lane + 32 * u;
+            const int p = r / hg;
+            h2[u] = r - p * hg;
+            const int idx = j * npos + p;
+            e2[u] = idx < item.z ? a.entries[item.y + idx] : -1;
+          }
+          float l2[2], d2[2], x2[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            t2[u] = e2[u] >= 0 ? (e2[u] >> 8) : 0;
+            const size_t hr = ((size_t)b * a.T + t2[u]) * a.Hq + g * hg + h2[u];
+            l2[u] = e2[u] >= 0 ? a.LSE[hr] : 0.f;
+            d2[u] = e2[u] >= 0 ? a.drow[hr] : 0.f;
+            x2[u] = e2[u] >= 0 ? a.lse_px[((size_t)b * a.T + t2[u]) * a.G + g] : 0.f;
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int r = lane + 32 * u;
+            m.entry[r] = e2[u];
+            m.lse2[r] = l2[u] * kLog2e;
+            m.dval[r] = d2[u];
+            m.lsepx2[r] = x2[u] * kLog2e;
           }
         }
         __syncwarp();

@@ -17,7 +17,8 @@
 // warps (one TMEM lane = one (query, head) row) mask keys past the query,
 // exponentiate, write P (bf16) to shared memory; tcgen05 computes O = P V_c
 // into TMEM; the same warps write the normalised partial O and its partial
-// LSE for (query, slot). Two S and two O accumulators (512 TMEM columns) let
+// LSE for (query, slot), in tile order (one TMA store per warp and 64-column
+// chunk). Two S and two O accumulators (512 TMEM columns) let
 // the tensor core work on one tile while the softmax warps work on the other.
 // A second kernel merges the k partials of every (query, head):
 // LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) O_s.
@@ -79,7 +80,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v) {
+    sparse_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                      const __grid_constant__ CUtensorMap map_o) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
@@ -250,13 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int p_in_tile = row / a.hg, h = row - (row / a.hg) * a.hg;
+    const int p_in_tile = row / a.hg;
     uint32_t tj = 0;
     bool ok = true;
     // pending tile (softmax done, output not yet written)
     float pm = 0.f, pl = 0.f;
     int pentry = -1;
-    int pb = 0, pg = 0;
+    int prow0 = 0;  // first partial-output row of the pending tile
+    // Partial outputs live in tile order: the tile's rows are consecutive, so
+    // each warp stages its 32 normalised rows (bf16, SW128 image) in the P
+    // buffer the O MMA has finished with and writes them with one TMA store
+    // per 64-column chunk.
     auto epilogue = [&](uint32_t u) -> bool {
       const int sb = u & 1;
       if (!mbar_wait(&sh.o_full[sb], (u >> 1) & 1, a.err, 321)) return false;
@@ -268,21 +274,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.o_empty[sb]);
-      if (pentry >= 0) {
-        const int t = pentry >> 8, slot = pentry & 255;
-        const float inv = 1.f / pl;
-        const size_t rowid = ((((size_t)pb * a.T + t) * a.G + pg) * a.k + slot) * a.hg + h;
-        uint4* dst = reinterpret_cast<uint4*>(a.o_part + rowid * 128);
+      const float inv = pentry >= 0 ? 1.f / pl : 0.f;
+      uint8_t* stage = sP + sb * kTile;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint4 v;
-          v.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-          v.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-          v.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-          v.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-          dst[q] = v;
-        }
-        a.lse_part[rowid] = (pm + __log2f(pl)) * kLn2;
+      for (int q = 0; q < 16; ++q) {
+        uint4 v;
+        v.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
+        v.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
+        v.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
+        v.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
+        *reinterpret_cast<uint4*>(stage + (q >> 3) * kChunk + sw128_off(row, q & 7)) = v;
+      }
+      if (pentry >= 0) a.lse_part[(size_t)prow0 + row] = (pm + __log2f(pl)) * kLn2;
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&map_o, stage + quarter * 4096, 0, prow0 + quarter * 32);
+        tma_store_2d(&map_o, stage + kChunk + quarter * 4096, 64, prow0 + quarter * 32);
+        bulk_commit();
       }
       return true;
     };
@@ -294,8 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.it_empty[s]);
       if (item.x < 0) break;
-      const int bg = item.x / a.n, c = item.x % a.n;
-      const int b = bg / a.G, g = bg % a.G;
+      const int c = item.x % a.n;
       const int ntiles = (item.z + P - 1) / P;
       for (int j = 0; j < ntiles; ++j, ++tj) {
         const int sb = tj & 1;
@@ -324,8 +332,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[i] = fast_exp2(x[i] - mm);
           l += x[i];
         }
-        // P[sb] is free once the O MMA of tile tj-2 has read it
+        // P[sb] is free once the O MMA of tile tj-2 has read it and this
+        // warp's TMA store of tile tj-2's partial rows has read its staging
         if (!mbar_wait(&sh.p_free[sb], ((tj >> 1) & 1) ^ 1, a.err, 324)) { ok = false; break; }
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
         uint8_t* prow = sP + sb * kTile;
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -345,13 +356,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         pm = mm;
         pl = l;
         pentry = entry;
-        pb = b;
-        pg = g;
+        prow0 = (item.w + j * P) * a.hg;
       }
       // the last tile of the item is finished at the start of the next item's
       // first tile, or after the loop ends
     }
     if (ok && tj > 0) ok = epilogue(tj - 1);
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!ok) *abort_flag = 1;
   }
 
@@ -361,10 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// One warp per (b, t, g): merge the k partials of each of the hg heads.
-__global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const __nv_bfloat16* __restrict__ o_part,
-                                 const float* __restrict__ lse_part, __nv_bfloat16* __restrict__ O,
-                                 float* __restrict__ LSE, int B, int T, int Hq, int G, int hg, int k) {
+// One warp per (b, t, g): merge the k partials of each of the hg heads. The
+// partial of (b, g, t, slot) sits at padded entry rev[(b*G + g)*T + t][slot].
+__global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
+                                 const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
+                                 __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int B, int T, int Hq, int G,
+                                 int hg, int k, long long max_padded) {
   const long long rows = (long long)B * T * G;
   const int lane = threadIdx.x & 31;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
@@ -372,19 +386,24 @@ __global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const __
     const int g = (int)(w % G);
     const long long bt = w / G;
     const int t = (int)(bt % T), b = (int)(bt / T);
-    const int32_t* sel = block_idx + (((size_t)b * G + g) * T + t) * k;
+    const size_t sel_row = (((size_t)b * G + g) * T + t) * k;
+    const int32_t* sel = block_idx + sel_row;
+    const int32_t* rv = rev + sel_row;
+    // a slot counts only if the map placed it (rows that failed validation
+    // keep -1 and are left unspecified, with the error word set)
+    auto live = [&](int s) { return sel[s] >= 0 && rv[s] >= 0 && (long long)rv[s] < max_padded; };
     for (int h = 0; h < hg; ++h) {
       float mx = -INFINITY;
       for (int s = 0; s < k; ++s)
-        if (sel[s] >= 0) mx = fmaxf(mx, lse_part[((size_t)w * k + s) * hg + h]);
+        if (live(s)) mx = fmaxf(mx, lse_part[(size_t)rv[s] * hg + h]);
       float z = 0.f;
       for (int s = 0; s < k; ++s)
-        if (sel[s] >= 0) z += expf(lse_part[((size_t)w * k + s) * hg + h] - mx);
+        if (live(s)) z += expf(lse_part[(size_t)rv[s] * hg + h] - mx);
       const float lse = mx + logf(z);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int s = 0; s < k; ++s) {
-        if (sel[s] < 0) continue;
-        const size_t rid = ((size_t)w * k + s) * hg + h;
+        if (!live(s)) continue;
+        const size_t rid = (size_t)rv[s] * hg + h;
         const float wgt = expf(lse_part[rid] - lse);
         const uint2 raw = *reinterpret_cast<const uint2*>(o_part + rid * 128 + lane * 4);
         const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
@@ -419,6 +438,14 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
     return cudaErrorInvalidValue;
   if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  CUtensorMap mo;
+  {
+    const uint64_t odims[2] = {128, (uint64_t)L.max_padded * p.hg};
+    const uint64_t ostr[1] = {256};
+    const uint32_t obox[2] = {64, 32};
+    if (!encode_tmap(&mo, ws + L.o_part, 2, odims, ostr, obox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   FwdArgs a;
   a.Q = static_cast<const __nv_bfloat16*>(Q);
   a.entries = reinterpret_cast<const int32_t*>(ws + L.entries);
@@ -445,13 +472,14 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
       return e;
     attr = true;
   }
-  sparse_fwd_kernel<<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv);
+  sparse_fwd_kernel<<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo);
   count_launches(2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.T * p.G;
   const int grid = (int)std::min<long long>((rows * 32 + 255) / 256, 16LL * num_sms());
-  fwd_merge_kernel<<<grid, 256, 0, st>>>(block_idx, a.o_part, a.lse_part, static_cast<__nv_bfloat16*>(O), LSE, p.B,
-                                         p.T, p.Hq, p.G, p.hg, p.k);
+  fwd_merge_kernel<<<grid, 256, 0, st>>>(block_idx, reinterpret_cast<const int32_t*>(ws + L.rev), a.o_part,
+                                         a.lse_part, static_cast<__nv_bfloat16*>(O), LSE, p.B, p.T, p.Hq, p.G, p.hg,
+                                         p.k, L.max_padded);
   return cudaGetLastError();
 }
 
