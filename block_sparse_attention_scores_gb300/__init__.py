@@ -31,7 +31,8 @@ MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUD
 MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD = 0, 1, 2
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
-            "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version")
+            "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version",
+            "msa_index_topk_noalloc")
 
 
 class MsaError(RuntimeError):
@@ -89,6 +90,8 @@ def load_library():
     lib.msa_check_device_status.restype = ctypes.c_int
     lib.msa_version.restype = ctypes.c_int32
     lib.msa_kernel_launches.restype = ctypes.c_int64
+    lib.msa_index_topk_noalloc.argtypes = [S, P, P, P, ctypes.c_int32, P]
+    lib.msa_index_topk_noalloc.restype = ctypes.c_int
     lib.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_int32, P]
     lib.msa_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
@@ -147,6 +150,12 @@ def msa_index_topk(shape, q_idx, k_idx, block_idx, workspace, stream=None, works
     wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
     _check(load_library().msa_index_topk(ctypes.byref(_shape(shape)), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx),
                                          _ptr(workspace), wb, _stream(stream)))
+
+
+def msa_index_topk_noalloc(shape, q_idx, k_idx, block_idx, check: bool = True, stream=None) -> None:
+    """msa_index_topk without a workspace (static scratch inside the library)."""
+    _check(load_library().msa_index_topk_noalloc(ctypes.byref(_shape(shape)), _ptr(q_idx), _ptr(k_idx),
+                                                 _ptr(block_idx), 1 if check else 0, _stream(stream)))
 
 
 def msa_sparse_fwd(shape, Q, K, V, block_idx, O, LSE, workspace, stream=None, workspace_bytes=None) -> None:

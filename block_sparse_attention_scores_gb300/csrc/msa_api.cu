@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <mutex>
 
 #include "msa_internal.h"
 #include "sm100.cuh"
@@ -299,3 +300,65 @@ msa_status msa_check_device_status(const void* workspace, msa_stream_t stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Index top-k without a caller workspace: scratch in a static device array.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up once).
+msa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return fail(MSA_ERR_UNSUPPORTED, "no usable current CUDA device");
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return fail(MSA_ERR_CUDA, "looking up the static scratch on device %d: %s", dev, cudaGetErrorString(e));
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MSA_OK;
+}
+}  // namespace
+
+extern "C" msa_status msa_index_topk_noalloc(const msa_shape* shape, const void* q_idx, const void* k_idx,
+                                             int32_t* block_idx, int32_t check, msa_stream_t stream) {
+  Prob p;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_ptr(q_idx, "q_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(k_idx, "k_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(block_idx, "block_idx", 16)) != MSA_OK) return s;
+  const WsLayout L = ws_layout(p, MSA_WS_TOPK);
+  if (L.total > (size_t)MSA_NOALLOC_SCRATCH_BYTES)
+    return fail(MSA_ERR_UNSUPPORTED, "this shape needs %zu bytes of scratch; the static scratch holds %d", L.total,
+                MSA_NOALLOC_SCRATCH_BYTES);
+  if ((s = check_device()) != MSA_OK) return s;
+  void* scratch = nullptr;
+  if ((s = noalloc_scratch(&scratch)) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // error word and work counter must start at zero; the rest is not read
+  if ((s = cuda_status(cudaMemsetAsync(scratch, 0, 256, st), "clearing static scratch")) != MSA_OK) return s;
+  if ((s = cuda_status(launch_index_topk(p, q_idx, k_idx, block_idx, scratch, L, st), "index top-k launch")) !=
+      MSA_OK)
+    return s;
+  if (!check) return MSA_OK;
+  int word = 0;
+  if ((s = cuda_status(cudaMemcpyAsync(&word, scratch, sizeof word, cudaMemcpyDeviceToHost, st),
+                       "reading the error word")) != MSA_OK)
+    return s;
+  if ((s = cuda_status(cudaStreamSynchronize(st), "stream synchronize")) != MSA_OK) return s;
+  if (word != 0)
+    return fail(MSA_ERR_DEVICE, "device error %s at site %d",
+                word / 65536 == kDevTimeout ? "timeout (a bounded wait ran out)" : "unknown", word % 65536);
+  return MSA_OK;
+}

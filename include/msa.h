@@ -167,6 +167,35 @@ MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K,
                    const int32_t *block_idx, float kl_weight, float *dQ, float *dK, float *dV, float *dq_idx,
                    float *dk_idx, float *KL, void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
+/*
+ * Index top-k for callers that cannot allocate device memory. The paper has
+ * no counterpart to this call; it computes exactly what msa_index_topk does.
+ *
+ * Some callers cannot call cudaMalloc: a plugin inside a host application
+ * that owns every byte of device memory and hands the plugin no allocator,
+ * or code on a latency-critical path where cudaMalloc's implicit device-wide
+ * synchronisation is not acceptable. This variant needs no workspace: its
+ * scratch (the kernel's error word and work counter, 256 bytes) lives in a
+ * static device array of MSA_NOALLOC_SCRATCH_BYTES bytes inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ * - The first call on a device looks up that array's device address (once
+ *   per device, with the device current); make that first call before any
+ *   stream capture.
+ * - Every call clears the scratch it relies on (asynchronously, on `stream`)
+ *   and then reuses it: calls that overlap on the GPU (different streams or
+ *   devices' contexts sharing the array) race on it. Serialise them.
+ * - A shape whose scratch would exceed MSA_NOALLOC_SCRATCH_BYTES is rejected
+ *   with MSA_ERR_UNSUPPORTED.
+ * - check != 0 synchronises `stream` and returns MSA_ERR_DEVICE if the kernel
+ *   reported a timeout; check == 0 returns without waiting (device-side
+ *   errors then go unreported).
+ * No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define MSA_NOALLOC_SCRATCH_BYTES 4096
+MSA_API msa_status msa_index_topk_noalloc(const msa_shape *shape, const void *q_idx, const void *k_idx,
+                                          int32_t *block_idx, int32_t check, msa_stream_t stream);
+
 /* Message describing the last non-OK status returned on this thread. */
 MSA_API const char *msa_last_error(void);
 
