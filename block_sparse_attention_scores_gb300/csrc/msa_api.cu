@@ -43,7 +43,7 @@ int num_sms() {
 }
 
 bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                 const uint32_t* box, CUtensorMapSwizzle swz) {
+                 const uint32_t* box, CUtensorMapSwizzle swz, CUtensorMapDataType dtype) {
   typedef CUresult (*EncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -65,7 +65,7 @@ bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, c
     e[i] = 1;
     if (i + 1 < rank) s[i] = strides_bytes[i];
   }
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+  return fn(map, dtype, rank, base, d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -111,7 +111,7 @@ WsLayout ws_layout(const Prob& p, int which) {
     L.px_part = take(rows * p.G * p.k * 4);
     L.lse_px = take(rows * p.G * 4);
     L.dq_part = take((size_t)L.max_padded * p.hg * p.d * 2);
-    L.dqi_part = take(rows * p.G * p.k * p.E * 4);
+    L.dqi_part = take((size_t)L.max_padded * p.E * 4);
     L.kl_part = take(rows * p.G * p.k * 4);
     L.dki_part = take((size_t)p.B * p.G * p.T * p.E * 4);
     L.o_part = L.dq_part;

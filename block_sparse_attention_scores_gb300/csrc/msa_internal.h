@@ -39,8 +39,8 @@ struct WsLayout {
   size_t drow = 0;          // fp32  [B,T,Hq]       rowsum(dO * O)
   size_t px_part = 0;       // fp32  [B,T,G,k]      index-branch partial LSE per slot
   size_t lse_px = 0;        // fp32  [B,T,G]        index-branch LSE over S(g,t)
-  size_t dq_part = 0;       // bf16  [B,T,G,k,hg,d] dQ partials per slot
-  size_t dqi_part = 0;      // fp32  [B,T,G,k,E]    dq_idx partials per slot
+  size_t dq_part = 0;       // bf16  [padded entries, hg, d] dQ partials, tile order
+  size_t dqi_part = 0;      // fp32  [padded entries, E]     dq_idx partials, tile order
   size_t kl_part = 0;       // fp32  [B,T,G,k]      KL partials per slot
   size_t dki_part = 0;      // fp32  [B,G,T,E]      dk_idx per group
   size_t total = 256;
@@ -55,7 +55,8 @@ int max_work_items(const Prob& p, int tiles_per_item, int rows_per_tile);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, const uint64_t* strides_bytes,
-                 const uint32_t* box, CUtensorMapSwizzle swz);
+                 const uint32_t* box, CUtensorMapSwizzle swz,
+                 CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
 
 int num_sms();
 

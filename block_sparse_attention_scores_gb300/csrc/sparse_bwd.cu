@@ -346,8 +346,8 @@ struct BwdArgs {
   int* err;
   float* dK;
   float* dV;
-  __nv_bfloat16* dq_part;  // [B,T,G,k,hg,d]
-  float* dqi_part;         // [B,T,G,k,E]
+  __nv_bfloat16* dq_part;  // [padded entries, hg, d], tile order
+  float* dqi_part;         // [padded entries, E], tile order
   float* kl_part;          // [B,T,G,k]
   float* dki_part;         // [B,G,T,E]
   int B, T, Hq, G, hg, n, k;
@@ -373,7 +373,8 @@ static_assert(kBwdSmem <= 232448, "backward kernel exceeds 227 KB of shared memo
 template <int HG>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(BwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-               const __grid_constant__ CUtensorMap map_ki) {
+               const __grid_constant__ CUtensorMap map_ki, const __grid_constant__ CUtensorMap map_dq,
+               const __grid_constant__ CUtensorMap map_dqi) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // uniform for the block: nothing started yet
     if (threadIdx.x == 0) dev_fail(a.err, kDevSmemAlign, 500);
@@ -622,6 +623,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 522)) { ok = false; break; }
         if (!mbar_wait(&sh.ph1_full, tj & 1, a.err, 523)) { ok = false; break; }
         tc_fence_after();
+        // this warp's key rows of the P_lo^T / dS^T / gs^T images double as
+        // its staging for the previous tile's partial stores: wait until read
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
         // ---- phase-1 epilogue: 64 rows, 16 at a time
         for (int q = 0; q < 4; ++q) {
           float sv[16], dp[16], xv[16];
@@ -705,26 +710,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           sh.kl_acc[kk] = 0.f;  // next writers come after the phase-2 rendezvous
         }
         // ---- phase-2 epilogue: dQ^T (lane = d), dq_idx^T (lane = e < 64)
+        // Partials are in tile order: this tile's 64 (query, head) rows are
+        // consecutive. Each warp stages its 32-column slice row-major in its
+        // own 4 KB of the consumed key-row images and writes it with one TMA
+        // store (bf16 dQ) or two (fp32 dq_idx).
         if (!mbar_wait(&sh.ph2_full, tj & 1, a.err, 524)) { ok = false; break; }
         tc_fence_after();
         {
+          const int prow0 = (item.w + j * npos) * hg;  // first dQ partial row of the tile
+          const int pos0 = item.w + j * npos;          // first dq_idx partial row
+          __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + oPL + quarter * 4096);
           float dq[32];
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             tmem_ld32(tmem + lane_off + cS + q * 32, dq);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int r = q * 32 + i;
-              const int e = m.entry[r];
-              if (e >= 0) {
-                const int h = r % hg;
-                const size_t rowid = ((((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)) * hg + h;
-                a.dq_part[rowid * 128 + kk] = __float2bfloat16_rn(dq[i]);
-              }
-            }
+            for (int i = 0; i < 32; ++i) stg[(q * 32 + i) * 32 + lane] = __float2bfloat16_rn(dq[i]);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) tma_store_2d(&map_dq, stg, quarter * 32, prow0);
           if (quarter < 2) {
+            // rows = queries of the tile, 32 per staging block; both blocks are
+            // this warp's own key rows (of the dS^T and gs^T images)
+            float* stgA = reinterpret_cast<float*>(smem + oDST + quarter * 4096);
+            float* stgB = reinterpret_cast<float*>(smem + oGST + quarter * 4096);
+            constexpr int kBox = npos < 32 ? npos : 32;
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
               tmem_ld32(tmem + lane_off + cX + q * 32, dq);
@@ -732,12 +744,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 const int r = q * 32 + i;
-                const int e = m.entry[r];
-                if (e >= 0 && (r % hg) == 0)
-                  a.dqi_part[((((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)) * 64 + kk] = dq[i];
+                if (r % hg == 0) {
+                  const int pq = r / hg;  // query index within the tile
+                  float* dst = (pq < kBox ? stgA : stgB) + (pq % kBox) * 32 + lane;
+                  *dst = dq[i];
+                }
               }
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&map_dqi, stgA, quarter * 32, pos0);
+              if (npos > kBox) tma_store_2d(&map_dqi, stgB, quarter * 32, pos0 + kBox);
+            }
           }
+          if (lane == 0) bulk_commit();
         }
         tc_fence_before();
         if (!warps_sync(&sh.epi_sync, sync_phase, a.err, 526)) { ok = false; break; }
@@ -778,6 +799,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) mbar_arrive(&sh.acc_free);
       }
     }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
     if (!ok) *abort_flag = 1;
   }
   __syncwarp();
@@ -787,10 +810,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // One warp per (b, t, g): dQ rows of its heads, dq_idx and KL from the slots.
-__global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const __nv_bfloat16* __restrict__ dq_part,
-                                 const float* __restrict__ dqi_part, const float* __restrict__ kl_part,
-                                 float* __restrict__ dQ, float* __restrict__ dq_idx,
-                                 float* __restrict__ KL, int B, int T, int Hq, int G, int hg, int k) {
+// The partials of (b, g, t, slot) sit at padded entry rev[(b*G + g)*T + t][slot]
+// (dQ: rows entry*hg + h; dq_idx: row entry); KL partials at (b, t, g, slot).
+__global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
+                                 const __nv_bfloat16* __restrict__ dq_part, const float* __restrict__ dqi_part,
+                                 const float* __restrict__ kl_part, float* __restrict__ dQ,
+                                 float* __restrict__ dq_idx, float* __restrict__ KL, int B, int T, int Hq, int G,
+                                 int hg, int k, long long max_padded) {
   const long long rows = (long long)B * T * G;
   const int lane = threadIdx.x & 31;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
@@ -798,12 +824,15 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const __
     const int g = (int)(w % G);
     const long long bt = w / G;
     const int t = (int)(bt % T), b = (int)(bt / T);
-    const int32_t* sel = block_idx + (((size_t)b * G + g) * T + t) * k;
+    const size_t sel_row = (((size_t)b * G + g) * T + t) * k;
+    const int32_t* sel = block_idx + sel_row;
+    const int32_t* rv = rev + sel_row;
+    auto live = [&](int s) { return sel[s] >= 0 && rv[s] >= 0 && (long long)rv[s] < max_padded; };
     for (int h = 0; h < hg; ++h) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       for (int s = 0; s < k; ++s) {
-        if (sel[s] < 0) continue;
-        const uint2 raw = *reinterpret_cast<const uint2*>(dq_part + (((size_t)w * k + s) * hg + h) * 128 + lane * 4);
+        if (!live(s)) continue;
+        const uint2 raw = *reinterpret_cast<const uint2*>(dq_part + ((size_t)rv[s] * hg + h) * 128 + lane * 4);
         const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
         const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
         acc[0] += f0.x;
@@ -816,8 +845,8 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const __
     }
     float a0 = 0.f, a1 = 0.f, kl = 0.f;
     for (int s = 0; s < k; ++s) {
-      if (sel[s] < 0) continue;
-      const float2 v = *reinterpret_cast<const float2*>(dqi_part + ((size_t)w * k + s) * 64 + lane * 2);
+      if (!live(s)) continue;
+      const float2 v = *reinterpret_cast<const float2*>(dqi_part + (size_t)rv[s] * 64 + lane * 2);
       a0 += v.x;
       a1 += v.y;
       kl += kl_part[(size_t)w * k + s];
@@ -851,7 +880,8 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
                        const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
                        float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
                        uint8_t* ws, const WsLayout& L, cudaStream_t st) {
-  cudaError_t e = build_block_map(p, block_idx, ws, L, 1, 1 << 30, st);
+  const int npos = 64 / p.hg;  // queries per backward tile (64 (query, head) rows)
+  cudaError_t e = build_block_map(p, block_idx, ws, L, npos, (1 << 30) / npos, st);
   if (e != cudaSuccess) return e;
   int* err = reinterpret_cast<int*>(ws + L.err);
   int* counters = reinterpret_cast<int*>(ws + L.counters);
@@ -880,6 +910,20 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if (!encode_tmap(&mk, const_cast<void*>(K), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
     if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
+  CUtensorMap mdq, mdqi;
+  {
+    const uint64_t dims[2] = {128, (uint64_t)L.max_padded * p.hg};
+    const uint64_t strides[1] = {256};
+    const uint32_t box[2] = {32, 64};
+    if (!encode_tmap(&mdq, ws + L.dq_part, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
+    const uint64_t dims2[2] = {64, (uint64_t)L.max_padded};
+    const uint64_t strides2[1] = {256};
+    const uint32_t box2[2] = {32, (uint32_t)std::min(npos, 32)};
+    if (!encode_tmap(&mdqi, ws + L.dqi_part, 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return cudaErrorInvalidValue;
   }
   static bool attr = false;
@@ -941,16 +985,16 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.scale_idx = p.scale_idx;
   ba.kl_weight = kl_weight;
   switch (p.hg) {
-    case 1: bwd_kernel<1><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
-    case 2: bwd_kernel<2><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
-    case 4: bwd_kernel<4><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
-    default: bwd_kernel<8><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki); break;
+    case 1: bwd_kernel<1><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
+    case 2: bwd_kernel<2><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
+    case 4: bwd_kernel<4><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
+    default: bwd_kernel<8><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
   }
   count_launches(6);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   bwd_merge_kernel<<<(int)std::min<long long>((grows * 32 + 255) / 256, 16LL * sms), 256, 0, st>>>(
-      block_idx, ba.dq_part, ba.dqi_part, ba.kl_part, static_cast<float*>(dQ), static_cast<float*>(dq_idx), KL,
-      p.B, p.T, p.Hq, p.G, p.hg, p.k);
+      block_idx, reinterpret_cast<const int32_t*>(ws + L.rev), ba.dq_part, ba.dqi_part, ba.kl_part,
+      static_cast<float*>(dQ), static_cast<float*>(dq_idx), KL, p.B, p.T, p.Hq, p.G, p.hg, p.k, L.max_padded);
   const long long n2 = (long long)p.B * p.T * 32;
   dki_merge_kernel<<<(int)std::min<long long>((n2 + 255) / 256, 16LL * sms), 256, 0, st>>>(
       ba.dki_part, static_cast<float*>(dk_idx), p.B, p.T, p.G);

@@ -23,17 +23,20 @@
 // A second kernel merges the k partials of every (query, head):
 // LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) O_s.
 //
-// Warp roles (192 threads, one CTA per SM, persistent):
-//   warp 0      item fetch, K/V TMA, Q-row gathers (cp.async, all 32 lanes)
+// Warp roles (224 threads, one CTA per SM, persistent):
+//   warp 0      item fetch, K/V TMA, Q-row gathers for tile rows 0..63
+//   warp 6      Q-row gathers for tile rows 64..127
 //   warp 1      TMEM owner, UMMA issuer (one thread)
 //   warps 2..5  softmax + partial-output epilogue
+// The gather warps keep one tile's cp.async copies in flight while issuing the
+// next tile's, and publish a tile once its copies have landed.
 #include "msa_internal.h"
 #include "sm100.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;  // 2 gather warps, 1 UMMA warp, 4 softmax/epilogue warps
 constexpr int kQStages = 2;
 constexpr int kTile = 32768;  // 128 rows x 128 bf16, as two 64-column SW128 chunks
 constexpr int kChunk = 16384;
@@ -63,7 +66,7 @@ struct FwdShared {
   uint64_t p_full[2], p_free[2];
   uint64_t o_full[2], o_empty[2];
   int4 item[2];
-  int tile_t[128];  // producer scratch: query of each tile position
+  const __nv_bfloat16* tile_src[2][64];  // per gather warp: Q row base of each tile position (null: padding)
   uint32_t tmem_base;
   int abort;
 };
@@ -79,6 +82,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+template <int HG>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                       const __grid_constant__ CUtensorMap map_o) {
@@ -94,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 5);
+      mbar_init(&sh.it_empty[i], 6);
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 4);
       mbar_init(&sh.p_full[i], 4);
@@ -103,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.o_empty[i], 4);
     }
     for (int i = 0; i < kQStages; ++i) {
-      mbar_init(&sh.q_full[i], 32);
+      mbar_init(&sh.q_full[i], 64);
       mbar_init(&sh.q_empty[i], 1);
     }
     mbar_init(&sh.kv_full, 1);
@@ -120,17 +124,82 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   volatile int* abort_flag = &sh.abort;
-  const int P = a.pos_per_tile;
+  constexpr int P = 128 / HG;  // query positions per tile
   const int n_items = *a.n_items;
 
-  if (warp == 0) {
+  // Gather of one tile half: rows [64 * hf, 64 * hf + 64) = positions
+  // [P/2 * hf, P/2 * hf + P/2); 64 rows x 16 chunks of 16 bytes, 32 per lane.
+  auto gather_half = [&](int hf, int b, int g, const int4& item, int j, uint32_t qdst) {
+    const __nv_bfloat16** src_of = sh.tile_src[hf];
+    __syncwarp();  // the previous tile's loop has finished reading src_of
+    for (int q = lane; q < P / 2; q += 32) {
+      const int idx = j * P + hf * (P / 2) + q;
+      const __nv_bfloat16* ptr = nullptr;
+      if (idx < item.z) {
+        const int t = a.entries[item.y + idx] >> 8;
+        ptr = a.Q + (((size_t)b * a.T + t) * a.Hq + g * HG) * 128;
+      }
+      src_of[q] = ptr;
+    }
+    __syncwarp();
+    const int chunk = lane & 15;
+    const uint32_t dst0 = qdst + (chunk >> 3) * kChunk;
+#pragma unroll 8
+    for (int i = 0; i < 32; ++i) {
+      const int rl = 2 * i + (lane >> 4);  // row within the half
+      const int r = hf * 64 + rl;
+      const __nv_bfloat16* base = src_of[rl / HG];
+      const bool valid = base != nullptr;
+      const __nv_bfloat16* src = valid ? base + (rl % HG) * 128 + chunk * 8 : a.Q;
+      cp_async_16_zfill(dst0 + sw128_off(r, chunk & 7), src, valid);
+    }
+    cp_async_commit();
+  };
+
+  if (warp == 6) {
+    // ------------------------------------------------------------ second gather warp
+    uint32_t tj = 0;
+    int pend = -1;  // Q stage whose copies are in flight
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 331)) { *abort_flag = 1; break; }
+      const int4 item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item.x < 0) break;
+      const int bg = item.x / a.n;
+      const int b = bg / a.G, g = bg % a.G;
+      const int ntiles = (item.z + P - 1) / P;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int qs = tj % kQStages;
+        if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 332)) { ok = false; break; }
+        gather_half(1, b, g, item, j, smem_u32(sQ + qs * kTile));
+        if (pend >= 0) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&sh.q_full[pend]);
+        }
+        pend = qs;
+      }
+      if (pend >= 0) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        mbar_arrive(&sh.q_full[pend]);
+        pend = -1;
+      }
+      __syncwarp();
+      if (!ok) { *abort_flag = 1; break; }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
     }
     uint32_t tj = 0;
-    const int chunk = lane & 15;  // 16-byte chunk of a 256-byte head row
+    int pend = -1;
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -168,29 +237,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < ntiles; ++j, ++tj) {
         const int qs = tj % kQStages;
         if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 303)) { ok = false; break; }
-        const uint32_t dst0 = smem_u32(sQ + qs * kTile) + (chunk >> 3) * kChunk;
-        // stage the tile's queries first: the loads are independent and overlap
-        for (int p = lane; p < P; p += 32) {
-          const int idx = j * P + p;
-          sh.tile_t[p] = idx < item.z ? (a.entries[item.y + idx] >> 8) : -1;
+        gather_half(0, b, g, item, j, smem_u32(sQ + qs * kTile));
+        if (pend >= 0) {  // the previous tile's copies: complete, publish
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&sh.q_full[pend]);
         }
-        __syncwarp();
-#pragma unroll 8
-        for (int i = 0; i < 64; ++i) {
-          const int r = 2 * i + (lane >> 4);
-          const int p = r / a.hg, h = r - p * a.hg;
-          const int tq = sh.tile_t[p];
-          const bool valid = tq >= 0;
-          const __nv_bfloat16* src =
-              a.Q + ((((size_t)b * a.T + (valid ? tq : 0)) * a.Hq + g * a.hg + h) * 128 + chunk * 8);
-          cp_async_16_zfill(dst0 + sw128_off(r, chunk & 7), src, valid);
-        }
-        cp_async_commit();
+        pend = qs;
+      }
+      if (pend >= 0) {
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        mbar_arrive(&sh.q_full[qs]);
-        __syncwarp();
+        mbar_arrive(&sh.q_full[pend]);
+        pend = -1;
       }
+      __syncwarp();
       if (!ok) { *abort_flag = 1; break; }
     }
   } else if (warp == 1) {
@@ -252,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const int p_in_tile = row / a.hg;
+    const int p_in_tile = row / HG;
     uint32_t tj = 0;
     bool ok = true;
     // pending tile (softmax done, output not yet written)
@@ -356,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pm = mm;
         pl = l;
         pentry = entry;
-        prow0 = (item.w + j * P) * a.hg;
+        prow0 = (item.w + j * P) * HG;
       }
       // the last tile of the item is finished at the start of the next item's
       // first tile, or after the loop ends
@@ -467,12 +528,17 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
   if ((e = cudaMemsetAsync(a.counter, 0, sizeof(int), st)) != cudaSuccess) return e;
   static bool attr = false;
   if (!attr) {
-    if ((e = cudaFuncSetAttribute(sparse_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) !=
-        cudaSuccess)
-      return e;
+    for (auto f : {sparse_fwd_kernel<1>, sparse_fwd_kernel<2>, sparse_fwd_kernel<4>, sparse_fwd_kernel<8>})
+      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) != cudaSuccess)
+        return e;
     attr = true;
   }
-  sparse_fwd_kernel<<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo);
+  switch (p.hg) {
+    case 1: sparse_fwd_kernel<1><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
+    case 2: sparse_fwd_kernel<2><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
+    case 4: sparse_fwd_kernel<4><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
+    default: sparse_fwd_kernel<8><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
+  }
   count_launches(2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.T * p.G;
