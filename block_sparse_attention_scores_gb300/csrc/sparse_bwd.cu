@@ -325,12 +325,44 @@ constexpr int oSh = oGST + kKeyRows;           // BwdShared
 // TMEM columns
 constexpr uint32_t cS = 0, cDP = 64, cX = 128, cDV = 192, cDK = 320, cKI = 448;
 
+// Per (query, head) row of a tile: {LSE * log2 e, D, lse_px * log2 e, entry
+// bits (t << 8 | slot, -1 for padding)}, one 16-byte shared load per column.
 struct RowMeta {
-  float lse2[kRows];   // LSE * log2(e)
-  float dval[kRows];   // D
-  float lsepx2[kRows]; // lse_px * log2(e) (per row of the query)
-  int entry[kRows];    // (t << 8 | slot), -1 for padding rows
+  float4 rec[kRows];
 };
+
+// Sum over the 32 lanes of NV per-lane values, with a butterfly that halves
+// the values a lane keeps at each step (NV - 1 shuffles instead of 5 NV), then
+// add each sum into acc[] (one shared atomic per value, distinct addresses).
+template <int NV>
+__device__ __forceinline__ void lanes_sum_add(float (&v)[NV], int lane, float* acc) {
+  int base = 0;
+#pragma unroll
+  for (int s = 0; s < 5; ++s) {
+    const int off = 16 >> s;
+    constexpr int kNV = NV;
+    const int n = kNV >> s;
+    if (n >= 2) {
+      const int half = n >> 1;
+      const bool up = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < (kNV >> (s + 1)); ++i) {
+        const float send = up ? v[i] : v[i + half];
+        const float keep = up ? v[i + half] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+      if (up) base += half;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    }
+  }
+  constexpr int kKeep = NV >= 32 ? NV / 32 : 1;
+  constexpr int kDup = NV >= 32 ? 1 : 32 / NV;  // lanes holding the same sums
+  if ((lane & (kDup - 1)) == 0) {
+#pragma unroll
+    for (int i = 0; i < kKeep; ++i) atomicAdd(&acc[base + i], v[i]);
+  }
+}
 
 struct BwdArgs {
   const __nv_bfloat16* Q;
@@ -358,11 +390,11 @@ struct BwdShared {
   uint64_t it_full[2], it_empty[2];
   uint64_t kv_full, kv_empty;
   uint64_t g_full[2], g_empty[2];
-  uint64_t ph1_full, ph1_done, ph2_full, ph2_done;
+  uint64_t ph1_full, p_ready, ds_ready, gs_ready, ph2_full, ph2_done;
   uint64_t acc_free;
   uint64_t epi_sync;  // rendezvous of the 4 epilogue warps
   RowMeta meta[2];
-  float kl_acc[kRows];  // per-query KL partial of the current tile (summed over the 4 warps)
+  float kl_acc[2][kRows];  // per-query KL partial of a tile (by tile parity), summed over the 4 warps
   int4 item[2];
   uint32_t tmem_base;
   int abort;
@@ -383,7 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + oSh);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRows; ++i) sh.kl_acc[i] = 0.f;
+    for (int i = 0; i < kRows; ++i) sh.kl_acc[0][i] = sh.kl_acc[1][i] = 0.f;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
       mbar_init(&sh.it_empty[i], 5);
@@ -393,7 +425,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&sh.kv_full, 1);
     mbar_init(&sh.kv_empty, 1);
     mbar_init(&sh.ph1_full, 1);
-    mbar_init(&sh.ph1_done, 4);
+    mbar_init(&sh.p_ready, 4);
+    mbar_init(&sh.ds_ready, 4);
+    mbar_init(&sh.gs_ready, 4);
     mbar_init(&sh.ph2_full, 1);
     mbar_init(&sh.ph2_done, 4);
     mbar_init(&sh.acc_free, 4);
@@ -480,13 +514,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             x2[u] = e2[u] >= 0 ? a.lse_px[((size_t)b * a.T + t2[u]) * a.G + g] : 0.f;
           }
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = lane + 32 * u;
-            m.entry[r] = e2[u];
-            m.lse2[r] = l2[u] * kLog2e;
-            m.dval[r] = d2[u];
-            m.lsepx2[r] = x2[u] * kLog2e;
-          }
+          for (int u = 0; u < 2; ++u)
+            m.rec[lane + 32 * u] = make_float4(l2[u] * kLog2e, d2[u], x2[u] * kLog2e, __int_as_float(e2[u]));
         }
         __syncwarp();
         // Q and dO rows: 64 rows x 16 chunks each; lane -> (row half, chunk)
@@ -495,7 +524,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int i = 0; i < 32; ++i) {
           const int r = 2 * i + (lane >> 4);
           const int h = r % hg;
-          const int e = m.entry[r];
+          const int e = __float_as_int(m.rec[r].w);
           const bool valid = e >= 0;
           const int t = valid ? (e >> 8) : 0;
           const size_t off = (((size_t)b * a.T + t) * a.Hq + g * hg + h) * 128 + chunk * 8;
@@ -507,7 +536,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 4
         for (int i = 0; i < 16; ++i) {
           const int r = 4 * i + (lane >> 3), ch = lane & 7;
-          const int e = m.entry[r];
+          const int e = __float_as_int(m.rec[r].w);
           const bool valid = e >= 0;
           const int t = valid ? (e >> 8) : 0;
           cp_async_16_zfill(qi0 + sw128_off(r, ch), a.q_idx + ((((size_t)b * a.T + t) * a.G + g) * 64 + ch * 8),
@@ -565,32 +594,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 32, 16, 1024, kSw128),
                          make_sdesc(gqi + ks * 32, 16, 1024, kSw128), id_sT, ks > 0);
           umma_commit(&sh.ph1_full);
-          // phase 2 once P^T, dS^T, gs^T are in shared memory
-          if (!mbar_wait(&sh.ph1_done, tj & 1, a.err, 515)) { ok = false; break; }
+          // phase 2, released in three steps by the epilogue: P^T (dV), dS^T
+          // (dK, dQ^T), gs^T (dk_idx, dq_idx^T)
+          if (!mbar_wait(&sh.p_ready, tj & 1, a.err, 515)) { ok = false; break; }
           if (j == 0 && !mbar_wait(&sh.acc_free, (it & 1) ^ 1, a.err, 516)) { ok = false; break; }
           tc_fence_after();
           const uint32_t acc = (j > 0) ? 1u : 0u;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            // dV += P^T dO, dK += dS^T Q   (K = 64 rows, 16 per step)
+            // dV += P^T dO with P = hi + lo   (K = 64 rows, 16 per step)
             umma_bf16_ss(tmem + cDV, make_sdesc(pt0 + ks * 32, 16, 1024, kSw128),
                          make_sdesc(gdo + ks * 2048, kRowChunk, 1024, kSw128), id_acc, acc | (ks > 0));
             umma_bf16_ss(tmem + cDV, make_sdesc(pl0 + ks * 32, 16, 1024, kSw128),
                          make_sdesc(gdo + ks * 2048, kRowChunk, 1024, kSw128), id_acc, 1u);
+          }
+          if (!mbar_wait(&sh.ds_ready, tj & 1, a.err, 517)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // dK += dS^T Q
             umma_bf16_ss(tmem + cDK, make_sdesc(dst0 + ks * 32, 16, 1024, kSw128),
                          make_sdesc(gq + ks * 2048, kRowChunk, 1024, kSw128), id_acc, acc | (ks > 0));
-            // dk_idx += gs^T QI
-            umma_bf16_ss(tmem + cKI, make_sdesc(gst0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gqi + ks * 2048, 16, 1024, kSw128), id_ki, acc | (ks > 0));
-          }
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            // dQ^T = K^T dS^T, dq_idx^T = KI^T gs^T   (K = 128 keys, 16 per step)
+          for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T   (K = 128 keys)
             umma_bf16_ss(tmem + cS, make_sdesc(k0 + ks * 2048, kKV / 2, 1024, kSw128),
                          make_sdesc(dst0 + ks * 2048, 16, 1024, kSw128), id_tr, ks > 0);
+          if (!mbar_wait(&sh.gs_ready, tj & 1, a.err, 518)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // dk_idx += gs^T QI
+            umma_bf16_ss(tmem + cKI, make_sdesc(gst0 + ks * 32, 16, 1024, kSw128),
+                         make_sdesc(gqi + ks * 2048, 16, 1024, kSw128), id_ki, acc | (ks > 0));
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)  // dq_idx^T = KI^T gs^T
             umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 2048, kKIb, 1024, kSw128),
                          make_sdesc(gst0 + ks * 2048, 16, 1024, kSw128), id_tr, ks > 0);
-          }
           umma_commit(&sh.ph2_full);
           umma_commit(&sh.g_empty[gb]);
         }
@@ -627,87 +664,103 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // its staging for the previous tile's partial stores: wait until read
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
-        // ---- phase-1 epilogue: 64 rows, 16 at a time
-        for (int q = 0; q < 4; ++q) {
-          float sv[16], dp[16], xv[16];
-          tmem_ld16(tmem + lane_off + cS + q * 16, sv);
-          tmem_ld16(tmem + lane_off + cDP + q * 16, dp);
-          tmem_ld16(tmem + lane_off + cX + q * 16, xv);
-          tmem_wait_ld();
-          float pv[16], dsv[16], gv[16];
+        // ---- phase-1 epilogue in three stages, each handing work to the
+        // UMMA warp as soon as its operand is in shared memory
+        float pv[kRows];
+        {  // stage A: P = exp(s - LSE) on visible keys; P^T as bf16 high + low parts
+          float sv[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int r = q * 16 + i;
-            const int e = m.entry[r];
-            const bool vis = e >= 0 && key <= (e >> 8);
-            pv[i] = vis ? fast_exp2(sv[i] * a.scale_log2 - m.lse2[r]) : 0.f;
-            dsv[i] = pv[i] * (dp[i] - m.dval[r]) * a.scale;
-          }
-          // index branch: one value per query (the first head row of each query)
+          for (int q = 0; q < 2; ++q) {
+            tmem_ld32(tmem + lane_off + cS + q * 32, sv);
+            tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            gv[i] = 0.f;
-            xv[i] = xv[i] * a.scale_idx_log2;  // log2-domain index score
+            for (int i = 0; i < 32; ++i) {
+              const float4 mr = m.rec[q * 32 + i];
+              const int e = __float_as_int(mr.w);
+              const bool vis = e >= 0 && key <= (e >> 8);
+              pv[q * 32 + i] = vis ? fast_exp2(sv[i] * a.scale_log2 - mr.x) : 0.f;
+            }
           }
 #pragma unroll
-          for (int i0 = 0; i0 < 16; i0 += hg) {
-            const int r = q * 16 + i0;
-            const int e = m.entry[r];
-            const bool vis = e >= 0 && key <= (e >> 8);
-            float pm = 0.f;
-#pragma unroll
-            for (int h = 0; h < hg; ++h) pm += pv[i0 + h];
-            pm *= 1.f / (float)hg;
-            const float lpx2 = xv[i0] - m.lsepx2[r];  // log2 p_px
-            const float ppx = vis ? fast_exp2(lpx2) : 0.f;
-            gv[i0] = vis ? a.kl_weight * (ppx - pm) * a.scale_idx : 0.f;
-            float term = 0.f;
-            if (vis && pm > 0.f) term = pm * (__log2f(pm) - lpx2) * kLn2;
-            // reduce over the 128 keys: warp shuffle, then across the 4 warps
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
-            if (lane == 0) atomicAdd(&sh.kl_acc[r / hg], term);
-          }
-          // write the 16 columns of this chunk: two 16-byte pieces per image
-#pragma unroll
-          for (int hlf = 0; hlf < 2; ++hlf) {
-            const int c16 = q * 2 + hlf;
-            uint4 v;
+          for (int c16 = 0; c16 < 8; ++c16) {
             float lo[8];
 #pragma unroll
-            for (int z = 0; z < 8; ++z) lo[z] = pv[8 * hlf + z] - __bfloat162float(__float2bfloat16_rn(pv[8 * hlf + z]));
-            v.x = pack_bf16(pv[8 * hlf + 0], pv[8 * hlf + 1]);
-            v.y = pack_bf16(pv[8 * hlf + 2], pv[8 * hlf + 3]);
-            v.z = pack_bf16(pv[8 * hlf + 4], pv[8 * hlf + 5]);
-            v.w = pack_bf16(pv[8 * hlf + 6], pv[8 * hlf + 7]);
-            *reinterpret_cast<uint4*>(smem + oPT + sw128_off(kk, c16)) = v;
-            v = make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
+            for (int z = 0; z < 8; ++z)
+              lo[z] = pv[8 * c16 + z] - __bfloat162float(__float2bfloat16_rn(pv[8 * c16 + z]));
+            *reinterpret_cast<uint4*>(smem + oPT + sw128_off(kk, c16)) =
+                make_uint4(pack_bf16(pv[8 * c16 + 0], pv[8 * c16 + 1]), pack_bf16(pv[8 * c16 + 2], pv[8 * c16 + 3]),
+                           pack_bf16(pv[8 * c16 + 4], pv[8 * c16 + 5]), pack_bf16(pv[8 * c16 + 6], pv[8 * c16 + 7]));
+            *reinterpret_cast<uint4*>(smem + oPL + sw128_off(kk, c16)) =
+                make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
                            pack_bf16(lo[6], lo[7]));
-            *reinterpret_cast<uint4*>(smem + oPL + sw128_off(kk, c16)) = v;
-            v.x = pack_bf16(dsv[8 * hlf + 0], dsv[8 * hlf + 1]);
-            v.y = pack_bf16(dsv[8 * hlf + 2], dsv[8 * hlf + 3]);
-            v.z = pack_bf16(dsv[8 * hlf + 4], dsv[8 * hlf + 5]);
-            v.w = pack_bf16(dsv[8 * hlf + 6], dsv[8 * hlf + 7]);
-            *reinterpret_cast<uint4*>(smem + oDST + sw128_off(kk, c16)) = v;
-            v.x = pack_bf16(gv[8 * hlf + 0], gv[8 * hlf + 1]);
-            v.y = pack_bf16(gv[8 * hlf + 2], gv[8 * hlf + 3]);
-            v.z = pack_bf16(gv[8 * hlf + 4], gv[8 * hlf + 5]);
-            v.w = pack_bf16(gv[8 * hlf + 6], gv[8 * hlf + 7]);
-            *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, c16)) = v;
           }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.p_ready);
         }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        if (!warps_sync(&sh.epi_sync, sync_phase, a.err, 525)) { ok = false; break; }
-        if (lane == 0) mbar_arrive(&sh.ph1_done);
-        // KL partial per query of the tile
-        if (kk < npos) {
-          const int r = kk * hg;
-          const int e = m.entry[r];
-          if (e >= 0) {
-            a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[kk];
+        {  // stage B: dS = P (dP - D) * scale
+          float dp[32];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            tmem_ld32(tmem + lane_off + cDP + q * 32, dp);
+            tmem_wait_ld();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              float d8[8];
+#pragma unroll
+              for (int z = 0; z < 8; ++z) {
+                const int r = q * 32 + c * 8 + z;
+                d8[z] = pv[r] * (dp[c * 8 + z] - m.rec[r].y) * a.scale;
+              }
+              *reinterpret_cast<uint4*>(smem + oDST + sw128_off(kk, q * 4 + c)) =
+                  make_uint4(pack_bf16(d8[0], d8[1]), pack_bf16(d8[2], d8[3]), pack_bf16(d8[4], d8[5]),
+                             pack_bf16(d8[6], d8[7]));
+            }
           }
-          sh.kl_acc[kk] = 0.f;  // next writers come after the phase-2 rendezvous
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.ds_ready);
+        }
+        {  // stage C: index branch, one column per query (its first head row)
+          float xv[32];
+          float gv[kRows];
+          float term[npos];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            tmem_ld32(tmem + lane_off + cX + q * 32, xv);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int r = q * 32 + i;
+              gv[r] = 0.f;
+              if (r % hg == 0) {
+                const float4 mr = m.rec[r];
+                const int e = __float_as_int(mr.w);
+                const bool vis = e >= 0 && key <= (e >> 8);
+                float pm = 0.f;
+#pragma unroll
+                for (int h = 0; h < hg; ++h) pm += pv[r + h];
+                pm *= 1.f / (float)hg;
+                const float lpx2 = xv[i] * a.scale_idx_log2 - mr.z;  // log2 p_px
+                const float ppx = vis ? fast_exp2(lpx2) : 0.f;
+                gv[r] = vis ? a.kl_weight * (ppx - pm) * a.scale_idx : 0.f;
+                term[r / hg] = (vis && pm > 0.f) ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
+              }
+            }
+          }
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16)
+            *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, c16)) =
+                make_uint4(pack_bf16(gv[8 * c16 + 0], gv[8 * c16 + 1]), pack_bf16(gv[8 * c16 + 2], gv[8 * c16 + 3]),
+                           pack_bf16(gv[8 * c16 + 4], gv[8 * c16 + 5]), pack_bf16(gv[8 * c16 + 6], gv[8 * c16 + 7]));
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.gs_ready);
+          // KL terms summed over the 128 keys (lanes here, warps via shared atomics)
+          lanes_sum_add<npos>(term, lane, sh.kl_acc[tj & 1]);
         }
         // ---- phase-2 epilogue: dQ^T (lane = d), dq_idx^T (lane = e < 64)
         // Partials are in tile order: this tile's 64 (query, head) rows are
@@ -762,6 +815,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         tc_fence_before();
         if (!warps_sync(&sh.epi_sync, sync_phase, a.err, 526)) { ok = false; break; }
+        // every warp has added its KL terms: write the per-query partials
+        if (kk < npos) {
+          const int e = __float_as_int(m.rec[kk * hg].w);
+          if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[tj & 1][kk];
+          sh.kl_acc[tj & 1][kk] = 0.f;  // reused by tile tj + 2, after the next rendezvous
+        }
         if (lane == 0) {
           mbar_arrive(&sh.ph2_done);
           mbar_arrive(&sh.g_empty[gb]);
