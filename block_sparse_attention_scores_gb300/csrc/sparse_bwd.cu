@@ -869,13 +869,44 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // One warp per (b, t, g): dQ rows of its heads, dq_idx and KL from the slots.
+// Loads n consecutive bf16 values (n = 4 or a multiple of 8) as fp32.
+template <int N>
+__device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&out)[N]) {
+  if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) {
+      const uint4 raw = reinterpret_cast<const uint4*>(src)[q];
+      const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const float2 f = __bfloat1622float2(v[z]);
+        out[q * 8 + 2 * z] = f.x;
+        out[q * 8 + 2 * z + 1] = f.y;
+      }
+    }
+  } else {
+    static_assert(N == 4, "4 or a multiple of 8 values");
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
+    out[0] = f0.x;
+    out[1] = f0.y;
+    out[2] = f1.x;
+    out[3] = f1.y;
+  }
+}
+
 // The partials of (b, g, t, slot) sit at padded entry rev[(b*G + g)*T + t][slot]
-// (dQ: rows entry*hg + h; dq_idx: row entry); KL partials at (b, t, g, slot).
+// (dQ: HG contiguous rows entry*HG + h; dq_idx: row entry); KL partials at
+// (b, t, g, slot). One warp per (b, t, g); every lane owns 4 * HG consecutive
+// dQ values and 2 dq_idx values.
+template <int HG>
 __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
                                  const __nv_bfloat16* __restrict__ dq_part, const float* __restrict__ dqi_part,
                                  const float* __restrict__ kl_part, float* __restrict__ dQ,
                                  float* __restrict__ dq_idx, float* __restrict__ KL, int B, int T, int Hq, int G,
-                                 int hg, int k, long long max_padded) {
+                                 int k, long long max_padded) {
+  constexpr int kPer = 4 * HG;
   const long long rows = (long long)B * T * G;
   const int lane = threadIdx.x & 31;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
@@ -884,34 +915,44 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
     const long long bt = w / G;
     const int t = (int)(bt % T), b = (int)(bt / T);
     const size_t sel_row = (((size_t)b * G + g) * T + t) * k;
-    const int32_t* sel = block_idx + sel_row;
-    const int32_t* rv = rev + sel_row;
-    auto live = [&](int s) { return sel[s] >= 0 && rv[s] >= 0 && (long long)rv[s] < max_padded; };
-    for (int h = 0; h < hg; ++h) {
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < k; ++s) {
-        if (!live(s)) continue;
-        const uint2 raw = *reinterpret_cast<const uint2*>(dq_part + ((size_t)rv[s] * hg + h) * 128 + lane * 4);
-        const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
-        acc[0] += f0.x;
-        acc[1] += f0.y;
-        acc[2] += f1.x;
-        acc[3] += f1.y;
+    int rv_own[2];
+    float kl_own = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int sidx = lane + 32 * u;
+      int r = -1;
+      if (sidx < k && block_idx[sel_row + sidx] >= 0) {
+        r = rev[sel_row + sidx];
+        if (r >= 0 && (long long)r >= max_padded) r = -1;
       }
-      *reinterpret_cast<float4*>(dQ + (((size_t)b * T + t) * Hq + g * hg + h) * 128 + lane * 4) =
-          make_float4(acc[0], acc[1], acc[2], acc[3]);
+      rv_own[u] = r;
+      if (r >= 0) kl_own += kl_part[(size_t)w * k + sidx];
     }
-    float a0 = 0.f, a1 = 0.f, kl = 0.f;
-    for (int s = 0; s < k; ++s) {
-      if (!live(s)) continue;
-      const float2 v = *reinterpret_cast<const float2*>(dqi_part + (size_t)rv[s] * 64 + lane * 2);
-      a0 += v.x;
-      a1 += v.y;
-      kl += kl_part[(size_t)w * k + s];
+    float acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      for (int src = 0; src < 32 && 32 * u + src < k; ++src) {
+        const int r = __shfl_sync(0xffffffffu, rv_own[u], src);
+        if (r < 0) continue;
+        float v[kPer];
+        load_bf16_row<kPer>(dq_part + (size_t)r * HG * 128 + lane * kPer, v);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] += v[i];
+        const float2 vi = *reinterpret_cast<const float2*>(dqi_part + (size_t)r * 64 + lane * 2);
+        a0 += vi.x;
+        a1 += vi.y;
+      }
     }
+    float4* dst = reinterpret_cast<float4*>(dQ + (((size_t)b * T + t) * Hq + g * HG) * 128) + lane * (kPer / 4);
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q) dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
     *reinterpret_cast<float2*>(dq_idx + (size_t)w * 64 + lane * 2) = make_float2(a0, a1);
-    if (lane == 0) KL[((size_t)b * G + g) * T + t] = kl;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kl_own += __shfl_xor_sync(0xffffffffu, kl_own, o);
+    if (lane == 0) KL[((size_t)b * G + g) * T + t] = kl_own;
   }
 }
 
@@ -1051,9 +1092,18 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   }
   count_launches(6);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  bwd_merge_kernel<<<(int)std::min<long long>((grows * 32 + 255) / 256, 16LL * sms), 256, 0, st>>>(
-      block_idx, reinterpret_cast<const int32_t*>(ws + L.rev), ba.dq_part, ba.dqi_part, ba.kl_part,
-      static_cast<float*>(dQ), static_cast<float*>(dq_idx), KL, p.B, p.T, p.Hq, p.G, p.hg, p.k, L.max_padded);
+  {
+    const int grid = (int)std::min<long long>((grows * 32 + 255) / 256, 16LL * sms);
+    const int32_t* rev = reinterpret_cast<const int32_t*>(ws + L.rev);
+    float* dQf = static_cast<float*>(dQ);
+    float* dqif = static_cast<float*>(dq_idx);
+    switch (p.hg) {
+      case 1: bwd_merge_kernel<1><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+      case 2: bwd_merge_kernel<2><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+      case 4: bwd_merge_kernel<4><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+      default: bwd_merge_kernel<8><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    }
+  }
   const long long n2 = (long long)p.B * p.T * 32;
   dki_merge_kernel<<<(int)std::min<long long>((n2 + 255) / 256, 16LL * sms), 256, 0, st>>>(
       ba.dki_part, static_cast<float*>(dk_idx), p.B, p.T, p.G);

@@ -23,11 +23,12 @@
 // A second kernel merges the k partials of every (query, head):
 // LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) O_s.
 //
-// Warp roles (224 threads, one CTA per SM, persistent):
+// Warp roles (352 threads, one CTA per SM, persistent):
 //   warp 0      item fetch, K/V TMA, Q-row gathers for tile rows 0..63
-//   warp 6      Q-row gathers for tile rows 64..127
+//   warp 10     Q-row gathers for tile rows 64..127
 //   warp 1      TMEM owner, UMMA issuer (one thread)
-//   warps 2..5  softmax + partial-output epilogue
+//   warps 2..9  softmax + partial-output epilogue, two warpgroups that take
+//               even and odd tiles (ping-pong over the two S/O/P buffers)
 // The gather warps keep one tile's cp.async copies in flight while issuing the
 // next tile's, and publish a tile once its copies have landed.
 #include "msa_internal.h"
@@ -36,7 +37,7 @@
 namespace msa {
 namespace {
 
-constexpr int kThreads = 224;  // 2 gather warps, 1 UMMA warp, 4 softmax/epilogue warps
+constexpr int kThreads = 352;  // 2 gather warps, 1 UMMA warp, 2 x 4 softmax/epilogue warps
 constexpr int kQStages = 2;
 constexpr int kTile = 32768;  // 128 rows x 128 bf16, as two 64-column SW128 chunks
 constexpr int kChunk = 16384;
@@ -98,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 6);
+      mbar_init(&sh.it_empty[i], 10);
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 4);
       mbar_init(&sh.p_full[i], 4);
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cp_async_commit();
   };
 
-  if (warp == 6) {
+  if (warp == 10) {
     // ------------------------------------------------------------ second gather warp
     uint32_t tj = 0;
     int pend = -1;  // Q stage whose copies are in flight
@@ -310,48 +311,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // Two warpgroups ping-pong: warpgroup wg owns the tiles tj with
+    // (tj & 1) == wg, hence S/O TMEM buffer wg and P buffer wg.
+    const int wg = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int p_in_tile = row / HG;
+    const uint32_t s_col = wg * 128, o_col = 256 + wg * 128;
+    uint8_t* pbuf = sP + wg * kTile;
     uint32_t tj = 0;
     bool ok = true;
-    // pending tile (softmax done, output not yet written)
+    // pending tile of this warpgroup (softmax done, output not yet written)
+    bool pending = false;
+    uint32_t pu = 0;
     float pm = 0.f, pl = 0.f;
     int pentry = -1;
-    int prow0 = 0;  // first partial-output row of the pending tile
+    int prow0 = 0;
     // Partial outputs live in tile order: the tile's rows are consecutive, so
     // each warp stages its 32 normalised rows (bf16, SW128 image) in the P
     // buffer the O MMA has finished with and writes them with one TMA store
     // per 64-column chunk.
-    auto epilogue = [&](uint32_t u) -> bool {
-      const int sb = u & 1;
-      if (!mbar_wait(&sh.o_full[sb], (u >> 1) & 1, a.err, 321)) return false;
+    auto epilogue = [&]() -> bool {
+      if (!mbar_wait(&sh.o_full[wg], (pu >> 1) & 1, a.err, 321)) return false;
       tc_fence_after();
-      float o[128];
+      const float inv = pentry >= 0 ? 1.f / pl : 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + 256 + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(o + q * 32));
-      tmem_wait_ld();
+      for (int q = 0; q < 4; ++q) {
+        float o[32];
+        tmem_ld32(tmem + lane_off + o_col + q * 32, o);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int c16 = q * 4 + c;
+          *reinterpret_cast<uint4*>(pbuf + (c16 >> 3) * kChunk + sw128_off(row, c16 & 7)) = make_uint4(
+              pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv), pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
+              pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+        }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.o_empty[sb]);
-      const float inv = pentry >= 0 ? 1.f / pl : 0.f;
-      uint8_t* stage = sP + sb * kTile;
-#pragma unroll
-      for (int q = 0; q < 16; ++q) {
-        uint4 v;
-        v.x = pack_bf16(o[8 * q + 0] * inv, o[8 * q + 1] * inv);
-        v.y = pack_bf16(o[8 * q + 2] * inv, o[8 * q + 3] * inv);
-        v.z = pack_bf16(o[8 * q + 4] * inv, o[8 * q + 5] * inv);
-        v.w = pack_bf16(o[8 * q + 6] * inv, o[8 * q + 7] * inv);
-        *reinterpret_cast<uint4*>(stage + (q >> 3) * kChunk + sw128_off(row, q & 7)) = v;
-      }
+      if (lane == 0) mbar_arrive(&sh.o_empty[wg]);
       if (pentry >= 0) a.lse_part[(size_t)prow0 + row] = (pm + __log2f(pl)) * kLn2;
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        tma_store_2d(&map_o, stage + quarter * 4096, 0, prow0 + quarter * 32);
-        tma_store_2d(&map_o, stage + kChunk + quarter * 4096, 64, prow0 + quarter * 32);
+        tma_store_2d(&map_o, pbuf + quarter * 4096, 0, prow0 + quarter * 32);
+        tma_store_2d(&map_o, pbuf + kChunk + quarter * 4096, 64, prow0 + quarter * 32);
         bulk_commit();
       }
       return true;
@@ -367,62 +373,69 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c = item.x % a.n;
       const int ntiles = (item.z + P - 1) / P;
       for (int j = 0; j < ntiles; ++j, ++tj) {
-        const int sb = tj & 1;
+        if ((int)(tj & 1) != wg) continue;
         const int idx = j * P + p_in_tile;
         const int entry = idx < item.z ? a.entries[item.y + idx] : -1;
         const int lim = entry >= 0 ? (entry >> 8) - c * 128 : -1;  // last visible key column
-        if (!mbar_wait(&sh.s_full[sb], (tj >> 1) & 1, a.err, 323)) { ok = false; break; }
+        if (!mbar_wait(&sh.s_full[wg], (tj >> 1) & 1, a.err, 323)) { ok = false; break; }
         tc_fence_after();
-        float x[128];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(x + q * 32));
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
+        // pass 1: row max over the visible keys
         float m = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          x[i] = (i <= lim) ? x[i] * a.scale_log2 : -INFINITY;
-          m = fmaxf(m, x[i]);
-        }
-        const float mm = (m == -INFINITY) ? 0.f : m;
-        float l = 0.f;
+        for (int q = 0; q < 4; ++q) {
+          float x[32];
+          tmem_ld32(tmem + lane_off + s_col + q * 32, x);
+          tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          x[i] = fast_exp2(x[i] - mm);
-          l += x[i];
+          for (int i = 0; i < 32; ++i)
+            if (q * 32 + i <= lim) m = fmaxf(m, x[i]);
         }
-        // P[sb] is free once the O MMA of tile tj-2 has read it and this
+        const float mm = (m == -INFINITY) ? 0.f : m * a.scale_log2;
+        // Tile tj-2 (same warpgroup, same P buffer) is finished first: its O
+        // is staged through P buffer wg, so it must leave before P(tj) goes in.
+        if (pending && !epilogue()) { ok = false; break; }
+        pending = false;
+        // P buffer wg is free once the O MMA of tile tj-2 has read it and this
         // warp's TMA store of tile tj-2's partial rows has read its staging
-        if (!mbar_wait(&sh.p_free[sb], ((tj >> 1) & 1) ^ 1, a.err, 324)) { ok = false; break; }
+        if (!mbar_wait(&sh.p_free[wg], ((tj >> 1) & 1) ^ 1, a.err, 324)) { ok = false; break; }
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
-        uint8_t* prow = sP + sb * kTile;
+        // pass 2: P = exp2(s * scale * log2 e - max), row sum, bf16 image
+        float l = 0.f;
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          uint4 v;
-          v.x = pack_bf16(x[8 * q + 0], x[8 * q + 1]);
-          v.y = pack_bf16(x[8 * q + 2], x[8 * q + 3]);
-          v.z = pack_bf16(x[8 * q + 4], x[8 * q + 5]);
-          v.w = pack_bf16(x[8 * q + 6], x[8 * q + 7]);
-          *reinterpret_cast<uint4*>(prow + (q >> 3) * kChunk + sw128_off(row, q & 7)) = v;
+        for (int q = 0; q < 4; ++q) {
+          float x[32];
+          tmem_ld32(tmem + lane_off + s_col + q * 32, x);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            x[i] = (q * 32 + i <= lim) ? fast_exp2(x[i] * a.scale_log2 - mm) : 0.f;
+            l += x[i];
+          }
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c16 = q * 4 + cc;
+            *reinterpret_cast<uint4*>(pbuf + (c16 >> 3) * kChunk + sw128_off(row, c16 & 7)) =
+                make_uint4(pack_bf16(x[8 * cc + 0], x[8 * cc + 1]), pack_bf16(x[8 * cc + 2], x[8 * cc + 3]),
+                           pack_bf16(x[8 * cc + 4], x[8 * cc + 5]), pack_bf16(x[8 * cc + 6], x[8 * cc + 7]));
+          }
         }
+        tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.p_full[sb]);
-        if (j > 0 || tj > 0) {
-          if (tj > 0 && !epilogue(tj - 1)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive(&sh.s_empty[wg]);
+          mbar_arrive(&sh.p_full[wg]);
         }
+        pending = true;
+        pu = tj;
         pm = mm;
         pl = l;
         pentry = entry;
         prow0 = (item.w + j * P) * HG;
       }
-      // the last tile of the item is finished at the start of the next item's
-      // first tile, or after the loop ends
     }
-    if (ok && tj > 0) ok = epilogue(tj - 1);
+    if (ok && pending) ok = epilogue();
     if (lane == 0) bulk_wait_all();
     __syncwarp();
     if (!ok) *abort_flag = 1;
@@ -434,52 +447,113 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// One warp per (b, t, g): merge the k partials of each of the hg heads. The
-// partial of (b, g, t, slot) sits at padded entry rev[(b*G + g)*T + t][slot].
+// Loads n consecutive bf16 values (n = 4 or a multiple of 8) as fp32.
+template <int N>
+__device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&out)[N]) {
+  if constexpr (N % 8 == 0) {
+#pragma unroll
+    for (int q = 0; q < N / 8; ++q) {
+      const uint4 raw = reinterpret_cast<const uint4*>(src)[q];
+      const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+      for (int z = 0; z < 4; ++z) {
+        const float2 f = __bfloat1622float2(v[z]);
+        out[q * 8 + 2 * z] = f.x;
+        out[q * 8 + 2 * z + 1] = f.y;
+      }
+    }
+  } else {
+    static_assert(N == 4, "4 or a multiple of 8 values");
+    const uint2 raw = *reinterpret_cast<const uint2*>(src);
+    const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
+    out[0] = f0.x;
+    out[1] = f0.y;
+    out[2] = f1.x;
+    out[3] = f1.y;
+  }
+}
+
+// One warp per (b, t, g): merge the k partials of each of the HG heads. The
+// partial of (b, g, t, slot) sits at padded entry rev[(b*G + g)*T + t][slot];
+// its HG head rows are one contiguous HG * 256-byte run. Lane s reads the HG
+// partial LSEs of slots s and s + 32 once; every lane then owns 4 * HG
+// consecutive output values (head lane / (32 / HG)).
+template <int HG>
 __global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
                                  const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
                                  __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int B, int T, int Hq, int G,
-                                 int hg, int k, long long max_padded) {
+                                 int k, long long max_padded) {
+  constexpr int kPer = 4 * HG;  // output values per lane
+  constexpr int kLanesPerHead = 32 / HG;
   const long long rows = (long long)B * T * G;
   const int lane = threadIdx.x & 31;
+  const int my_head = lane / kLanesPerHead;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
        w += ((long long)gridDim.x * blockDim.x) >> 5) {
     const int g = (int)(w % G);
     const long long bt = w / G;
     const int t = (int)(bt % T), b = (int)(bt / T);
     const size_t sel_row = (((size_t)b * G + g) * T + t) * k;
-    const int32_t* sel = block_idx + sel_row;
-    const int32_t* rv = rev + sel_row;
     // a slot counts only if the map placed it (rows that failed validation
     // keep -1 and are left unspecified, with the error word set)
-    auto live = [&](int s) { return sel[s] >= 0 && rv[s] >= 0 && (long long)rv[s] < max_padded; };
-    for (int h = 0; h < hg; ++h) {
-      float mx = -INFINITY;
-      for (int s = 0; s < k; ++s)
-        if (live(s)) mx = fmaxf(mx, lse_part[(size_t)rv[s] * hg + h]);
-      float z = 0.f;
-      for (int s = 0; s < k; ++s)
-        if (live(s)) z += expf(lse_part[(size_t)rv[s] * hg + h] - mx);
-      const float lse = mx + logf(z);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int s = 0; s < k; ++s) {
-        if (!live(s)) continue;
-        const size_t rid = (size_t)rv[s] * hg + h;
-        const float wgt = expf(lse_part[rid] - lse);
-        const uint2 raw = *reinterpret_cast<const uint2*>(o_part + rid * 128 + lane * 4);
-        const __nv_bfloat162* v = reinterpret_cast<const __nv_bfloat162*>(&raw);
-        const float2 f0 = __bfloat1622float2(v[0]), f1 = __bfloat1622float2(v[1]);
-        acc[0] += wgt * f0.x;
-        acc[1] += wgt * f0.y;
-        acc[2] += wgt * f1.x;
-        acc[3] += wgt * f1.y;
+    float l_own[2][HG];
+    int rv_own[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int sidx = lane + 32 * u;
+      int r = -1;
+      if (sidx < k && block_idx[sel_row + sidx] >= 0) {
+        r = rev[sel_row + sidx];
+        if (r >= 0 && (long long)r >= max_padded) r = -1;
       }
-      const size_t orow = ((size_t)b * T + t) * Hq + g * hg + h;
-      uint2 out;
-      out.x = pack_bf16(acc[0], acc[1]);
-      out.y = pack_bf16(acc[2], acc[3]);
-      *reinterpret_cast<uint2*>(O + orow * 128 + lane * 4) = out;
-      if (lane == 0) LSE[orow] = lse;
+      rv_own[u] = r;
+#pragma unroll
+      for (int h = 0; h < HG; ++h) l_own[u][h] = r >= 0 ? lse_part[(size_t)r * HG + h] : -INFINITY;
+    }
+    float lse[HG];
+#pragma unroll
+    for (int h = 0; h < HG; ++h) {
+      float mx = fmaxf(l_own[0][h], l_own[1][h]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      float z = (l_own[0][h] > -INFINITY ? expf(l_own[0][h] - mx) : 0.f) +
+                (l_own[1][h] > -INFINITY ? expf(l_own[1][h] - mx) : 0.f);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+      lse[h] = mx + logf(z);
+    }
+    float acc[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      for (int src = 0; src < 32 && 32 * u + src < k; ++src) {
+        const int r = __shfl_sync(0xffffffffu, rv_own[u], src);
+        if (r < 0) continue;
+        float wgt = 0.f;
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float lh = __shfl_sync(0xffffffffu, l_own[u][h], src);
+          if (h == my_head) wgt = expf(lh - lse[h]);
+        }
+        float v[kPer];
+        load_bf16_row<kPer>(o_part + (size_t)r * HG * 128 + lane * kPer, v);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) acc[i] += wgt * v[i];
+      }
+    }
+    const size_t orow0 = ((size_t)b * T + t) * Hq + g * HG;
+    uint2* dst = reinterpret_cast<uint2*>(O + orow0 * 128 + lane * kPer);
+#pragma unroll
+    for (int q = 0; q < kPer / 4; ++q)
+      dst[q] = make_uint2(pack_bf16(acc[q * 4 + 0], acc[q * 4 + 1]), pack_bf16(acc[q * 4 + 2], acc[q * 4 + 3]));
+    if (lane < HG) {
+      float v = lse[0];
+#pragma unroll
+      for (int h = 1; h < HG; ++h)
+        if (lane == h) v = lse[h];
+      LSE[orow0 + lane] = v;
     }
   }
 }
@@ -543,9 +617,14 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.T * p.G;
   const int grid = (int)std::min<long long>((rows * 32 + 255) / 256, 16LL * num_sms());
-  fwd_merge_kernel<<<grid, 256, 0, st>>>(block_idx, reinterpret_cast<const int32_t*>(ws + L.rev), a.o_part,
-                                         a.lse_part, static_cast<__nv_bfloat16*>(O), LSE, p.B, p.T, p.Hq, p.G, p.hg,
-                                         p.k, L.max_padded);
+  const int32_t* rev = reinterpret_cast<const int32_t*>(ws + L.rev);
+  __nv_bfloat16* Ob = static_cast<__nv_bfloat16*>(O);
+  switch (p.hg) {
+    case 1: fwd_merge_kernel<1><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    case 2: fwd_merge_kernel<2><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    case 4: fwd_merge_kernel<4><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    default: fwd_merge_kernel<8><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+  }
   return cudaGetLastError();
 }
 
