@@ -305,7 +305,7 @@ __global__ void px_merge_kernel(const int32_t* __restrict__ block_idx, const flo
 }
 
 // ============================================================================ fused backward
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 224;  // 2 producer warps, 1 UMMA warp, 4 epilogue warps
 constexpr int kRows = 64;                // (query, head) rows per tile
 constexpr int kKV = 32768;               // 128 keys x 128 d
 constexpr int kKIb = 16384;              // 128 keys x 64
@@ -418,8 +418,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < kRows; ++i) sh.kl_acc[0][i] = sh.kl_acc[1][i] = 0.f;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 5);
-      mbar_init(&sh.g_full[i], 32);
+      mbar_init(&sh.it_empty[i], 6);
+      mbar_init(&sh.g_full[i], 64);
       mbar_init(&sh.g_empty[i], 1 + 4);  // MMA commit + epilogue warps (meta)
     }
     mbar_init(&sh.kv_full, 1);
@@ -448,8 +448,99 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int hg = HG;          // heads per group (compile time: static register indexing)
   constexpr int npos = kRows / hg;  // queries per tile
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  // Producer warps: warp hf fills rows [32 hf, 32 hf + 32) of every tile.
+  // Lane = row for the metadata; the next tile's entry and metadata are
+  // loaded into registers right after the current tile is published, so their
+  // memory latency overlaps the wait for the next free buffer.
+  auto load_entry = [&](const int4& item, int j, int r) -> int {
+    const int idx = j * npos + r / hg;
+    return idx < item.z ? a.entries[item.y + idx] : -1;
+  };
+  auto load_rec = [&](int b, int g, int e, int r) -> float4 {
+    float l = 0.f, d = 0.f, x = 0.f;
+    if (e >= 0) {
+      const int t = e >> 8;
+      const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + (r % hg);
+      l = a.LSE[hr];
+      d = a.drow[hr];
+      x = a.lse_px[((size_t)b * a.T + t) * a.G + g];
+    }
+    return make_float4(l * kLog2e, d, x * kLog2e, __int_as_float(e));
+  };
+  // Writes this warp's metadata rows and issues its gathers (one cp.async
+  // group), waits for them and publishes its half of buffer gb.
+  auto fill_half = [&](int hf, int b, int g, int gb, const float4& rec) {
+    uint8_t* buf = smem + oG + gb * kGather;
+    const uint32_t q0 = smem_u32(buf), do0 = q0 + kRowTile, qi0 = q0 + 2 * kRowTile;
+    RowMeta& m = sh.meta[gb];
+    m.rec[32 * hf + lane] = rec;
+    __syncwarp();
+    // Q and dO rows: 32 rows x 16 chunks; lane -> (row pair half, chunk)
+    const int chunk = lane & 15;
+#pragma unroll 4
+    for (int i = 0; i < 16; ++i) {
+      const int r = 32 * hf + 2 * i + (lane >> 4);
+      const int h = r % hg;
+      const int e = __float_as_int(m.rec[r].w);
+      const bool valid = e >= 0;
+      const int t = valid ? (e >> 8) : 0;
+      const size_t off = (((size_t)b * a.T + t) * a.Hq + g * hg + h) * 128 + chunk * 8;
+      const uint32_t dd = (chunk >> 3) * kRowChunk + sw128_off(r, chunk & 7);
+      cp_async_16_zfill(q0 + dd, a.Q + off, valid);
+      cp_async_16_zfill(do0 + dd, a.dO + off, valid);
+    }
+    // q_idx rows (replicated over the heads of a query): 32 rows x 8 chunks
+#pragma unroll 4
+    for (int i = 0; i < 8; ++i) {
+      const int r = 32 * hf + 4 * i + (lane >> 3), ch = lane & 7;
+      const int e = __float_as_int(m.rec[r].w);
+      const bool valid = e >= 0;
+      const int t = valid ? (e >> 8) : 0;
+      cp_async_16_zfill(qi0 + sw128_off(r, ch), a.q_idx + ((((size_t)b * a.T + t) * a.G + g) * 64 + ch * 8),
+                        valid);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    mbar_arrive(&sh.g_full[gb]);
+    __syncwarp();
+  };
+  // All tiles of one item for producer warp hf.
+  auto fill_item = [&](int hf, const int4& item, int b, int g, uint32_t& tj) -> bool {
+    const int ntiles = (item.z + npos - 1) / npos;
+    const int r = 32 * hf + lane;
+    int e_next = load_entry(item, 0, r);
+    float4 rec = load_rec(b, g, e_next, r);
+    e_next = ntiles > 1 ? load_entry(item, 1, r) : -1;
+    for (int j = 0; j < ntiles; ++j, ++tj) {
+      const int gb = tj & 1;
+      if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503 + 30 * hf)) return false;
+      fill_half(hf, b, g, gb, rec);
+      if (j + 1 < ntiles) {
+        rec = load_rec(b, g, e_next, r);
+        e_next = j + 2 < ntiles ? load_entry(item, j + 2, r) : -1;
+      }
+    }
+    return true;
+  };
+
+  if (warp == 6) {
+    // ------------------------------------------------------------ second producer (rows 32..63)
+    uint32_t tj = 0;
+    for (int it = 0;; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 531)) { *abort_flag = 1; break; }
+      const int4 item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      if (!fill_item(1, item, b, g, tj)) { *abort_flag = 1; break; }
+    }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ producer (items, K/V, rows 0..31)
     uint32_t tj = 0;
     for (int it = 0;; ++it) {
       const int s = it & 1;
@@ -465,6 +556,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       item.x = __shfl_sync(0xffffffffu, item.x, 0);
       item.y = __shfl_sync(0xffffffffu, item.y, 0);
       item.z = __shfl_sync(0xffffffffu, item.z, 0);
+      item.w = __shfl_sync(0xffffffffu, item.w, 0);
       if (item.x < 0) break;
       int b, g, c;
       decode_list(item.x, a.n, a.G, b, g, c);
@@ -483,72 +575,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
       if (*abort_flag) break;
-      const int ntiles = (item.z + npos - 1) / npos;
-      bool ok = true;
-      for (int j = 0; j < ntiles; ++j, ++tj) {
-        const int gb = tj & 1;
-        if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503)) { ok = false; break; }
-        uint8_t* buf = smem + oG + gb * kGather;
-        const uint32_t q0 = smem_u32(buf), do0 = q0 + kRowTile, qi0 = q0 + 2 * kRowTile;
-        // row metadata first, then the gathers read it. Each lane owns rows
-        // lane and lane + 32: both entry loads go out together, then all six
-        // dependent loads together (two memory round trips per tile).
-        RowMeta& m = sh.meta[gb];
-        {
-          int e2[2], t2[2], h2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int r = lane + 32 * u;
-            const int p = r / hg;
-            h2[u] = r - p * hg;
-            const int idx = j * npos + p;
-            e2[u] = idx < item.z ? a.entries[item.y + idx] : -1;
-          }
-          float l2[2], d2[2], x2[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            t2[u] = e2[u] >= 0 ? (e2[u] >> 8) : 0;
-            const size_t hr = ((size_t)b * a.T + t2[u]) * a.Hq + g * hg + h2[u];
-            l2[u] = e2[u] >= 0 ? a.LSE[hr] : 0.f;
-            d2[u] = e2[u] >= 0 ? a.drow[hr] : 0.f;
-            x2[u] = e2[u] >= 0 ? a.lse_px[((size_t)b * a.T + t2[u]) * a.G + g] : 0.f;
-          }
-#pragma unroll
-          for (int u = 0; u < 2; ++u)
-            m.rec[lane + 32 * u] = make_float4(l2[u] * kLog2e, d2[u], x2[u] * kLog2e, __int_as_float(e2[u]));
-        }
-        __syncwarp();
-        // Q and dO rows: 64 rows x 16 chunks each; lane -> (row half, chunk)
-        const int chunk = lane & 15;
-#pragma unroll 4
-        for (int i = 0; i < 32; ++i) {
-          const int r = 2 * i + (lane >> 4);
-          const int h = r % hg;
-          const int e = __float_as_int(m.rec[r].w);
-          const bool valid = e >= 0;
-          const int t = valid ? (e >> 8) : 0;
-          const size_t off = (((size_t)b * a.T + t) * a.Hq + g * hg + h) * 128 + chunk * 8;
-          const uint32_t d = (chunk >> 3) * kRowChunk + sw128_off(r, chunk & 7);
-          cp_async_16_zfill(q0 + d, a.Q + off, valid);
-          cp_async_16_zfill(do0 + d, a.dO + off, valid);
-        }
-        // q_idx rows (replicated over the heads of a query): 64 rows x 8 chunks
-#pragma unroll 4
-        for (int i = 0; i < 16; ++i) {
-          const int r = 4 * i + (lane >> 3), ch = lane & 7;
-          const int e = __float_as_int(m.rec[r].w);
-          const bool valid = e >= 0;
-          const int t = valid ? (e >> 8) : 0;
-          cp_async_16_zfill(qi0 + sw128_off(r, ch), a.q_idx + ((((size_t)b * a.T + t) * a.G + g) * 64 + ch * 8),
-                            valid);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&sh.g_full[gb]);
-        __syncwarp();
-      }
-      if (!ok) { *abort_flag = 1; break; }
+      if (!fill_item(0, item, b, g, tj)) { *abort_flag = 1; break; }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
