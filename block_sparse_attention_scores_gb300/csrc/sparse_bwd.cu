@@ -305,7 +305,7 @@ __global__ void px_merge_kernel(const int32_t* __restrict__ block_idx, const flo
 }
 
 // ============================================================================ fused backward
-constexpr int kBwdThreads = 224;  // 2 producer warps, 1 UMMA warp, 4 epilogue warps
+constexpr int kBwdThreads = 352;  // 2 producer warps, 1 UMMA warp, 8 epilogue warps (two column halves)
 constexpr int kRows = 64;                // (query, head) rows per tile
 constexpr int kKV = 32768;               // 128 keys x 128 d
 constexpr int kKIb = 16384;              // 128 keys x 64
@@ -325,10 +325,15 @@ constexpr int oSh = oGST + kKeyRows;           // BwdShared
 // TMEM columns
 constexpr uint32_t cS = 0, cDP = 64, cX = 128, cDV = 192, cDK = 320, cKI = 448;
 
-// Per (query, head) row of a tile: {LSE * log2 e, D, lse_px * log2 e, entry
-// bits (t << 8 | slot, -1 for padding)}, one 16-byte shared load per column.
-struct RowMeta {
-  float4 rec[kRows];
+// Per (query, head) row of a tile, structure of arrays so that a 16-byte
+// shared load serves four columns. Padding rows hold +inf log-sum-exps, which
+// make their probabilities exactly zero without a mask.
+struct __align__(16) RowMeta {
+  float lse2[kRows];  // LSE * log2 e
+  float dsc[kRows];   // D * scale
+  float lpx2[kRows];  // lse_px * log2 e
+  int ent[kRows];     // entry bits t << 8 | slot, -1 for padding
+  int diag[2];        // per producer half: some row sees only part of the block (causal mask needed)
 };
 
 // Sum over the 32 lanes of NV per-lane values, with a butterfly that halves
@@ -392,9 +397,9 @@ struct BwdShared {
   uint64_t g_full[2], g_empty[2];
   uint64_t ph1_full, p_ready, ds_ready, gs_ready, ph2_full, ph2_done;
   uint64_t acc_free;
-  uint64_t epi_sync;  // rendezvous of the 4 epilogue warps
+  uint64_t kl_ready, kl_free;  // KL sums of a tile complete / read and cleared
   RowMeta meta[2];
-  float kl_acc[2][kRows];  // per-query KL partial of a tile (by tile parity), summed over the 4 warps
+  float kl_acc[kRows];  // per-query KL sum of the current tile (shared atomics of the 8 epilogue warps)
   int4 item[2];
   uint32_t tmem_base;
   int abort;
@@ -415,23 +420,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + oSh);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRows; ++i) sh.kl_acc[0][i] = sh.kl_acc[1][i] = 0.f;
+    for (int i = 0; i < kRows; ++i) sh.kl_acc[i] = 0.f;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 6);
-      mbar_init(&sh.g_full[i], 64);
-      mbar_init(&sh.g_empty[i], 1 + 4);  // MMA commit + epilogue warps (meta)
+      mbar_init(&sh.it_empty[i], 10);  // second producer, UMMA, 8 epilogue warps
+      mbar_init(&sh.g_full[i], 64);    // every lane of both producer warps
+      mbar_init(&sh.g_empty[i], 1 + 8);  // MMA commit + epilogue warps (meta, store staging)
     }
     mbar_init(&sh.kv_full, 1);
     mbar_init(&sh.kv_empty, 1);
     mbar_init(&sh.ph1_full, 1);
-    mbar_init(&sh.p_ready, 4);
-    mbar_init(&sh.ds_ready, 4);
-    mbar_init(&sh.gs_ready, 4);
+    mbar_init(&sh.p_ready, 8);
+    mbar_init(&sh.ds_ready, 8);
+    mbar_init(&sh.gs_ready, 8);
     mbar_init(&sh.ph2_full, 1);
-    mbar_init(&sh.ph2_done, 4);
-    mbar_init(&sh.acc_free, 4);
-    mbar_init(&sh.epi_sync, 4);
+    mbar_init(&sh.ph2_done, 8);
+    mbar_init(&sh.acc_free, 8);
+    mbar_init(&sh.kl_ready, 8);
+    mbar_init(&sh.kl_free, 1);
     sh.abort = 0;
     fence_barrier_init();
   }
@@ -457,23 +463,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     return idx < item.z ? a.entries[item.y + idx] : -1;
   };
   auto load_rec = [&](int b, int g, int e, int r) -> float4 {
-    float l = 0.f, d = 0.f, x = 0.f;
-    if (e >= 0) {
-      const int t = e >> 8;
-      const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + (r % hg);
-      l = a.LSE[hr];
-      d = a.drow[hr];
-      x = a.lse_px[((size_t)b * a.T + t) * a.G + g];
-    }
-    return make_float4(l * kLog2e, d, x * kLog2e, __int_as_float(e));
+    if (e < 0) return make_float4(INFINITY, 0.f, INFINITY, __int_as_float(e));
+    const int t = e >> 8;
+    const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + (r % hg);
+    const float l = a.LSE[hr], d = a.drow[hr];
+    const float x = a.lse_px[((size_t)b * a.T + t) * a.G + g];
+    return make_float4(l * kLog2e, d * a.scale, x * kLog2e, __int_as_float(e));
   };
   // Writes this warp's metadata rows and issues its gathers (one cp.async
-  // group), waits for them and publishes its half of buffer gb.
-  auto fill_half = [&](int hf, int b, int g, int gb, const float4& rec) {
+  // group), waits for them and publishes its half of buffer gb. key_last is
+  // the last key of the block: rows with an earlier query need the mask.
+  auto fill_half = [&](int hf, int b, int g, int key_last, int gb, const float4& rec) {
     uint8_t* buf = smem + oG + gb * kGather;
     const uint32_t q0 = smem_u32(buf), do0 = q0 + kRowTile, qi0 = q0 + 2 * kRowTile;
     RowMeta& m = sh.meta[gb];
-    m.rec[32 * hf + lane] = rec;
+    const int r_own = 32 * hf + lane;
+    const int e_own = __float_as_int(rec.w);
+    m.lse2[r_own] = rec.x;
+    m.dsc[r_own] = rec.y;
+    m.lpx2[r_own] = rec.z;
+    m.ent[r_own] = e_own;
+    const unsigned dg = __ballot_sync(0xffffffffu, e_own >= 0 && (e_own >> 8) < key_last);
+    if (lane == 0) m.diag[hf] = dg != 0u;
     __syncwarp();
     // Q and dO rows: 32 rows x 16 chunks; lane -> (row pair half, chunk)
     const int chunk = lane & 15;
@@ -481,7 +492,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < 16; ++i) {
       const int r = 32 * hf + 2 * i + (lane >> 4);
       const int h = r % hg;
-      const int e = __float_as_int(m.rec[r].w);
+      const int e = m.ent[r];
       const bool valid = e >= 0;
       const int t = valid ? (e >> 8) : 0;
       const size_t off = (((size_t)b * a.T + t) * a.Hq + g * hg + h) * 128 + chunk * 8;
@@ -493,7 +504,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll 4
     for (int i = 0; i < 8; ++i) {
       const int r = 32 * hf + 4 * i + (lane >> 3), ch = lane & 7;
-      const int e = __float_as_int(m.rec[r].w);
+      const int e = m.ent[r];
       const bool valid = e >= 0;
       const int t = valid ? (e >> 8) : 0;
       cp_async_16_zfill(qi0 + sw128_off(r, ch), a.q_idx + ((((size_t)b * a.T + t) * a.G + g) * 64 + ch * 8),
@@ -506,7 +517,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncwarp();
   };
   // All tiles of one item for producer warp hf.
-  auto fill_item = [&](int hf, const int4& item, int b, int g, uint32_t& tj) -> bool {
+  auto fill_item = [&](int hf, const int4& item, int b, int g, int c, uint32_t& tj) -> bool {
     const int ntiles = (item.z + npos - 1) / npos;
     const int r = 32 * hf + lane;
     int e_next = load_entry(item, 0, r);
@@ -515,7 +526,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int j = 0; j < ntiles; ++j, ++tj) {
       const int gb = tj & 1;
       if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503 + 30 * hf)) return false;
-      fill_half(hf, b, g, gb, rec);
+      fill_half(hf, b, g, c * 128 + 127, gb, rec);
       if (j + 1 < ntiles) {
         rec = load_rec(b, g, e_next, r);
         e_next = j + 2 < ntiles ? load_entry(item, j + 2, r) : -1;
@@ -537,7 +548,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (item.x < 0) break;
       int b, g, c;
       decode_list(item.x, a.n, a.G, b, g, c);
-      if (!fill_item(1, item, b, g, tj)) { *abort_flag = 1; break; }
+      if (!fill_item(1, item, b, g, c, tj)) { *abort_flag = 1; break; }
     }
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer (items, K/V, rows 0..31)
@@ -575,7 +586,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       __syncwarp();
       if (*abort_flag) break;
-      if (!fill_item(0, item, b, g, tj)) { *abort_flag = 1; break; }
+      if (!fill_item(0, item, b, g, c, tj)) { *abort_flag = 1; break; }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
@@ -664,10 +675,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (thread = key / d lane)
+    // Warps 2-5 and 7-10: two warps per TMEM lane quarter, warpgroup hf owns
+    // the tile columns (rows of the tile) [32 hf, 32 hf + 32).
     const int quarter = warp & 3;
+    const int hf = warp < 6 ? 0 : 1;
+    const int col0 = 32 * hf;
     const int kk = quarter * 32 + lane;  // TMEM lane: key in block c (phase 1), d (dQ^T), e (dq_idx^T)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    uint32_t tj = 0, sync_phase = 0;
+    const bool kl_writer = warp == 2;   // a quarter-2 warp: no dq_idx^T rows to store
+    uint32_t tj = 0;
     bool ok = true;
     for (int it = 0; ok; ++it) {
       const int s = it & 1;
@@ -687,39 +703,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 522)) { ok = false; break; }
         if (!mbar_wait(&sh.ph1_full, tj & 1, a.err, 523)) { ok = false; break; }
         tc_fence_after();
-        // this warp's key rows of the P_lo^T / dS^T / gs^T images double as
-        // its staging for the previous tile's partial stores: wait until read
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+        const bool masked = (m.diag[0] | m.diag[1]) != 0;
         // ---- phase-1 epilogue in three stages, each handing work to the
         // UMMA warp as soon as its operand is in shared memory
-        float pv[kRows];
-        {  // stage A: P = exp(s - LSE) on visible keys; P^T as bf16 high + low parts
+        float pv[32];
+        {  // stage A: P = exp(s - LSE) (zero on masked keys and padding rows); P^T as bf16 high + low parts
           float sv[32];
+          tmem_ld32(tmem + lane_off + cS + col0, sv);
+          tmem_wait_ld();
+          const float4* l4 = reinterpret_cast<const float4*>(m.lse2 + col0);
+          if (!masked) {
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            tmem_ld32(tmem + lane_off + cS + q * 32, sv);
-            tmem_wait_ld();
+            for (int i = 0; i < 8; ++i) {
+              const float4 l = l4[i];
+              pv[4 * i + 0] = fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x));
+              pv[4 * i + 1] = fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y));
+              pv[4 * i + 2] = fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z));
+              pv[4 * i + 3] = fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w));
+            }
+          } else {
+            const int4* e4 = reinterpret_cast<const int4*>(m.ent + col0);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const float4 mr = m.rec[q * 32 + i];
-              const int e = __float_as_int(mr.w);
-              const bool vis = e >= 0 && key <= (e >> 8);
-              pv[q * 32 + i] = vis ? fast_exp2(sv[i] * a.scale_log2 - mr.x) : 0.f;
+            for (int i = 0; i < 8; ++i) {
+              const float4 l = l4[i];
+              const int4 e = e4[i];
+              pv[4 * i + 0] = key <= (e.x >> 8) ? fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x)) : 0.f;
+              pv[4 * i + 1] = key <= (e.y >> 8) ? fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y)) : 0.f;
+              pv[4 * i + 2] = key <= (e.z >> 8) ? fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z)) : 0.f;
+              pv[4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
             }
           }
 #pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16) {
-            float lo[8];
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int z = 0; z < 8; ++z)
-              lo[z] = pv[8 * c16 + z] - __bfloat162float(__float2bfloat16_rn(pv[8 * c16 + z]));
-            *reinterpret_cast<uint4*>(smem + oPT + sw128_off(kk, c16)) =
-                make_uint4(pack_bf16(pv[8 * c16 + 0], pv[8 * c16 + 1]), pack_bf16(pv[8 * c16 + 2], pv[8 * c16 + 3]),
-                           pack_bf16(pv[8 * c16 + 4], pv[8 * c16 + 5]), pack_bf16(pv[8 * c16 + 6], pv[8 * c16 + 7]));
-            *reinterpret_cast<uint4*>(smem + oPL + sw128_off(kk, c16)) =
-                make_uint4(pack_bf16(lo[0], lo[1]), pack_bf16(lo[2], lo[3]), pack_bf16(lo[4], lo[5]),
-                           pack_bf16(lo[6], lo[7]));
+            for (int z = 0; z < 4; ++z) {
+              const float p0 = pv[8 * cc + 2 * z], p1 = pv[8 * cc + 2 * z + 1];
+              hi[z] = pack_bf16(p0, p1);
+              const float h0 = __uint_as_float(hi[z] << 16), h1 = __uint_as_float(hi[z] & 0xffff0000u);
+              lo[z] = pack_bf16(p0 - h0, p1 - h1);
+            }
+            const uint32_t off = sw128_off(kk, 4 * hf + cc);
+            *reinterpret_cast<uint4*>(smem + oPT + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(smem + oPL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
           }
           tc_fence_before();
           fence_proxy_async_smem();
@@ -728,22 +754,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         {  // stage B: dS = P (dP - D) * scale
           float dp[32];
+          tmem_ld32(tmem + lane_off + cDP + col0, dp);
+          tmem_wait_ld();
+          const float4* d4 = reinterpret_cast<const float4*>(m.dsc + col0);
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            tmem_ld32(tmem + lane_off + cDP + q * 32, dp);
-            tmem_wait_ld();
+          for (int cc = 0; cc < 4; ++cc) {
+            const float4 da = d4[2 * cc], db = d4[2 * cc + 1];
+            const float dv[8] = {da.x, da.y, da.z, da.w, db.x, db.y, db.z, db.w};
+            float d8[8];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              float d8[8];
-#pragma unroll
-              for (int z = 0; z < 8; ++z) {
-                const int r = q * 32 + c * 8 + z;
-                d8[z] = pv[r] * (dp[c * 8 + z] - m.rec[r].y) * a.scale;
-              }
-              *reinterpret_cast<uint4*>(smem + oDST + sw128_off(kk, q * 4 + c)) =
-                  make_uint4(pack_bf16(d8[0], d8[1]), pack_bf16(d8[2], d8[3]), pack_bf16(d8[4], d8[5]),
-                             pack_bf16(d8[6], d8[7]));
-            }
+            for (int z = 0; z < 8; ++z) d8[z] = pv[8 * cc + z] * fmaf(dp[8 * cc + z], a.scale, -dv[z]);
+            *reinterpret_cast<uint4*>(smem + oDST + sw128_off(kk, 4 * hf + cc)) =
+                make_uint4(pack_bf16(d8[0], d8[1]), pack_bf16(d8[2], d8[3]), pack_bf16(d8[4], d8[5]),
+                           pack_bf16(d8[6], d8[7]));
           }
           tc_fence_before();
           fence_proxy_async_smem();
@@ -751,135 +774,122 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (lane == 0) mbar_arrive(&sh.ds_ready);
         }
         {  // stage C: index branch, one column per query (its first head row)
+          constexpr int kQ = 32 / hg;  // queries in this warp's columns
           float xv[32];
-          float gv[kRows];
-          float term[npos];
+          float term[kQ];
+          uint32_t gp[16];  // gs^T row of this key, bf16 pairs
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            tmem_ld32(tmem + lane_off + cX + q * 32, xv);
-            tmem_wait_ld();
+          for (int z = 0; z < 16; ++z) gp[z] = 0u;
+          tmem_ld32(tmem + lane_off + cX + col0, xv);
+          tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              const int r = q * 32 + i;
-              gv[r] = 0.f;
-              if (r % hg == 0) {
-                const float4 mr = m.rec[r];
-                const int e = __float_as_int(mr.w);
-                const bool vis = e >= 0 && key <= (e >> 8);
-                float pm = 0.f;
+          for (int qq = 0; qq < kQ; ++qq) {
+            const int r = qq * hg;  // local column of the query's first head
+            float pm = 0.f;
 #pragma unroll
-                for (int h = 0; h < hg; ++h) pm += pv[r + h];
-                pm *= 1.f / (float)hg;
-                const float lpx2 = xv[i] * a.scale_idx_log2 - mr.z;  // log2 p_px
-                const float ppx = vis ? fast_exp2(lpx2) : 0.f;
-                gv[r] = vis ? a.kl_weight * (ppx - pm) * a.scale_idx : 0.f;
-                term[r / hg] = (vis && pm > 0.f) ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
-              }
-            }
+            for (int h = 0; h < hg; ++h) pm += pv[r + h];
+            pm *= 1.f / (float)hg;
+            const float lpx2 = fmaf(xv[r], a.scale_idx_log2, -m.lpx2[col0 + r]);  // log2 p_px
+            float ppx = fast_exp2(lpx2);
+            if (masked && key > (m.ent[col0 + r] >> 8)) ppx = 0.f;
+            const float gsv = a.kl_weight * (ppx - pm) * a.scale_idx;
+            const uint32_t bits = pack_bf16(gsv, 0.f) & 0xffffu;
+            gp[r >> 1] |= (r & 1) ? (bits << 16) : bits;
+            term[qq] = pm > 0.f ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
           }
 #pragma unroll
-          for (int c16 = 0; c16 < 8; ++c16)
-            *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, c16)) =
-                make_uint4(pack_bf16(gv[8 * c16 + 0], gv[8 * c16 + 1]), pack_bf16(gv[8 * c16 + 2], gv[8 * c16 + 3]),
-                           pack_bf16(gv[8 * c16 + 4], gv[8 * c16 + 5]), pack_bf16(gv[8 * c16 + 6], gv[8 * c16 + 7]));
+          for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, 4 * hf + cc)) =
+                make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
           tc_fence_before();
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.gs_ready);
-          // KL terms summed over the 128 keys (lanes here, warps via shared atomics)
-          lanes_sum_add<npos>(term, lane, sh.kl_acc[tj & 1]);
+          // KL terms summed over the 128 keys: lanes by a butterfly, the four
+          // key quarters by shared atomics into the tile's cleared sums
+          if (!mbar_wait(&sh.kl_free, (tj & 1) ^ 1, a.err, 525)) { ok = false; break; }
+          lanes_sum_add<kQ>(term, lane, sh.kl_acc + col0 / hg);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.kl_ready);
         }
         // ---- phase-2 epilogue: dQ^T (lane = d), dq_idx^T (lane = e < 64)
         // Partials are in tile order: this tile's 64 (query, head) rows are
-        // consecutive. Each warp stages its 32-column slice row-major in its
-        // own 4 KB of the consumed key-row images and writes it with one TMA
-        // store (bf16 dQ) or two (fp32 dq_idx).
+        // consecutive. Each warp stages its 32 x 32 slice row-major in the
+        // tile's own gather buffer (free once the phase-2 MMAs are complete)
+        // and writes it with one TMA store; the buffer goes back to the
+        // producers when the stores have read it.
         if (!mbar_wait(&sh.ph2_full, tj & 1, a.err, 524)) { ok = false; break; }
         tc_fence_after();
         {
+          uint8_t* gbuf = smem + oG + gb * kGather;
           const int prow0 = (item.w + j * npos) * hg;  // first dQ partial row of the tile
           const int pos0 = item.w + j * npos;          // first dq_idx partial row
-          __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(smem + oPL + quarter * 4096);
+          __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(gbuf + (hf * 4 + quarter) * 2048);
+          float* stq = reinterpret_cast<float*>(gbuf + kRowTile + (hf * 2 + (quarter & 1)) * 4096);
           float dq[32];
+          tmem_ld32(tmem + lane_off + cS + col0, dq);
+          tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            tmem_ld32(tmem + lane_off + cS + q * 32, dq);
+          for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __float2bfloat16_rn(dq[i]);
+          if (quarter < 2) {
+            tmem_ld32(tmem + lane_off + cX + col0, dq);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) stg[(q * 32 + i) * 32 + lane] = __float2bfloat16_rn(dq[i]);
+            for (int i = 0; i < 32; i += hg) stq[(i / hg) * 32 + lane] = dq[i];
           }
+          tc_fence_before();
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) tma_store_2d(&map_dq, stg, quarter * 32, prow0);
-          if (quarter < 2) {
-            // rows = queries of the tile, 32 per staging block; both blocks are
-            // this warp's own key rows (of the dS^T and gs^T images)
-            float* stgA = reinterpret_cast<float*>(smem + oDST + quarter * 4096);
-            float* stgB = reinterpret_cast<float*>(smem + oGST + quarter * 4096);
-            constexpr int kBox = npos < 32 ? npos : 32;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              tmem_ld32(tmem + lane_off + cX + q * 32, dq);
-              tmem_wait_ld();
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                const int r = q * 32 + i;
-                if (r % hg == 0) {
-                  const int pq = r / hg;  // query index within the tile
-                  float* dst = (pq < kBox ? stgA : stgB) + (pq % kBox) * 32 + lane;
-                  *dst = dq[i];
-                }
-              }
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&map_dqi, stgA, quarter * 32, pos0);
-              if (npos > kBox) tma_store_2d(&map_dqi, stgB, quarter * 32, pos0 + kBox);
-            }
+          if (lane == 0) {
+            mbar_arrive(&sh.ph2_done);  // TMEM read: the next tile's phase 1 may start
+            tma_store_2d(&map_dq, stg, quarter * 32, prow0 + col0);
+            if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + col0 / hg);
+            bulk_commit();
           }
-          if (lane == 0) bulk_commit();
         }
-        tc_fence_before();
-        if (!warps_sync(&sh.epi_sync, sync_phase, a.err, 526)) { ok = false; break; }
-        // every warp has added its KL terms: write the per-query partials
-        if (kk < npos) {
-          const int e = __float_as_int(m.rec[kk * hg].w);
-          if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[tj & 1][kk];
-          sh.kl_acc[tj & 1][kk] = 0.f;  // reused by tile tj + 2, after the next rendezvous
+        if (kl_writer) {
+          // every epilogue warp has added its KL terms: write the per-query sums
+          if (!mbar_wait(&sh.kl_ready, tj & 1, a.err, 526)) { ok = false; break; }
+          for (int q = lane; q < npos; q += 32) {
+            const int e = m.ent[q * hg];
+            if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
+            sh.kl_acc[q] = 0.f;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.kl_free);
         }
         if (lane == 0) {
-          mbar_arrive(&sh.ph2_done);
+          bulk_wait_read_all();
           mbar_arrive(&sh.g_empty[gb]);
         }
+        __syncwarp();
       }
       if (!ok) break;
-      // ---- list end: dV, dK, dk_idx accumulators (lane = key)
+      // ---- list end: dV, dK, dk_idx accumulators (lane = key); warpgroup hf
+      // takes dV/dK columns [64 hf, 64 hf + 64) and dk_idx columns [32 hf, 32 hf + 32)
       {
         const size_t orow = ((size_t)b * a.T + key) * a.G + g;
         float v[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          tmem_ld32(tmem + lane_off + cDV + q * 32, v);
-          tmem_wait_ld();
-          float4* dst = reinterpret_cast<float4*>(a.dV + orow * 128 + q * 32);
-#pragma unroll
-          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
-          tmem_ld32(tmem + lane_off + cDK + q * 32, v);
-          tmem_wait_ld();
-          dst = reinterpret_cast<float4*>(a.dK + orow * 128 + q * 32);
-#pragma unroll
-          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
-        }
-        float* dki = a.dki_part + (((size_t)b * a.G + g) * a.T + key) * 64;
-#pragma unroll
         for (int q = 0; q < 2; ++q) {
-          tmem_ld32(tmem + lane_off + cKI + q * 32, v);
+          const int d0 = 64 * hf + 32 * q;
+          tmem_ld32(tmem + lane_off + cDV + d0, v);
           tmem_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(a.dV + orow * 128 + d0);
 #pragma unroll
-          for (int z = 0; z < 8; ++z)
-            reinterpret_cast<float4*>(dki + q * 32)[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+          tmem_ld32(tmem + lane_off + cDK + d0, v);
+          tmem_wait_ld();
+          dst = reinterpret_cast<float4*>(a.dK + orow * 128 + d0);
+#pragma unroll
+          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
         }
+        float* dki = a.dki_part + (((size_t)b * a.G + g) * a.T + key) * 64 + 32 * hf;
+        tmem_ld32(tmem + lane_off + cKI + 32 * hf, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int z = 0; z < 8; ++z)
+          reinterpret_cast<float4*>(dki)[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_free);
@@ -1043,12 +1053,12 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   {
     const uint64_t dims[2] = {128, (uint64_t)L.max_padded * p.hg};
     const uint64_t strides[1] = {256};
-    const uint32_t box[2] = {32, 64};
+    const uint32_t box[2] = {32, 32};  // 32 d x 32 rows per epilogue warp
     if (!encode_tmap(&mdq, ws + L.dq_part, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const uint64_t dims2[2] = {64, (uint64_t)L.max_padded};
     const uint64_t strides2[1] = {256};
-    const uint32_t box2[2] = {32, (uint32_t)std::min(npos, 32)};
+    const uint32_t box2[2] = {32, (uint32_t)(32 / p.hg)};  // 32 e x the queries of 32 rows
     if (!encode_tmap(&mdqi, ws + L.dqi_part, 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return cudaErrorInvalidValue;
