@@ -411,7 +411,8 @@ template <int HG>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(BwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                const __grid_constant__ CUtensorMap map_ki, const __grid_constant__ CUtensorMap map_dq,
-               const __grid_constant__ CUtensorMap map_dqi) {
+               const __grid_constant__ CUtensorMap map_dqi, const __grid_constant__ CUtensorMap map_q,
+               const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_qi) {
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // uniform for the block: nothing started yet
     if (threadIdx.x == 0) dev_fail(a.err, kDevSmemAlign, 500);
@@ -424,7 +425,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
       mbar_init(&sh.it_empty[i], 10);  // second producer, UMMA, 8 epilogue warps
-      mbar_init(&sh.g_full[i], 64);    // every lane of both producer warps
+      mbar_init(&sh.g_full[i], 2);     // both producer warps (with their TMA bytes)
       mbar_init(&sh.g_empty[i], 1 + 8);  // MMA commit + epilogue warps (meta, store staging)
     }
     mbar_init(&sh.kv_full, 1);
@@ -445,6 +446,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tmem_alloc(&sh.tmem_base, 512);
     tmem_relinquish();
   }
+  // q_idx rows and gs^T columns past the queries of a tile (hg = 8 pads the
+  // index MMAs to N = 16) are never written by the pipeline: zero them once
+  for (int i = threadIdx.x; i < kQIb / 16; i += kBwdThreads) {
+    reinterpret_cast<uint4*>(smem + oG + 2 * kRowTile)[i] = make_uint4(0u, 0u, 0u, 0u);
+    reinterpret_cast<uint4*>(smem + oG + kGather + 2 * kRowTile)[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  for (int i = threadIdx.x; i < kKeyRows / 16; i += kBwdThreads)
+    reinterpret_cast<uint4*>(smem + oGST)[i] = make_uint4(0u, 0u, 0u, 0u);
+  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -453,6 +463,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int n_items = *a.n_items;
   constexpr int hg = HG;          // heads per group (compile time: static register indexing)
   constexpr int npos = kRows / hg;  // queries per tile
+  constexpr int NX = npos < 16 ? 16 : npos;  // index-score columns (one per query; MMA N >= 16)
+  constexpr int kQ = 32 / hg;       // queries in the 32 rows of a producer warp / epilogue column half
 
   // Producer warps: warp hf fills rows [32 hf, 32 hf + 32) of every tile.
   // Lane = row for the metadata; the next tile's entry and metadata are
@@ -470,12 +482,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float x = a.lse_px[((size_t)b * a.T + t) * a.G + g];
     return make_float4(l * kLog2e, d * a.scale, x * kLog2e, __int_as_float(e));
   };
-  // Writes this warp's metadata rows and issues its gathers (one cp.async
-  // group), waits for them and publishes its half of buffer gb. key_last is
-  // the last key of the block: rows with an earlier query need the mask.
+  // Writes this warp's metadata rows and gathers its 32 rows of buffer gb
+  // with TMA: per query, its hg consecutive head rows of Q and dO (one box per
+  // 64-column chunk) and its q_idx row (row = query index in the tile). TMA swizzles by the
+  // shared address, so a box landing at row r0 matches the tile's 128-byte
+  // swizzle; padding queries load an out-of-range box, which is zero-filled.
+  // key_last is the last key of the block: rows with an earlier query need
+  // the causal mask.
   auto fill_half = [&](int hf, int b, int g, int key_last, int gb, const float4& rec) {
     uint8_t* buf = smem + oG + gb * kGather;
-    const uint32_t q0 = smem_u32(buf), do0 = q0 + kRowTile, qi0 = q0 + 2 * kRowTile;
     RowMeta& m = sh.meta[gb];
     const int r_own = 32 * hf + lane;
     const int e_own = __float_as_int(rec.w);
@@ -484,36 +499,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     m.lpx2[r_own] = rec.z;
     m.ent[r_own] = e_own;
     const unsigned dg = __ballot_sync(0xffffffffu, e_own >= 0 && (e_own >> 8) < key_last);
-    if (lane == 0) m.diag[hf] = dg != 0u;
+    if (lane == 0) {
+      m.diag[hf] = dg != 0u;
+      mbar_arrive_expect_tx(&sh.g_full[gb], 2 * 32 * 256 + kQ * 128);
+    }
     __syncwarp();
-    // Q and dO rows: 32 rows x 16 chunks; lane -> (row pair half, chunk)
-    const int chunk = lane & 15;
-#pragma unroll 4
-    for (int i = 0; i < 16; ++i) {
-      const int r = 32 * hf + 2 * i + (lane >> 4);
-      const int h = r % hg;
-      const int e = m.ent[r];
-      const bool valid = e >= 0;
-      const int t = valid ? (e >> 8) : 0;
-      const size_t off = (((size_t)b * a.T + t) * a.Hq + g * hg + h) * 128 + chunk * 8;
-      const uint32_t dd = (chunk >> 3) * kRowChunk + sw128_off(r, chunk & 7);
-      cp_async_16_zfill(q0 + dd, a.Q + off, valid);
-      cp_async_16_zfill(do0 + dd, a.dO + off, valid);
+    constexpr int kOps = 5;  // Q and dO chunk boxes, then the q_idx row
+    const int BT = a.B * a.T;
+#pragma unroll 1
+    for (int o = lane; o < kQ * kOps; o += 32) {
+      const int qq = o / kOps, op = o - qq * kOps;
+      const int r0 = 32 * hf + qq * hg;
+      const int e = m.ent[r0];
+      const int bt = e >= 0 ? b * a.T + (e >> 8) : BT;  // BT: out of range, zero fill
+      if (op < 4) {
+        const int which = op >> 1, chunk = op & 1;
+        tma_load_3d(buf + which * kRowTile + chunk * kRowChunk + r0 * 128, which ? &map_do : &map_q,
+                    &sh.g_full[gb], chunk * 64, g * hg, bt);
+      } else {
+        tma_load_2d(buf + 2 * kRowTile + (r0 / hg) * 128, &map_qi, &sh.g_full[gb], 0, bt * a.G + g);
+      }
     }
-    // q_idx rows (replicated over the heads of a query): 32 rows x 8 chunks
-#pragma unroll 4
-    for (int i = 0; i < 8; ++i) {
-      const int r = 32 * hf + 4 * i + (lane >> 3), ch = lane & 7;
-      const int e = m.ent[r];
-      const bool valid = e >= 0;
-      const int t = valid ? (e >> 8) : 0;
-      cp_async_16_zfill(qi0 + sw128_off(r, ch), a.q_idx + ((((size_t)b * a.T + t) * a.G + g) * 64 + ch * 8),
-                        valid);
-    }
-    cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    mbar_arrive(&sh.g_full[gb]);
     __syncwarp();
   };
   // All tiles of one item for producer warp hf.
@@ -595,6 +601,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_acc = make_idesc_bf16(128, 128, false, true);  // K-major A, MN-major B, N=128
       constexpr uint32_t id_tr = make_idesc_bf16(128, 64, true, true);     // MN-major A and B, N=64
       constexpr uint32_t id_ki = make_idesc_bf16(128, 64, false, true);    // K-major A, MN-major B, N=64
+      constexpr uint32_t id_x = make_idesc_bf16(128, NX, false, false);    // K-major x K-major, N=NX
+      constexpr uint32_t id_trx = make_idesc_bf16(128, NX, true, true);    // MN-major A and B, N=NX
       const uint32_t k0 = smem_u32(smem + oK), v0 = smem_u32(smem + oV), ki0 = smem_u32(smem + oKI);
       const uint32_t pt0 = smem_u32(smem + oPT), pl0 = smem_u32(smem + oPL);
       const uint32_t dst0 = smem_u32(smem + oDST), gst0 = smem_u32(smem + oGST);
@@ -630,7 +638,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gqi + ks * 32, 16, 1024, kSw128), id_sT, ks > 0);
+                         make_sdesc(gqi + ks * 32, 16, 1024, kSw128), id_x, ks > 0);
           umma_commit(&sh.ph1_full);
           // phase 2, released in three steps by the epilogue: P^T (dV), dS^T
           // (dK, dQ^T), gs^T (dk_idx, dq_idx^T)
@@ -659,13 +667,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (!mbar_wait(&sh.gs_ready, tj & 1, a.err, 518)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)  // dk_idx += gs^T QI
+          for (int ks = 0; ks < NX / 16; ++ks)  // dk_idx += gs^T QI   (K = NX queries)
             umma_bf16_ss(tmem + cKI, make_sdesc(gst0 + ks * 32, 16, 1024, kSw128),
                          make_sdesc(gqi + ks * 2048, 16, 1024, kSw128), id_ki, acc | (ks > 0));
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dq_idx^T = KI^T gs^T
             umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 2048, kKIb, 1024, kSw128),
-                         make_sdesc(gst0 + ks * 2048, 16, 1024, kSw128), id_tr, ks > 0);
+                         make_sdesc(gst0 + ks * 2048, 16, 1024, kSw128), id_trx, ks > 0);
           umma_commit(&sh.ph2_full);
           umma_commit(&sh.g_empty[gb]);
         }
@@ -773,34 +781,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.ds_ready);
         }
-        {  // stage C: index branch, one column per query (its first head row)
-          constexpr int kQ = 32 / hg;  // queries in this warp's columns
-          float xv[32];
+        {  // stage C: index branch; X^T and gs^T have one column per query
+          float xv[kQ];
           float term[kQ];
-          uint32_t gp[16];  // gs^T row of this key, bf16 pairs
+          uint32_t gp[kQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs
 #pragma unroll
-          for (int z = 0; z < 16; ++z) gp[z] = 0u;
-          tmem_ld32(tmem + lane_off + cX + col0, xv);
+          for (int z = 0; z < kQ / 2; ++z) gp[z] = 0u;
+          tmem_ld_cols<kQ>(tmem + lane_off + cX + hf * kQ, xv);
           tmem_wait_ld();
 #pragma unroll
           for (int qq = 0; qq < kQ; ++qq) {
-            const int r = qq * hg;  // local column of the query's first head
+            const int r = qq * hg;  // local column of the query's first head row
             float pm = 0.f;
 #pragma unroll
             for (int h = 0; h < hg; ++h) pm += pv[r + h];
             pm *= 1.f / (float)hg;
-            const float lpx2 = fmaf(xv[r], a.scale_idx_log2, -m.lpx2[col0 + r]);  // log2 p_px
+            const float lpx2 = fmaf(xv[qq], a.scale_idx_log2, -m.lpx2[col0 + r]);  // log2 p_px
             float ppx = fast_exp2(lpx2);
             if (masked && key > (m.ent[col0 + r] >> 8)) ppx = 0.f;
             const float gsv = a.kl_weight * (ppx - pm) * a.scale_idx;
             const uint32_t bits = pack_bf16(gsv, 0.f) & 0xffffu;
-            gp[r >> 1] |= (r & 1) ? (bits << 16) : bits;
+            gp[qq >> 1] |= (qq & 1) ? (bits << 16) : bits;
             term[qq] = pm > 0.f ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
           }
+          // columns [hf kQ, hf kQ + kQ) of the gs^T row
+          if constexpr (kQ >= 8) {
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, 4 * hf + cc)) =
-                make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
+            for (int cc = 0; cc < kQ / 8; ++cc)
+              *reinterpret_cast<uint4*>(smem + oGST + sw128_off(kk, hf * (kQ / 8) + cc)) =
+                  make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
+          } else {
+            *reinterpret_cast<uint2*>(smem + oGST + sw128_off(kk, 0) + 8 * hf) = make_uint2(gp[0], gp[1]);
+          }
           tc_fence_before();
           fence_proxy_async_smem();
           __syncwarp();
@@ -808,7 +820,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // KL terms summed over the 128 keys: lanes by a butterfly, the four
           // key quarters by shared atomics into the tile's cleared sums
           if (!mbar_wait(&sh.kl_free, (tj & 1) ^ 1, a.err, 525)) { ok = false; break; }
-          lanes_sum_add<kQ>(term, lane, sh.kl_acc + col0 / hg);
+          lanes_sum_add<kQ>(term, lane, sh.kl_acc + hf * kQ);
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.kl_ready);
         }
@@ -832,10 +844,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __float2bfloat16_rn(dq[i]);
           if (quarter < 2) {
-            tmem_ld32(tmem + lane_off + cX + col0, dq);
+            float dqi[kQ];
+            tmem_ld_cols<kQ>(tmem + lane_off + cX + hf * kQ, dqi);
             tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; i += hg) stq[(i / hg) * 32 + lane] = dq[i];
+            for (int i = 0; i < kQ; ++i) stq[i * 32 + lane] = dqi[i];
           }
           tc_fence_before();
           fence_proxy_async_smem();
@@ -843,7 +856,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (lane == 0) {
             mbar_arrive(&sh.ph2_done);  // TMEM read: the next tile's phase 1 may start
             tma_store_2d(&map_dq, stg, quarter * 32, prow0 + col0);
-            if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + col0 / hg);
+            if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kQ);
             bulk_commit();
           }
         }
@@ -1049,6 +1062,22 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  CUtensorMap mq, mdo, mqi;
+  {
+    // one query's head rows of its group: box {64 d, hg heads, 1 token}
+    const uint64_t dims[3] = {128, (uint64_t)p.Hq, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {256, (uint64_t)p.Hq * 256};
+    const uint32_t box[3] = {64, (uint32_t)p.hg, 1};
+    if (!encode_tmap(&mq, const_cast<void*>(Q), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (!encode_tmap(&mdo, const_cast<void*>(dO), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    const uint64_t dims2[2] = {64, (uint64_t)p.BT() * p.G};
+    const uint64_t strides2[1] = {128};
+    const uint32_t box2[2] = {64, 1};
+    if (!encode_tmap(&mqi, const_cast<void*>(q_idx), 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   CUtensorMap mdq, mdqi;
   {
     const uint64_t dims[2] = {128, (uint64_t)L.max_padded * p.hg};
@@ -1122,10 +1151,10 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.scale_idx = p.scale_idx;
   ba.kl_weight = kl_weight;
   switch (p.hg) {
-    case 1: bwd_kernel<1><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
-    case 2: bwd_kernel<2><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
-    case 4: bwd_kernel<4><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
-    default: bwd_kernel<8><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi); break;
+    case 1: bwd_kernel<1><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    case 2: bwd_kernel<2><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    case 4: bwd_kernel<4><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    default: bwd_kernel<8><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
   }
   count_launches(6);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
