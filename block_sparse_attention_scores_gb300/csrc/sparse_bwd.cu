@@ -305,7 +305,8 @@ __global__ void px_merge_kernel(const int32_t* __restrict__ block_idx, const flo
 }
 
 // ============================================================================ fused backward
-constexpr int kBwdThreads = 352;  // 2 producer warps, 1 UMMA warp, 8 epilogue warps (two column halves)
+constexpr int kBwdThreads = 512;  // 7 producer warps, 1 UMMA warp, 8 epilogue warps (two column halves)
+constexpr int kProd = 7;          // producer warps: 0, 6, 11..15
 constexpr int kRows = 64;                // (query, head) rows per tile
 constexpr int kKV = 32768;               // 128 keys x 128 d
 constexpr int kKIb = 16384;              // 128 keys x 64
@@ -317,13 +318,16 @@ constexpr int kGather = 2 * kRowTile + kQIb;  // Q, dO, QI per tile
 // smem map (the dynamic base is 1024-aligned; checked at entry)
 constexpr int oK = 0, oV = kKV, oKI = 2 * kKV;
 constexpr int oG = 2 * kKV + kKIb;             // 2 gather buffers
-constexpr int oPT = oG + 2 * kGather;          // P^T (bf16 high part)
-constexpr int oPL = oPT + kKeyRows;            // P^T low part: P - bf16(P), for an exact-enough dV
-constexpr int oDST = oPL + kKeyRows;           // dS^T
+constexpr int oPT = oG + 2 * kGather;          // P^T image (bf16), used when P^T does not fit in TMEM (hg = 1)
+constexpr int oDST = oPT + kKeyRows;           // dS^T
 constexpr int oGST = oDST + kKeyRows;          // gs^T
 constexpr int oSh = oGST + kKeyRows;           // BwdShared
-// TMEM columns
-constexpr uint32_t cS = 0, cDP = 64, cX = 128, cDV = 192, cDK = 320, cKI = 448;
+// TMEM columns. A tile's 64 columns at cR[tile parity] hold S^T, then dP^T
+// (once the epilogue has loaded S), then dQ^T (once it has loaded dP): the
+// next tile's S^T goes to the other region while this tile finishes. cX holds
+// the index scores X^T, then dq_idx^T. cP holds P^T as packed bf16 pairs,
+// the A operand of dV += P^T dO, when cX leaves room for it (hg >= 2).
+constexpr uint32_t cR0 = 0, cX = 128, cP = 160, cDV = 192, cDK = 320, cKI = 448;
 
 // Per (query, head) row of a tile, structure of arrays so that a 16-byte
 // shared load serves four columns. Padding rows hold +inf log-sum-exps, which
@@ -333,7 +337,7 @@ struct __align__(16) RowMeta {
   float dsc[kRows];   // D * scale
   float lpx2[kRows];  // lse_px * log2 e
   int ent[kRows];     // entry bits t << 8 | slot, -1 for padding
-  int diag[2];        // per producer half: some row sees only part of the block (causal mask needed)
+  int diag[8];        // per producer: some row sees only part of the block (causal mask needed)
 };
 
 // Sum over the 32 lanes of NV per-lane values, with a butterfly that halves
@@ -395,7 +399,9 @@ struct BwdShared {
   uint64_t it_full[2], it_empty[2];
   uint64_t kv_full, kv_empty;
   uint64_t g_full[2], g_empty[2];
-  uint64_t ph1_full, p_ready, ds_ready, gs_ready, ph2_full, ph2_done;
+  uint64_t s_full, s_read, dp_full, x_full;  // S^T computed / loaded by the epilogue, dP^T and X^T computed
+  uint64_t p_ready, ds_ready, gs_ready, ph2_full;
+  uint64_t r_free[2], x_free;  // a tile's dQ^T / dq_idx^T read out of TMEM (by tile parity / every tile)
   uint64_t acc_free;
   uint64_t kl_ready, kl_free;  // KL sums of a tile complete / read and cleared
   RowMeta meta[2];
@@ -422,20 +428,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRows; ++i) sh.kl_acc[i] = 0.f;
+    for (int i = 0; i < 8; ++i) sh.meta[0].diag[i] = sh.meta[1].diag[i] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 10);  // second producer, UMMA, 8 epilogue warps
-      mbar_init(&sh.g_full[i], 2);     // both producer warps (with their TMA bytes)
+      mbar_init(&sh.it_empty[i], kProd - 1 + 1 + 8);  // other producers, UMMA, epilogue warps
+      mbar_init(&sh.g_full[i], kProd);  // every producer warp (with its TMA bytes)
       mbar_init(&sh.g_empty[i], 1 + 8);  // MMA commit + epilogue warps (meta, store staging)
     }
     mbar_init(&sh.kv_full, 1);
     mbar_init(&sh.kv_empty, 1);
-    mbar_init(&sh.ph1_full, 1);
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.s_read, 8);
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.x_full, 1);
     mbar_init(&sh.p_ready, 8);
     mbar_init(&sh.ds_ready, 8);
     mbar_init(&sh.gs_ready, 8);
     mbar_init(&sh.ph2_full, 1);
-    mbar_init(&sh.ph2_done, 8);
+    mbar_init(&sh.r_free[0], 8);
+    mbar_init(&sh.r_free[1], 8);
+    mbar_init(&sh.x_free, 8);
     mbar_init(&sh.acc_free, 8);
     mbar_init(&sh.kl_ready, 8);
     mbar_init(&sh.kl_free, 1);
@@ -465,51 +477,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr int npos = kRows / hg;  // queries per tile
   constexpr int NX = npos < 16 ? 16 : npos;  // index-score columns (one per query; MMA N >= 16)
   constexpr int kQ = 32 / hg;       // queries in the 32 rows of a producer warp / epilogue column half
+  constexpr bool kPTmem = NX <= 32; // P^T fits in TMEM beside X^T (hg >= 2)
 
-  // Producer warps: warp hf fills rows [32 hf, 32 hf + 32) of every tile.
-  // Lane = row for the metadata; the next tile's entry and metadata are
-  // loaded into registers right after the current tile is published, so their
-  // memory latency overlaps the wait for the next free buffer.
-  auto load_entry = [&](const int4& item, int j, int r) -> int {
-    const int idx = j * npos + r / hg;
+  // Producer warps (kProd of them): producer p owns the queries p, p + kProd,
+  // ... of every tile, i.e. their metadata rows and their TMA boxes, so the
+  // producers never wait on one another. Lane l < (its queries) x hg holds
+  // the row of query p + kProd (l / hg), head l % hg. The next tile's entry
+  // and metadata are loaded into registers right after the current tile is
+  // published, so their memory latency overlaps the wait for the next buffer.
+  auto load_entry = [&](const int4& item, int j, int q) -> int {
+    const int idx = j * npos + q;
     return idx < item.z ? a.entries[item.y + idx] : -1;
   };
-  auto load_rec = [&](int b, int g, int e, int r) -> float4 {
+  auto load_rec = [&](int b, int g, int e, int h) -> float4 {
     if (e < 0) return make_float4(INFINITY, 0.f, INFINITY, __int_as_float(e));
     const int t = e >> 8;
-    const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + (r % hg);
+    const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + h;
     const float l = a.LSE[hr], d = a.drow[hr];
     const float x = a.lse_px[((size_t)b * a.T + t) * a.G + g];
     return make_float4(l * kLog2e, d * a.scale, x * kLog2e, __int_as_float(e));
   };
-  // Writes this warp's metadata rows and gathers its 32 rows of buffer gb
+  // Writes this producer's metadata rows of buffer gb and gathers its queries
   // with TMA: per query, its hg consecutive head rows of Q and dO (one box per
-  // 64-column chunk) and its q_idx row (row = query index in the tile). TMA swizzles by the
-  // shared address, so a box landing at row r0 matches the tile's 128-byte
-  // swizzle; padding queries load an out-of-range box, which is zero-filled.
-  // key_last is the last key of the block: rows with an earlier query need
-  // the causal mask.
-  auto fill_half = [&](int hf, int b, int g, int key_last, int gb, const float4& rec) {
+  // 64-column chunk) and its q_idx row (row = query index in the tile). TMA
+  // swizzles by the shared address, so a box landing at row r0 matches the
+  // tile's 128-byte swizzle; padding queries load an out-of-range box, which
+  // is zero-filled. key_last is the last key of the block: rows with an
+  // earlier query need the causal mask.
+  auto fill_part = [&](int p, int nq, int b, int g, int key_last, int gb, const float4& rec) {
     uint8_t* buf = smem + oG + gb * kGather;
     RowMeta& m = sh.meta[gb];
-    const int r_own = 32 * hf + lane;
+    const bool mine = lane < nq * hg;
     const int e_own = __float_as_int(rec.w);
-    m.lse2[r_own] = rec.x;
-    m.dsc[r_own] = rec.y;
-    m.lpx2[r_own] = rec.z;
-    m.ent[r_own] = e_own;
-    const unsigned dg = __ballot_sync(0xffffffffu, e_own >= 0 && (e_own >> 8) < key_last);
+    if (mine) {
+      const int r = (p + kProd * (lane / hg)) * hg + lane % hg;
+      m.lse2[r] = rec.x;
+      m.dsc[r] = rec.y;
+      m.lpx2[r] = rec.z;
+      m.ent[r] = e_own;
+    }
+    const unsigned dg = __ballot_sync(0xffffffffu, mine && e_own >= 0 && (e_own >> 8) < key_last);
     if (lane == 0) {
-      m.diag[hf] = dg != 0u;
-      mbar_arrive_expect_tx(&sh.g_full[gb], 2 * 32 * 256 + kQ * 128);
+      m.diag[p] = dg != 0u;
+      mbar_arrive_expect_tx(&sh.g_full[gb], nq * (2 * hg * 256 + 128));
     }
     __syncwarp();
-    constexpr int kOps = 5;  // Q and dO chunk boxes, then the q_idx row
     const int BT = a.B * a.T;
 #pragma unroll 1
-    for (int o = lane; o < kQ * kOps; o += 32) {
-      const int qq = o / kOps, op = o - qq * kOps;
-      const int r0 = 32 * hf + qq * hg;
+    for (int o = lane; o < nq * 5; o += 32) {  // per query: Q and dO chunk boxes, then the q_idx row
+      const int i = o / 5, op = o - i * 5;
+      const int q = p + kProd * i;
+      const int r0 = q * hg;
       const int e = m.ent[r0];
       const int bt = e >= 0 ? b * a.T + (e >> 8) : BT;  // BT: out of range, zero fill
       if (op < 4) {
@@ -517,82 +535,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_load_3d(buf + which * kRowTile + chunk * kRowChunk + r0 * 128, which ? &map_do : &map_q,
                     &sh.g_full[gb], chunk * 64, g * hg, bt);
       } else {
-        tma_load_2d(buf + 2 * kRowTile + (r0 / hg) * 128, &map_qi, &sh.g_full[gb], 0, bt * a.G + g);
+        tma_load_2d(buf + 2 * kRowTile + q * 128, &map_qi, &sh.g_full[gb], 0, bt * a.G + g);
       }
     }
     __syncwarp();
   };
-  // All tiles of one item for producer warp hf.
-  auto fill_item = [&](int hf, const int4& item, int b, int g, int c, uint32_t& tj) -> bool {
+  // All tiles of one item for producer p.
+  auto fill_item = [&](int p, const int4& item, int b, int g, int c, uint32_t& tj) -> bool {
     const int ntiles = (item.z + npos - 1) / npos;
-    const int r = 32 * hf + lane;
-    int e_next = load_entry(item, 0, r);
-    float4 rec = load_rec(b, g, e_next, r);
-    e_next = ntiles > 1 ? load_entry(item, 1, r) : -1;
+    const int nq = (npos - p + kProd - 1) / kProd;  // queries of this producer in a tile
+    const int q = p + kProd * (lane / hg), h = lane % hg;
+    const bool mine = lane < nq * hg;
+    int e_next = mine ? load_entry(item, 0, q) : -1;
+    float4 rec = load_rec(b, g, e_next, h);
+    e_next = (mine && ntiles > 1) ? load_entry(item, 1, q) : -1;
     for (int j = 0; j < ntiles; ++j, ++tj) {
       const int gb = tj & 1;
-      if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503 + 30 * hf)) return false;
-      fill_half(hf, b, g, c * 128 + 127, gb, rec);
+      if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503 + p)) return false;
+      fill_part(p, nq, b, g, c * 128 + 127, gb, rec);
       if (j + 1 < ntiles) {
-        rec = load_rec(b, g, e_next, r);
-        e_next = j + 2 < ntiles ? load_entry(item, j + 2, r) : -1;
+        rec = load_rec(b, g, e_next, h);
+        e_next = (mine && j + 2 < ntiles) ? load_entry(item, j + 2, q) : -1;
       }
     }
     return true;
   };
 
-  if (warp == 6) {
-    // ------------------------------------------------------------ second producer (rows 32..63)
-    uint32_t tj = 0;
-    for (int it = 0;; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!mbar_wait(&sh.it_full[s], ph, a.err, 531)) { *abort_flag = 1; break; }
-      const int4 item = sh.item[s];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
-      if (item.x < 0) break;
-      int b, g, c;
-      decode_list(item.x, a.n, a.G, b, g, c);
-      if (!fill_item(1, item, b, g, c, tj)) { *abort_flag = 1; break; }
-    }
-  } else if (warp == 0) {
-    // ------------------------------------------------------------ producer (items, K/V, rows 0..31)
+  const int prod = warp == 0 ? 0 : warp == 6 ? 1 : warp >= 11 ? warp - 9 : -1;
+  if (prod >= 0) {
+    // ------------------------------------------------------------ producers; producer 0 also
+    // fetches the work items and loads each item's K, V and k_idx block
     uint32_t tj = 0;
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
       int4 item = make_int4(-1, 0, 0, 0);
-      if (lane == 0) {
-        if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 501)) *abort_flag = 1;
-        const int id = atomicAdd(a.counter, 1);
-        if (id < n_items && !*abort_flag) item = a.items[id];
-        sh.item[s] = item;
-        mbar_arrive(&sh.it_full[s]);
+      if (prod == 0) {
+        if (lane == 0) {
+          if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 501)) *abort_flag = 1;
+          const int id = atomicAdd(a.counter, 1);
+          if (id < n_items && !*abort_flag) item = a.items[id];
+          sh.item[s] = item;
+          mbar_arrive(&sh.it_full[s]);
+        }
+        item.x = __shfl_sync(0xffffffffu, item.x, 0);
+        item.y = __shfl_sync(0xffffffffu, item.y, 0);
+        item.z = __shfl_sync(0xffffffffu, item.z, 0);
+        item.w = __shfl_sync(0xffffffffu, item.w, 0);
+      } else {
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 531)) { *abort_flag = 1; break; }
+        item = sh.item[s];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.it_empty[s]);
       }
-      item.x = __shfl_sync(0xffffffffu, item.x, 0);
-      item.y = __shfl_sync(0xffffffffu, item.y, 0);
-      item.z = __shfl_sync(0xffffffffu, item.z, 0);
-      item.w = __shfl_sync(0xffffffffu, item.w, 0);
       if (item.x < 0) break;
       int b, g, c;
       decode_list(item.x, a.n, a.G, b, g, c);
-      if (lane == 0) {
-        if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 502)) {
-          mbar_arrive_expect_tx(&sh.kv_full, 2 * kKV + kKIb);
-          const int row0 = b * a.T + c * 128;
-          tma_load_3d(smem + oK, &map_k, &sh.kv_full, 0, g, row0);
-          tma_load_3d(smem + oK + kKV / 2, &map_k, &sh.kv_full, 64, g, row0);
-          tma_load_3d(smem + oV, &map_v, &sh.kv_full, 0, g, row0);
-          tma_load_3d(smem + oV + kKV / 2, &map_v, &sh.kv_full, 64, g, row0);
-          tma_load_2d(smem + oKI, &map_ki, &sh.kv_full, 0, row0);
-        } else {
-          *abort_flag = 1;
+      if (prod == 0) {
+        if (lane == 0) {
+          if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 502)) {
+            mbar_arrive_expect_tx(&sh.kv_full, 2 * kKV + kKIb);
+            const int row0 = b * a.T + c * 128;
+            tma_load_3d(smem + oK, &map_k, &sh.kv_full, 0, g, row0);
+            tma_load_3d(smem + oK + kKV / 2, &map_k, &sh.kv_full, 64, g, row0);
+            tma_load_3d(smem + oV, &map_v, &sh.kv_full, 0, g, row0);
+            tma_load_3d(smem + oV + kKV / 2, &map_v, &sh.kv_full, 64, g, row0);
+            tma_load_2d(smem + oKI, &map_ki, &sh.kv_full, 0, row0);
+          } else {
+            *abort_flag = 1;
+          }
         }
+        __syncwarp();
+        if (*abort_flag) break;
       }
-      __syncwarp();
-      if (*abort_flag) break;
-      if (!fill_item(0, item, b, g, c, tj)) { *abort_flag = 1; break; }
+      if (!fill_item(prod, item, b, g, c, tj)) { *abort_flag = 1; break; }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
@@ -603,9 +619,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       constexpr uint32_t id_ki = make_idesc_bf16(128, 64, false, true);    // K-major A, MN-major B, N=64
       constexpr uint32_t id_x = make_idesc_bf16(128, NX, false, false);    // K-major x K-major, N=NX
       constexpr uint32_t id_trx = make_idesc_bf16(128, NX, true, true);    // MN-major A and B, N=NX
-      const uint32_t k0 = smem_u32(smem + oK), v0 = smem_u32(smem + oV), ki0 = smem_u32(smem + oKI);
-      const uint32_t pt0 = smem_u32(smem + oPT), pl0 = smem_u32(smem + oPL);
-      const uint32_t dst0 = smem_u32(smem + oDST), gst0 = smem_u32(smem + oGST);
+      // Shared-memory descriptors, built once: a k-step or the other gather
+      // buffer moves only the start-address field, so every UMMA below adds a
+      // constant to one of these bases.
+      const uint64_t dK = make_sdesc(smem_u32(smem + oK), 16, 1024, kSw128);        // K, K-major
+      const uint64_t dKt = make_sdesc(smem_u32(smem + oK), kKV / 2, 1024, kSw128);   // K as MN-major A
+      const uint64_t dV = make_sdesc(smem_u32(smem + oV), 16, 1024, kSw128);
+      const uint64_t dKI = make_sdesc(smem_u32(smem + oKI), 16, 1024, kSw128);
+      const uint64_t dKIt = make_sdesc(smem_u32(smem + oKI), kKIb, 1024, kSw128);
+      const uint64_t dPT = make_sdesc(smem_u32(smem + oPT), 16, 1024, kSw128);
+      const uint64_t dDS = make_sdesc(smem_u32(smem + oDST), 16, 1024, kSw128);
+      const uint64_t dGS = make_sdesc(smem_u32(smem + oGST), 16, 1024, kSw128);
+      const uint64_t dG = make_sdesc(smem_u32(smem + oG), 16, 1024, kSw128);
+      const uint64_t dGt = make_sdesc(smem_u32(smem + oG), kRowChunk, 1024, kSw128);  // rows as MN-major B
+      auto at = [](uint64_t d, uint32_t off) -> uint64_t { return d + (uint64_t)(off >> 4); };
       uint32_t tj = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
@@ -620,26 +647,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int j = 0; j < ntiles; ++j, ++tj) {
           const int gb = tj & 1;
           if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 513)) { ok = false; break; }
-          // the previous tile's epilogue has read dQ^T / dq_idx^T out of TMEM
-          if (!mbar_wait(&sh.ph2_done, (tj & 1) ^ 1, a.err, 514)) { ok = false; break; }
+          // region cR[tj & 1] was read out by the epilogue of tile tj - 2
+          if (!mbar_wait(&sh.r_free[tj & 1], ((tj >> 1) & 1) ^ 1, a.err, 514)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t g0 = smem_u32(smem + oG + gb * kGather);
-          const uint32_t gq = g0, gdo = g0 + kRowTile, gqi = g0 + 2 * kRowTile;
-          // phase 1: S^T = K Q^T, dP^T = V dO^T, X^T = KI QI^T
+          const uint32_t tR = tmem + cR0 + 64 * (tj & 1);
+          const uint32_t goff = gb * kGather;
+          const uint64_t bQ = at(dG, goff), bO = at(dG, goff + kRowTile), bQI = at(dG, goff + 2 * kRowTile);
+          const uint64_t bQt = at(dGt, goff), bOt = at(dGt, goff + kRowTile);
+          // S^T = K Q^T
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t ao = (ks >> 2) * (kKV / 2) + (ks & 3) * 32;
             const uint32_t bo = (ks >> 2) * kRowChunk + (ks & 3) * 32;
-            umma_bf16_ss(tmem + cS, make_sdesc(k0 + ao, 16, 1024, kSw128), make_sdesc(gq + bo, 16, 1024, kSw128),
-                         id_sT, ks > 0);
-            umma_bf16_ss(tmem + cDP, make_sdesc(v0 + ao, 16, 1024, kSw128),
-                         make_sdesc(gdo + bo, 16, 1024, kSw128), id_sT, ks > 0);
+            umma_bf16_ss(tR, at(dK, ao), at(bQ, bo), id_sT, ks > 0);
           }
+          umma_commit(&sh.s_full);
+          // X^T = KI QI^T, once the previous tile's dq_idx^T has been read
+          if (!mbar_wait(&sh.x_free, (tj & 1) ^ 1, a.err, 519)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gqi + ks * 32, 16, 1024, kSw128), id_x, ks > 0);
-          umma_commit(&sh.ph1_full);
+          for (int ks = 0; ks < 4; ++ks) umma_bf16_ss(tmem + cX, at(dKI, ks * 32), at(bQI, ks * 32), id_x, ks > 0);
+          umma_commit(&sh.x_full);
+          // dP^T = V dO^T into the same columns, once every epilogue warp has loaded S^T
+          if (!mbar_wait(&sh.s_read, tj & 1, a.err, 520)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t ao = (ks >> 2) * (kKV / 2) + (ks & 3) * 32;
+            const uint32_t bo = (ks >> 2) * kRowChunk + (ks & 3) * 32;
+            umma_bf16_ss(tR, at(dV, ao), at(bO, bo), id_sT, ks > 0);
+          }
+          umma_commit(&sh.dp_full);
           // phase 2, released in three steps by the epilogue: P^T (dV), dS^T
           // (dK, dQ^T), gs^T (dk_idx, dq_idx^T)
           if (!mbar_wait(&sh.p_ready, tj & 1, a.err, 515)) { ok = false; break; }
@@ -647,33 +685,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tc_fence_after();
           const uint32_t acc = (j > 0) ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            // dV += P^T dO with P = hi + lo   (K = 64 rows, 16 per step)
-            umma_bf16_ss(tmem + cDV, make_sdesc(pt0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gdo + ks * 2048, kRowChunk, 1024, kSw128), id_acc, acc | (ks > 0));
-            umma_bf16_ss(tmem + cDV, make_sdesc(pl0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gdo + ks * 2048, kRowChunk, 1024, kSw128), id_acc, 1u);
+          for (int ks = 0; ks < 4; ++ks) {  // dV += P^T dO   (K = 64 rows, 16 per step)
+            if constexpr (kPTmem)
+              umma_bf16_ts(tmem + cDV, tmem + cP + ks * 8, at(bOt, ks * 2048), id_acc, acc | (ks > 0));
+            else
+              umma_bf16_ss(tmem + cDV, at(dPT, ks * 32), at(bOt, ks * 2048), id_acc, acc | (ks > 0));
           }
           if (!mbar_wait(&sh.ds_ready, tj & 1, a.err, 517)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)  // dK += dS^T Q
-            umma_bf16_ss(tmem + cDK, make_sdesc(dst0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gq + ks * 2048, kRowChunk, 1024, kSw128), id_acc, acc | (ks > 0));
+            umma_bf16_ss(tmem + cDK, at(dDS, ks * 32), at(bQt, ks * 2048), id_acc, acc | (ks > 0));
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T   (K = 128 keys)
-            umma_bf16_ss(tmem + cS, make_sdesc(k0 + ks * 2048, kKV / 2, 1024, kSw128),
-                         make_sdesc(dst0 + ks * 2048, 16, 1024, kSw128), id_tr, ks > 0);
+          for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T into cR (dP^T has been loaded)   (K = 128 keys)
+            umma_bf16_ss(tR, at(dKt, ks * 2048), at(dDS, ks * 2048), id_tr, ks > 0);
           if (!mbar_wait(&sh.gs_ready, tj & 1, a.err, 518)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int ks = 0; ks < NX / 16; ++ks)  // dk_idx += gs^T QI   (K = NX queries)
-            umma_bf16_ss(tmem + cKI, make_sdesc(gst0 + ks * 32, 16, 1024, kSw128),
-                         make_sdesc(gqi + ks * 2048, 16, 1024, kSw128), id_ki, acc | (ks > 0));
+            umma_bf16_ss(tmem + cKI, at(dGS, ks * 32), at(bQI, ks * 2048), id_ki, acc | (ks > 0));
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dq_idx^T = KI^T gs^T
-            umma_bf16_ss(tmem + cX, make_sdesc(ki0 + ks * 2048, kKIb, 1024, kSw128),
-                         make_sdesc(gst0 + ks * 2048, 16, 1024, kSw128), id_trx, ks > 0);
+            umma_bf16_ss(tmem + cX, at(dKIt, ks * 2048), at(dGS, ks * 2048), id_trx, ks > 0);
           umma_commit(&sh.ph2_full);
           umma_commit(&sh.g_empty[gb]);
         }
@@ -709,16 +742,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int gb = tj & 1;
         const RowMeta& m = sh.meta[gb];
         if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 522)) { ok = false; break; }
-        if (!mbar_wait(&sh.ph1_full, tj & 1, a.err, 523)) { ok = false; break; }
+        if (!mbar_wait(&sh.s_full, tj & 1, a.err, 523)) { ok = false; break; }
         tc_fence_after();
-        const bool masked = (m.diag[0] | m.diag[1]) != 0;
+        const uint32_t cR = cR0 + 64 * (tj & 1);
+        const int4 dg0 = *reinterpret_cast<const int4*>(m.diag);
+        const int4 dg1 = *reinterpret_cast<const int4*>(m.diag + 4);
+        const bool masked = (dg0.x | dg0.y | dg0.z | dg0.w | dg1.x | dg1.y | dg1.z | dg1.w) != 0;
         // ---- phase-1 epilogue in three stages, each handing work to the
         // UMMA warp as soon as its operand is in shared memory
         float pv[32];
-        {  // stage A: P = exp(s - LSE) (zero on masked keys and padding rows); P^T as bf16 high + low parts
+        {  // stage A: P = exp(s - LSE) (zero on masked keys and padding rows); P^T as bf16, into TMEM or an image
           float sv[32];
-          tmem_ld32(tmem + lane_off + cS + col0, sv);
+          tmem_ld32(tmem + lane_off + cR + col0, sv);
           tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.s_read);  // the UMMA warp may overwrite S^T with dP^T
           const float4* l4 = reinterpret_cast<const float4*>(m.lse2 + col0);
           if (!masked) {
 #pragma unroll
@@ -741,19 +780,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               pv[4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
             }
           }
+          if constexpr (kPTmem) {
+            uint32_t pk[16];  // P^T row of this key, bf16 pairs (low half = even row)
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t hi[4], lo[4];
+            for (int z = 0; z < 16; ++z) pk[z] = pack_bf16(pv[2 * z], pv[2 * z + 1]);
+            tmem_st16(tmem + lane_off + cP + 16 * hf, pk);
+            tmem_wait_st();
+          } else {
 #pragma unroll
-            for (int z = 0; z < 4; ++z) {
-              const float p0 = pv[8 * cc + 2 * z], p1 = pv[8 * cc + 2 * z + 1];
-              hi[z] = pack_bf16(p0, p1);
-              const float h0 = __uint_as_float(hi[z] << 16), h1 = __uint_as_float(hi[z] & 0xffff0000u);
-              lo[z] = pack_bf16(p0 - h0, p1 - h1);
-            }
-            const uint32_t off = sw128_off(kk, 4 * hf + cc);
-            *reinterpret_cast<uint4*>(smem + oPT + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4*>(smem + oPL + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int cc = 0; cc < 4; ++cc)
+              *reinterpret_cast<uint4*>(smem + oPT + sw128_off(kk, 4 * hf + cc)) =
+                  make_uint4(pack_bf16(pv[8 * cc + 0], pv[8 * cc + 1]), pack_bf16(pv[8 * cc + 2], pv[8 * cc + 3]),
+                             pack_bf16(pv[8 * cc + 4], pv[8 * cc + 5]), pack_bf16(pv[8 * cc + 6], pv[8 * cc + 7]));
           }
           tc_fence_before();
           fence_proxy_async_smem();
@@ -762,7 +800,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         {  // stage B: dS = P (dP - D) * scale
           float dp[32];
-          tmem_ld32(tmem + lane_off + cDP + col0, dp);
+          if (!mbar_wait(&sh.dp_full, tj & 1, a.err, 527)) { ok = false; break; }
+          tc_fence_after();
+          tmem_ld32(tmem + lane_off + cR + col0, dp);
           tmem_wait_ld();
           const float4* d4 = reinterpret_cast<const float4*>(m.dsc + col0);
 #pragma unroll
@@ -787,6 +827,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           uint32_t gp[kQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs
 #pragma unroll
           for (int z = 0; z < kQ / 2; ++z) gp[z] = 0u;
+          if (!mbar_wait(&sh.x_full, tj & 1, a.err, 528)) { ok = false; break; }
+          tc_fence_after();
           tmem_ld_cols<kQ>(tmem + lane_off + cX + hf * kQ, xv);
           tmem_wait_ld();
 #pragma unroll
@@ -839,7 +881,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(gbuf + (hf * 4 + quarter) * 2048);
           float* stq = reinterpret_cast<float*>(gbuf + kRowTile + (hf * 2 + (quarter & 1)) * 4096);
           float dq[32];
-          tmem_ld32(tmem + lane_off + cS + col0, dq);
+          tmem_ld32(tmem + lane_off + cR + col0, dq);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __float2bfloat16_rn(dq[i]);
@@ -854,7 +896,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&sh.ph2_done);  // TMEM read: the next tile's phase 1 may start
+            mbar_arrive(&sh.r_free[tj & 1]);  // TMEM read: cR may take tile tj + 2's S^T,
+            mbar_arrive(&sh.x_free);          // cX the next tile's X^T
             tma_store_2d(&map_dq, stg, quarter * 32, prow0 + col0);
             if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kQ);
             bulk_commit();
