@@ -312,16 +312,10 @@ constexpr int kKV = 32768;               // 128 keys x 128 d
 constexpr int kKIb = 16384;              // 128 keys x 64
 constexpr int kRowTile = kRows * 256;    // 64 rows x 128 d  (16 KB)
 constexpr int kRowChunk = kRows * 128;   // one 64-column chunk of it (8 KB)
-constexpr int kQIb = kRows * 128;        // 64 rows x 64     (8 KB)
 constexpr int kKeyRows = 128 * 128;      // 128 keys x 64 bf16 (16 KB)
-constexpr int kGather = 2 * kRowTile + kQIb;  // Q, dO, QI per tile
-// smem map (the dynamic base is 1024-aligned; checked at entry)
+// smem map (the dynamic base is 1024-aligned; checked at entry): K, V, k_idx
+// of the block, then the per-HG part (BwdLayout)
 constexpr int oK = 0, oV = kKV, oKI = 2 * kKV;
-constexpr int oG = 2 * kKV + kKIb;             // 2 gather buffers
-constexpr int oPT = oG + 2 * kGather;          // P^T image (bf16), used when P^T does not fit in TMEM (hg = 1)
-constexpr int oDST = oPT + kKeyRows;           // dS^T
-constexpr int oGST = oDST + kKeyRows;          // gs^T
-constexpr int oSh = oGST + kKeyRows;           // BwdShared
 // TMEM columns. A tile's 64 columns at cR[tile parity] hold S^T, then dP^T
 // (once the epilogue has loaded S), then dQ^T (once it has loaded dP): the
 // next tile's S^T goes to the other region while this tile finishes. cX holds
@@ -398,20 +392,38 @@ struct BwdArgs {
 struct BwdShared {
   uint64_t it_full[2], it_empty[2];
   uint64_t kv_full, kv_empty;
-  uint64_t g_full[2], g_empty[2];
+  uint64_t g_full[3], g_empty[3];
   uint64_t s_full, s_read, dp_full, x_full;  // S^T computed / loaded by the epilogue, dP^T and X^T computed
   uint64_t p_ready, ds_ready, gs_ready, ph2_full;
   uint64_t r_free[2], x_free;  // a tile's dQ^T / dq_idx^T read out of TMEM (by tile parity / every tile)
   uint64_t acc_free;
   uint64_t kl_ready, kl_free;  // KL sums of a tile complete / read and cleared
-  RowMeta meta[2];
+  RowMeta meta[3];  // one per gather buffer
   float kl_acc[kRows];  // per-query KL sum of the current tile (shared atomics of the 8 epilogue warps)
   int4 item[2];
   uint32_t tmem_base;
   int abort;
 };
-constexpr int kBwdSmem = oSh + (int)sizeof(BwdShared);
-static_assert(kBwdSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
+// Shared-memory layout for HG heads per group. A tile's gather buffer holds
+// its Q and dO rows and its q_idx rows (one per query, NX of them). Three
+// buffers when P^T lives in TMEM (its shared image is not needed), else two.
+template <int HG>
+struct BwdLayout {
+  static constexpr int kNpos = kRows / HG;                    // queries per tile
+  static constexpr int kNX = kNpos < 16 ? 16 : kNpos;         // index-score columns (MMA N >= 16)
+  static constexpr bool kPTmem = kNX <= 32;                   // P^T fits in TMEM beside X^T
+  static constexpr int kQI = kNX * 128;                       // q_idx rows of a tile
+  static constexpr int kGather = 2 * kRowTile + kQI;          // Q, dO, q_idx
+  static constexpr int kNG = kPTmem ? 3 : 2;                  // gather buffers
+  static constexpr int oG = 2 * kKV + kKIb;
+  static constexpr int oPT = oG + kNG * kGather;              // P^T image (only without TMEM room)
+  static constexpr int oDST = oPT + (kPTmem ? 0 : kKeyRows);  // dS^T
+  static constexpr int oGST = oDST + kKeyRows;                // gs^T
+  static constexpr int oSh = oGST + kKeyRows;                 // BwdShared
+  static constexpr int kSmem = oSh + (int)sizeof(BwdShared);
+  static_assert(kGather % 1024 == 0, "gather buffers keep the 1024-byte swizzle alignment");
+  static_assert(kSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
+};
 
 template <int HG>
 __global__ void __launch_bounds__(kBwdThreads, 1)
@@ -424,15 +436,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (threadIdx.x == 0) dev_fail(a.err, kDevSmemAlign, 500);
     return;
   }
-  BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + oSh);
+  using L = BwdLayout<HG>;
+  constexpr int oG = L::oG, kGather = L::kGather, kNG = L::kNG;
+  constexpr int oPT = L::oPT, oDST = L::oDST, oGST = L::oGST;
+  BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + L::oSh);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRows; ++i) sh.kl_acc[i] = 0.f;
-    for (int i = 0; i < 8; ++i) sh.meta[0].diag[i] = sh.meta[1].diag[i] = 0;
+    for (int i = 0; i < 8; ++i) sh.meta[0].diag[i] = sh.meta[1].diag[i] = sh.meta[2].diag[i] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
       mbar_init(&sh.it_empty[i], kProd - 1 + 1 + 8);  // other producers, UMMA, epilogue warps
-      mbar_init(&sh.g_full[i], kProd);  // every producer warp (with its TMA bytes)
+    }
+    for (int i = 0; i < kNG; ++i) {
+      mbar_init(&sh.g_full[i], kProd);   // every producer warp (with its TMA bytes)
       mbar_init(&sh.g_empty[i], 1 + 8);  // MMA commit + epilogue warps (meta, store staging)
     }
     mbar_init(&sh.kv_full, 1);
@@ -460,10 +477,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   // q_idx rows and gs^T columns past the queries of a tile (hg = 8 pads the
   // index MMAs to N = 16) are never written by the pipeline: zero them once
-  for (int i = threadIdx.x; i < kQIb / 16; i += kBwdThreads) {
-    reinterpret_cast<uint4*>(smem + oG + 2 * kRowTile)[i] = make_uint4(0u, 0u, 0u, 0u);
-    reinterpret_cast<uint4*>(smem + oG + kGather + 2 * kRowTile)[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  for (int i = threadIdx.x; i < kNG * (L::kQI / 16); i += kBwdThreads)
+    reinterpret_cast<uint4*>(smem + oG + (i / (L::kQI / 16)) * kGather + 2 * kRowTile)[i % (L::kQI / 16)] =
+        make_uint4(0u, 0u, 0u, 0u);
   for (int i = threadIdx.x; i < kKeyRows / 16; i += kBwdThreads)
     reinterpret_cast<uint4*>(smem + oGST)[i] = make_uint4(0u, 0u, 0u, 0u);
   fence_proxy_async_smem();
@@ -474,10 +490,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   volatile int* abort_flag = &sh.abort;
   const int n_items = *a.n_items;
   constexpr int hg = HG;          // heads per group (compile time: static register indexing)
-  constexpr int npos = kRows / hg;  // queries per tile
-  constexpr int NX = npos < 16 ? 16 : npos;  // index-score columns (one per query; MMA N >= 16)
+  constexpr int npos = L::kNpos;   // queries per tile
+  constexpr int NX = L::kNX;        // index-score columns (one per query; MMA N >= 16)
   constexpr int kQ = 32 / hg;       // queries in the 32 rows of a producer warp / epilogue column half
-  constexpr bool kPTmem = NX <= 32; // P^T fits in TMEM beside X^T (hg >= 2)
+  constexpr bool kPTmem = L::kPTmem;
 
   // Producer warps (kProd of them): producer p owns the queries p, p + kProd,
   // ... of every tile, i.e. their metadata rows and their TMA boxes, so the
@@ -550,8 +566,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     float4 rec = load_rec(b, g, e_next, h);
     e_next = (mine && ntiles > 1) ? load_entry(item, 1, q) : -1;
     for (int j = 0; j < ntiles; ++j, ++tj) {
-      const int gb = tj & 1;
-      if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 503 + p)) return false;
+      const int gb = tj % kNG;
+      if (!mbar_wait(&sh.g_empty[gb], ((tj / kNG) & 1) ^ 1, a.err, 503 + p)) return false;
       fill_part(p, nq, b, g, c * 128 + 127, gb, rec);
       if (j + 1 < ntiles) {
         rec = load_rec(b, g, e_next, h);
@@ -645,8 +661,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int ntiles = (item.z + npos - 1) / npos;
         if (!mbar_wait(&sh.kv_full, it & 1, a.err, 512)) { ok = false; break; }
         for (int j = 0; j < ntiles; ++j, ++tj) {
-          const int gb = tj & 1;
-          if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 513)) { ok = false; break; }
+          const int gb = tj % kNG;
+          if (!mbar_wait(&sh.g_full[gb], (tj / kNG) & 1, a.err, 513)) { ok = false; break; }
           // region cR[tj & 1] was read out by the epilogue of tile tj - 2
           if (!mbar_wait(&sh.r_free[tj & 1], ((tj >> 1) & 1) ^ 1, a.err, 514)) { ok = false; break; }
           tc_fence_after();
@@ -739,9 +755,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int key = c * 128 + kk;
       const int ntiles = (item.z + npos - 1) / npos;
       for (int j = 0; j < ntiles; ++j, ++tj) {
-        const int gb = tj & 1;
+        const int gb = tj % kNG;
         const RowMeta& m = sh.meta[gb];
-        if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 522)) { ok = false; break; }
+        if (!mbar_wait(&sh.g_full[gb], (tj / kNG) & 1, a.err, 522)) { ok = false; break; }
         if (!mbar_wait(&sh.s_full, tj & 1, a.err, 523)) { ok = false; break; }
         tc_fence_after();
         const uint32_t cR = cR0 + 64 * (tj & 1);
@@ -1140,9 +1156,15 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if ((e = cudaFuncSetAttribute(px_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPxSmem)) !=
         cudaSuccess)
       return e;
-    for (auto f : {bwd_kernel<1>, bwd_kernel<2>, bwd_kernel<4>, bwd_kernel<8>})
-      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem)) != cudaSuccess)
-        return e;
+    if ((e = cudaFuncSetAttribute(bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  BwdLayout<1>::kSmem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  BwdLayout<2>::kSmem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  BwdLayout<4>::kSmem)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(bwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  BwdLayout<8>::kSmem)) != cudaSuccess)
+      return e;
     attr = true;
   }
   PxArgs pa;
@@ -1194,10 +1216,10 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.scale_idx = p.scale_idx;
   ba.kl_weight = kl_weight;
   switch (p.hg) {
-    case 1: bwd_kernel<1><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
-    case 2: bwd_kernel<2><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
-    case 4: bwd_kernel<4><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
-    default: bwd_kernel<8><<<sms, kBwdThreads, kBwdSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    case 1: bwd_kernel<1><<<sms, kBwdThreads, BwdLayout<1>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    case 2: bwd_kernel<2><<<sms, kBwdThreads, BwdLayout<2>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    case 4: bwd_kernel<4><<<sms, kBwdThreads, BwdLayout<4>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+    default: bwd_kernel<8><<<sms, kBwdThreads, BwdLayout<8>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
   }
   count_launches(6);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
