@@ -12,8 +12,9 @@
 // GB300 design. A work item is a run of up to 32 tiles from the inverted list
 // of one (b, g, KV block c). K_c and V_c (128 x 128 bf16 each) are staged once
 // per item by TMA; each tile gathers the Q rows of 128 / hg selecting queries
-// (hg heads each, 256 B per head row) with cp.async into a 128 x 128 K-major
-// SW128 tile. Per tile, tcgen05 computes S = Q K_c^T into TMEM; the softmax
+// with TMA, one box per query and 64-column chunk holding its hg head rows,
+// into a 128 x 128 K-major SW128 tile (TMA swizzles by the shared address, so
+// a box landing at row q * hg matches the tile's swizzle). Per tile, tcgen05 computes S = Q K_c^T into TMEM; the softmax
 // warps (one TMEM lane = one (query, head) row) mask keys past the query,
 // exponentiate, write P (bf16) to shared memory; tcgen05 computes O = P V_c
 // into TMEM; the same warps write the normalised partial O and its partial
@@ -23,22 +24,23 @@
 // A second kernel merges the k partials of every (query, head):
 // LSE = ln sum_s exp(lse_s), O = sum_s exp(lse_s - LSE) O_s.
 //
-// Warp roles (352 threads, one CTA per SM, persistent):
-//   warp 0      item fetch, K/V TMA, Q-row gathers for tile rows 0..63
-//   warp 10     Q-row gathers for tile rows 64..127
+// Warp roles (384 threads, one CTA per SM, persistent):
+//   warp 0      item fetch, K/V TMA, and producer 0
+//   warps 10-11 producers 1 and 2; producer p gathers the queries p, p + 3, ...
+//               of every tile into one of three Q stages, with the next tile's
+//               entries prefetched into registers
 //   warp 1      TMEM owner, UMMA issuer (one thread)
 //   warps 2..9  softmax + partial-output epilogue, two warpgroups that take
 //               even and odd tiles (ping-pong over the two S/O/P buffers)
-// The gather warps keep one tile's cp.async copies in flight while issuing the
-// next tile's, and publish a tile once its copies have landed.
 #include "msa_internal.h"
 #include "sm100.cuh"
 
 namespace msa {
 namespace {
 
-constexpr int kThreads = 352;  // 2 gather warps, 1 UMMA warp, 2 x 4 softmax/epilogue warps
-constexpr int kQStages = 2;
+constexpr int kThreads = 384;  // 3 producer warps, 1 UMMA warp, 2 x 4 softmax/epilogue warps
+constexpr int kFProd = 3;      // producer warps 0, 10, 11
+constexpr int kQStages = 3;
 constexpr int kTile = 32768;  // 128 rows x 128 bf16, as two 64-column SW128 chunks
 constexpr int kChunk = 16384;
 constexpr int kSmemBytes = (2 + kQStages + 2) * kTile + 1024;
@@ -67,7 +69,6 @@ struct FwdShared {
   uint64_t p_full[2], p_free[2];
   uint64_t o_full[2], o_empty[2];
   int4 item[2];
-  const __nv_bfloat16* tile_src[2][64];  // per gather warp: Q row base of each tile position (null: padding)
   uint32_t tmem_base;
   int abort;
 };
@@ -86,7 +87,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 template <int HG>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_fwd_kernel(FwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                      const __grid_constant__ CUtensorMap map_o) {
+                      const __grid_constant__ CUtensorMap map_o, const __grid_constant__ CUtensorMap map_q) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = smem;
@@ -99,7 +100,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 10);
+      mbar_init(&sh.it_empty[i], kFProd - 1 + 1 + 8);  // other producers, UMMA, softmax warps
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 4);
       mbar_init(&sh.p_full[i], 4);
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.o_empty[i], 4);
     }
     for (int i = 0; i < kQStages; ++i) {
-      mbar_init(&sh.q_full[i], 64);
+      mbar_init(&sh.q_full[i], kFProd);  // every producer (with its TMA bytes)
       mbar_init(&sh.q_empty[i], 1);
     }
     mbar_init(&sh.kv_full, 1);
@@ -128,39 +129,60 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int P = 128 / HG;  // query positions per tile
   const int n_items = *a.n_items;
 
-  // Gather of one tile half: rows [64 * hf, 64 * hf + 64) = positions
-  // [P/2 * hf, P/2 * hf + P/2); 64 rows x 16 chunks of 16 bytes, 32 per lane.
-  auto gather_half = [&](int hf, int b, int g, const int4& item, int j, uint32_t qdst) {
-    const __nv_bfloat16** src_of = sh.tile_src[hf];
-    __syncwarp();  // the previous tile's loop has finished reading src_of
-    for (int q = lane; q < P / 2; q += 32) {
-      const int idx = j * P + hf * (P / 2) + q;
-      const __nv_bfloat16* ptr = nullptr;
-      if (idx < item.z) {
-        const int t = a.entries[item.y + idx] >> 8;
-        ptr = a.Q + (((size_t)b * a.T + t) * a.Hq + g * HG) * 128;
+  // Producer p owns the queries p, p + kFProd, ... of every tile: per query,
+  // two TMA boxes (one per 64-column chunk) of its hg head rows, landing at
+  // rows q * hg. Padding queries load an out-of-range box (zero fill). Lane u
+  // issues requests lane + 32 u; their token rows come from the entries,
+  // prefetched one tile ahead.
+  constexpr int kMaxQ = (P + kFProd - 1) / kFProd;    // queries of producer 0 per tile
+  constexpr int kRPL = (2 * kMaxQ + 31) / 32;         // requests per lane
+  auto load_rows = [&](int p, int b, const int4& item, int j, int (&bt)[kRPL]) {
+    const int nq = (P - p + kFProd - 1) / kFProd;
+    const int BT = a.B * a.T;
+#pragma unroll
+    for (int u = 0; u < kRPL; ++u) {
+      const int o = lane + 32 * u;
+      int v = BT;
+      if (o < 2 * nq) {
+        const int idx = j * P + p + kFProd * (o >> 1);
+        if (idx < item.z) v = b * a.T + (a.entries[item.y + idx] >> 8);
       }
-      src_of[q] = ptr;
+      bt[u] = v;
+    }
+  };
+  auto issue_rows = [&](int p, int g, int qs, const int (&bt)[kRPL]) {
+    const int nq = (P - p + kFProd - 1) / kFProd;
+    if (lane == 0) mbar_arrive_expect_tx(&sh.q_full[qs], nq * HG * 256);
+    __syncwarp();
+    uint8_t* dst = sQ + qs * kTile;
+#pragma unroll
+    for (int u = 0; u < kRPL; ++u) {
+      const int o = lane + 32 * u;
+      if (o < 2 * nq) {
+        const int q = p + kFProd * (o >> 1), chunk = o & 1;
+        tma_load_3d(dst + chunk * kChunk + q * HG * 128, &map_q, &sh.q_full[qs], chunk * 64, g * HG, bt[u]);
+      }
     }
     __syncwarp();
-    const int chunk = lane & 15;
-    const uint32_t dst0 = qdst + (chunk >> 3) * kChunk;
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const int rl = 2 * i + (lane >> 4);  // row within the half
-      const int r = hf * 64 + rl;
-      const __nv_bfloat16* base = src_of[rl / HG];
-      const bool valid = base != nullptr;
-      const __nv_bfloat16* src = valid ? base + (rl % HG) * 128 + chunk * 8 : a.Q;
-      cp_async_16_zfill(dst0 + sw128_off(r, chunk & 7), src, valid);
+  };
+  auto produce_item = [&](int p, const int4& item, int b, int g, uint32_t& tj) -> bool {
+    const int ntiles = (item.z + P - 1) / P;
+    int bt[kRPL];
+    load_rows(p, b, item, 0, bt);
+    for (int j = 0; j < ntiles; ++j, ++tj) {
+      const int qs = tj % kQStages;
+      if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 303 + 30 * p)) return false;
+      issue_rows(p, g, qs, bt);
+      if (j + 1 < ntiles) load_rows(p, b, item, j + 1, bt);
     }
-    cp_async_commit();
+    return true;
   };
 
-  if (warp == 10) {
-    // ------------------------------------------------------------ second gather warp
+  const int prod = warp == 0 ? 0 : warp >= 10 ? warp - 9 : -1;
+  if (prod > 0) {
+    // ------------------------------------------------------------ producers 1, 2
+    if (lane == 0) tma_prefetch_desc(&map_q);
     uint32_t tj = 0;
-    int pend = -1;  // Q stage whose copies are in flight
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -171,36 +193,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item.x < 0) break;
       const int bg = item.x / a.n;
       const int b = bg / a.G, g = bg % a.G;
-      const int ntiles = (item.z + P - 1) / P;
-      bool ok = true;
-      for (int j = 0; j < ntiles; ++j, ++tj) {
-        const int qs = tj % kQStages;
-        if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 332)) { ok = false; break; }
-        gather_half(1, b, g, item, j, smem_u32(sQ + qs * kTile));
-        if (pend >= 0) {
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&sh.q_full[pend]);
-        }
-        pend = qs;
-      }
-      if (pend >= 0) {
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&sh.q_full[pend]);
-        pend = -1;
-      }
-      __syncwarp();
-      if (!ok) { *abort_flag = 1; break; }
+      if (!produce_item(prod, item, b, g, tj)) { *abort_flag = 1; break; }
     }
   } else if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ items, K/V, producer 0
     if (lane == 0) {
       tma_prefetch_desc(&map_k);
       tma_prefetch_desc(&map_v);
+      tma_prefetch_desc(&map_q);
     }
     uint32_t tj = 0;
-    int pend = -1;
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -233,27 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (*abort_flag) break;
-      const int ntiles = (item.z + P - 1) / P;
-      bool ok = true;
-      for (int j = 0; j < ntiles; ++j, ++tj) {
-        const int qs = tj % kQStages;
-        if (!mbar_wait(&sh.q_empty[qs], ((tj / kQStages) & 1) ^ 1, a.err, 303)) { ok = false; break; }
-        gather_half(0, b, g, item, j, smem_u32(sQ + qs * kTile));
-        if (pend >= 0) {  // the previous tile's copies: complete, publish
-          cp_async_wait<1>();
-          fence_proxy_async_smem();
-          mbar_arrive(&sh.q_full[pend]);
-        }
-        pend = qs;
-      }
-      if (pend >= 0) {
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(&sh.q_full[pend]);
-        pend = -1;
-      }
-      __syncwarp();
-      if (!ok) { *abort_flag = 1; break; }
+      if (!produce_item(0, item, b, g, tj)) { *abort_flag = 1; break; }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
@@ -573,7 +555,15 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
     return cudaErrorInvalidValue;
   if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  CUtensorMap mo;
+  CUtensorMap mo, mq;
+  {
+    // one query's head rows of its group: box {64 d, hg heads, 1 token}
+    const uint64_t qdims[3] = {128, (uint64_t)p.Hq, (uint64_t)p.BT()};
+    const uint64_t qstr[2] = {256, (uint64_t)p.Hq * 256};
+    const uint32_t qbox[3] = {64, (uint32_t)p.hg, 1};
+    if (!encode_tmap(&mq, const_cast<void*>(Q), 3, qdims, qstr, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   {
     const uint64_t odims[2] = {128, (uint64_t)L.max_padded * p.hg};
     const uint64_t ostr[1] = {256};
@@ -608,10 +598,10 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
     attr = true;
   }
   switch (p.hg) {
-    case 1: sparse_fwd_kernel<1><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
-    case 2: sparse_fwd_kernel<2><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
-    case 4: sparse_fwd_kernel<4><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
-    default: sparse_fwd_kernel<8><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo); break;
+    case 1: sparse_fwd_kernel<1><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
+    case 2: sparse_fwd_kernel<2><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
+    case 4: sparse_fwd_kernel<4><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
+    default: sparse_fwd_kernel<8><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
   }
   count_launches(2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
