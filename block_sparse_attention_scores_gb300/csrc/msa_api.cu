@@ -91,7 +91,7 @@ WsLayout ws_layout(const Prob& p, int which) {
   if (which >= MSA_WS_FWD) {
     L.list_count = take(lists * 4);
     L.list_off = take((lists + 1) * 4);
-    L.list_cursor = take(lists * 4);
+    L.chunk_off = take((size_t)p.B * p.G * ((size_t)p.n * (p.n + 1) / 2) * 4);
     L.list_poff = take((lists + 1) * 4);
     L.entries = take(rows * p.G * p.k * 4);
     L.rev = take(rows * p.G * p.k * 4);

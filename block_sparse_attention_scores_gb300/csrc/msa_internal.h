@@ -28,7 +28,7 @@ struct WsLayout {
   size_t counters = 64;     // int32 work counters [16]
   size_t list_count = 0;    // int32 [B*G*n]   selections per KV block
   size_t list_off = 0;      // int32 [B*G*n+1] exclusive prefix of list_count
-  size_t list_cursor = 0;   // int32 [B*G*n]   scatter cursors
+  size_t chunk_off = 0;     // int32 [B*G, n(n+1)/2] per (list, query block): position of its first entry
   size_t list_poff = 0;     // int32 [B*G*n+1] prefix of list lengths padded to whole tiles
   size_t rev = 0;           // int32 [B*G*T*k] padded entry index of (b, g, t, slot)
   size_t entries = 0;       // int32 [B*G*T*k] (t << 8 | slot), grouped by list

@@ -6,18 +6,23 @@
 // the block is staged in shared memory once and reused by all of them.
 //
 // Lists are keyed by l = (b * G + g) * n + c. Entry = (t << 8) | slot, where
-// slot is the position of c in block_idx[b, g, t, :]. Build:
-//   1. count   -- validate every row, count selections per list (atomics)
-//   2. scan    -- exclusive prefix over lists; emit work items in descending
-//                 list-length order (block id ascending first, which is the
-//                 order of decreasing expected length)
-//   3. scatter -- place entries with per-list cursors (atomics)
-//   4. sort    -- sort each list by t (deterministic order; lists longer than
-//                 the shared-memory buffer keep scatter order, which changes
-//                 only the fp32 summation order downstream), and record the
-//                 reverse map (b, g, t, slot) -> padded entry index, so the
-//                 kernels can write per-(query, slot) partials in tile order
-//                 (whole tiles, one TMA store each) and the merges find them
+// slot is the position of c in block_idx[b, g, t, :]. Every list comes out
+// sorted by t, with no atomics on global counters and no sort pass: the
+// queries are cut into chunks of 128 (one query block qb), and a chunk only
+// selects blocks c <= qb. Build:
+//   1. chunk count -- one CTA per (b, g, qb): validate its 128 rows, mark in
+//                     shared bitmaps which rows select each block c, write the
+//                     popcounts to chunk_off[(b, g), c, qb] (upper triangle)
+//   2. chunk scan  -- per list: exclusive prefix over qb (the chunk's first
+//                     position in the list) and the list length
+//   3. list scan   -- exclusive prefix over lists (and over lists padded to
+//                     whole tiles); work items in block-id-major order, which
+//                     is the order of decreasing expected list length
+//   4. scatter     -- one CTA per chunk again: an entry's position is its
+//                     chunk's offset plus the rows before it in the bitmap;
+//                     also the reverse map (b, g, t, slot) -> padded entry
+//                     index, so the kernels write per-(query, slot) partials in
+//                     tile order and the merges find them
 #include "msa_internal.h"
 #include "sm100.cuh"
 
@@ -44,22 +49,70 @@ __device__ __forceinline__ int check_row(const int32_t* row, int k, int own) {
   return (ok && has_own) ? nvalid : -1;
 }
 
-__global__ void map_count_kernel(const int32_t* __restrict__ block_idx, int B, int G, int T, int n, int k,
-                                 int* __restrict__ count, int* err) {
-  const long long rows = (long long)B * G * T;
-  for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows;
-       r += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(r % T);
-    const long long bg = r / T;
-    const int32_t* row = block_idx + r * k;
-    if (check_row(row, k, t / 128) < 0) {
-      dev_fail(err, kDevBadIndex, 201);
-      continue;
-    }
+// Position of (block c, query block qb), 0 <= c <= qb < n, in one (b, g)'s
+// upper triangle, stored list-major: the chunks of list c are contiguous.
+__device__ __forceinline__ long long tri_index(int c, int qb, int n) {
+  return (long long)c * n - (long long)c * (c - 1) / 2 + (qb - c);
+}
+
+// Shared bitmaps of one chunk: bit (row) of mask[4 c .. 4 c + 3] is set when
+// that row of the chunk selects block c. Returns false for an invalid row.
+__device__ __forceinline__ bool chunk_masks(const int32_t* __restrict__ block_idx, long long bg, int qb, int T,
+                                            int k, uint32_t* mask, int* err, int where) {
+  const int tl = threadIdx.x;
+  for (int i = tl; i < (qb + 1) * 4; i += 128) mask[i] = 0u;
+  __syncthreads();
+  const int32_t* row = block_idx + ((size_t)bg * T + (size_t)qb * 128 + tl) * k;
+  const bool valid = check_row(row, k, qb) >= 0;
+  if (!valid) {
+    dev_fail(err, kDevBadIndex, where);
+  } else {
     for (int i = 0; i < k; ++i) {
       const int c = row[i];
-      if (c >= 0) atomicAdd(&count[bg * n + c], 1);
+      if (c >= 0) atomicOr(&mask[c * 4 + (tl >> 5)], 1u << (tl & 31));
     }
+  }
+  __syncthreads();
+  return valid;
+}
+
+// One CTA (128 threads = rows) per (b, g, qb).
+__global__ void __launch_bounds__(128) map_chunk_count_kernel(const int32_t* __restrict__ block_idx, int T, int n,
+                                                              int k, int* __restrict__ chunk_off, int* err) {
+  extern __shared__ uint32_t mask[];
+  const int qb = blockIdx.x % n;
+  const long long bg = blockIdx.x / n;
+  chunk_masks(block_idx, bg, qb, T, k, mask, err, 201);
+  int* tri = chunk_off + bg * ((long long)n * (n + 1) / 2);
+  for (int c = threadIdx.x; c <= qb; c += 128)
+    tri[tri_index(c, qb, n)] =
+        __popc(mask[4 * c]) + __popc(mask[4 * c + 1]) + __popc(mask[4 * c + 2]) + __popc(mask[4 * c + 3]);
+}
+
+// One warp per list (bg, c): exclusive prefix of its chunk counts over qb, in
+// place, and the list length.
+__global__ void map_chunk_scan_kernel(int L, int n, int* __restrict__ chunk_off, int* __restrict__ count) {
+  const int lane = threadIdx.x & 31;
+  for (long long l = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; l < L;
+       l += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const long long bg = l / n;
+    const int c = (int)(l - bg * n);
+    int* run = chunk_off + bg * ((long long)n * (n + 1) / 2) + tri_index(c, c, n);
+    const int len = n - c;
+    int carry = 0;
+    for (int base = 0; base < len; base += 32) {
+      const int i = base + lane;
+      const int v = i < len ? run[i] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (i < len) run[i] = carry + x - v;
+      carry += __shfl_sync(0xffffffffu, x, 31);
+    }
+    if (lane == 0) count[l] = carry;
   }
 }
 
@@ -150,66 +203,33 @@ __global__ void __launch_bounds__(1024) map_scan_kernel(const int* __restrict__ 
   if (tid == 0) *n_items = min(carry, max_items);
 }
 
-__global__ void map_scatter_kernel(const int32_t* __restrict__ block_idx, int B, int G, int T, int n, int k,
-                                   const int* __restrict__ off, int* __restrict__ cursor,
-                                   int32_t* __restrict__ entries) {
-  const long long rows = (long long)B * G * T;
-  for (long long r = blockIdx.x * (long long)blockDim.x + threadIdx.x; r < rows;
-       r += (long long)gridDim.x * blockDim.x) {
-    const int t = (int)(r % T);
-    const long long bg = r / T;
-    const int32_t* row = block_idx + r * k;
-    if (check_row(row, k, t / 128) < 0) continue;
-    for (int i = 0; i < k; ++i) {
-      const int c = row[i];
-      if (c < 0) continue;
-      const long long l = bg * n + c;
-      const int pos = atomicAdd(&cursor[l], 1);
-      entries[off[l] + pos] = (t << 8) | i;
-    }
-  }
-}
-
-constexpr int kSortCap = 16384;
-
-// Sorts each list by query (lists up to kSortCap entries; longer ones keep
-// scatter order), then records for every (b, g, t, slot) the padded
-// partial-output index of its entry: rev[(bg * T + t) * k + slot].
-__global__ void __launch_bounds__(1024) map_sort_kernel(const int* __restrict__ off, const int* __restrict__ poff,
-                                                        int L, int n, int T, int k, int32_t* __restrict__ entries,
-                                                        int32_t* __restrict__ rev) {
-  extern __shared__ int32_t keys[];
-  for (int l = blockIdx.x; l < L; l += gridDim.x) {
-    const int start = off[l], len = off[l + 1] - start;
-    if (len > 1 && len <= kSortCap) {
-      int np = 1;
-      while (np < len) np <<= 1;
-      for (int i = threadIdx.x; i < np; i += blockDim.x) keys[i] = i < len ? entries[start + i] : 0x7fffffff;
-      __syncthreads();
-      for (int size = 2; size <= np; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int i = threadIdx.x; i < np / 2; i += blockDim.x) {
-            const int lo = 2 * i - (i & (stride - 1));
-            const int hi = lo + stride;
-            const bool up = ((lo & size) == 0);
-            const int a = keys[lo], b = keys[hi];
-            if ((a > b) == up) {
-              keys[lo] = b;
-              keys[hi] = a;
-            }
-          }
-          __syncthreads();
-        }
-      }
-      for (int i = threadIdx.x; i < len; i += blockDim.x) entries[start + i] = keys[i];
-      __syncthreads();
-    }
-    const long long bg = l / n;
-    for (int i = threadIdx.x; i < len; i += blockDim.x) {
-      const int e = entries[start + i];
-      rev[(bg * T + (e >> 8)) * k + (e & 255)] = poff[l] + i;
-    }
-    __syncthreads();
+// One CTA (128 threads = rows) per (b, g, qb): entries in query order and
+// the reverse map.
+__global__ void __launch_bounds__(128) map_chunk_scatter_kernel(const int32_t* __restrict__ block_idx, int T, int n,
+                                                                int k, const int* __restrict__ chunk_off,
+                                                                const int* __restrict__ off,
+                                                                const int* __restrict__ poff,
+                                                                int32_t* __restrict__ entries,
+                                                                int32_t* __restrict__ rev, int* err) {
+  extern __shared__ uint32_t mask[];
+  const int qb = blockIdx.x % n;
+  const long long bg = blockIdx.x / n;
+  if (!chunk_masks(block_idx, bg, qb, T, k, mask, err, 203)) return;  // after the last barrier
+  const int tl = threadIdx.x, t = qb * 128 + tl;
+  const int w = tl >> 5;
+  const uint32_t below = (1u << (tl & 31)) - 1u;
+  const int* tri = chunk_off + bg * ((long long)n * (n + 1) / 2);
+  const size_t rrow = ((size_t)bg * T + t) * k;
+  for (int i = 0; i < k; ++i) {
+    const int c = block_idx[rrow + i];
+    if (c < 0) continue;
+    const uint32_t* mk = mask + 4 * c;
+    int rank = __popc(mk[w] & below);
+    for (int u = 0; u < w; ++u) rank += __popc(mk[u]);
+    const long long l = bg * n + c;
+    const int pos = tri[tri_index(c, qb, n)] + rank;  // position within the list
+    entries[off[l] + pos] = (t << 8) | i;
+    rev[rrow + i] = poff[l] + pos;
   }
 }
 
@@ -220,7 +240,7 @@ cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws
   const int lists = p.B * p.G * p.n;
   int* count = reinterpret_cast<int*>(ws + L.list_count);
   int* off = reinterpret_cast<int*>(ws + L.list_off);
-  int* cursor = reinterpret_cast<int*>(ws + L.list_cursor);
+  int* chunk = reinterpret_cast<int*>(ws + L.chunk_off);
   int* poff = reinterpret_cast<int*>(ws + L.list_poff);
   int32_t* rev = reinterpret_cast<int32_t*>(ws + L.rev);
   int32_t* entries = reinterpret_cast<int32_t*>(ws + L.entries);
@@ -228,25 +248,26 @@ cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws
   int* n_items = reinterpret_cast<int*>(ws + L.n_items);
   int* err = reinterpret_cast<int*>(ws + L.err);
   cudaError_t e;
-  if ((e = cudaMemsetAsync(count, 0, (size_t)lists * 4, st)) != cudaSuccess) return e;
-  if ((e = cudaMemsetAsync(cursor, 0, (size_t)lists * 4, st)) != cudaSuccess) return e;
   // rows that fail validation never get an entry: their reverse-map slots stay -1
   if ((e = cudaMemsetAsync(rev, 0xff, (size_t)p.B * p.G * p.T * p.k * 4, st)) != cudaSuccess) return e;
-  const long long rows = (long long)p.B * p.G * p.T;
-  const int grid = (int)std::min<long long>((rows + 255) / 256, 8LL * num_sms());
-  map_count_kernel<<<grid, 256, 0, st>>>(block_idx, p.B, p.G, p.T, p.n, p.k, count, err);
+  const int chunks = p.B * p.G * p.n;  // one per (b, g, query block)
+  const int mask_bytes = p.n * 16;     // bitmaps of blocks 0..qb, 128 rows each
+  static int attr_bytes = 0;
+  if (mask_bytes > 48 * 1024 && mask_bytes > attr_bytes) {
+    if ((e = cudaFuncSetAttribute(map_chunk_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  mask_bytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(map_chunk_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  mask_bytes)) != cudaSuccess)
+      return e;
+    attr_bytes = mask_bytes;
+  }
+  map_chunk_count_kernel<<<chunks, 128, mask_bytes, st>>>(block_idx, p.T, p.n, p.k, chunk, err);
+  map_chunk_scan_kernel<<<(int)std::min<long long>(((long long)lists * 32 + 255) / 256, 16LL * num_sms()), 256, 0,
+                          st>>>(lists, p.n, chunk, count);
   map_scan_kernel<<<1, 1024, 0, st>>>(count, lists, p.B * p.G, p.n, rows_per_tile, tiles_per_item, off, poff,
                                       items, L.max_items, n_items, err);
-  map_scatter_kernel<<<grid, 256, 0, st>>>(block_idx, p.B, p.G, p.T, p.n, p.k, off, cursor, entries);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if ((e = cudaFuncSetAttribute(map_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSortCap * 4)) !=
-        cudaSuccess)
-      return e;
-    attr_set = true;
-  }
-  map_sort_kernel<<<std::min(lists, 4 * num_sms()), 1024, kSortCap * 4, st>>>(off, poff, lists, p.n, p.T, p.k,
-                                                                              entries, rev);
+  map_chunk_scatter_kernel<<<chunks, 128, mask_bytes, st>>>(block_idx, p.T, p.n, p.k, chunk, off, poff, entries,
+                                                             rev, err);
   count_launches(4);
   return cudaGetLastError();
 }
