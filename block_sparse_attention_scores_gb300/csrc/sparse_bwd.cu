@@ -78,10 +78,14 @@ __global__ void drow_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bflo
 }
 
 // ============================================================================ px stats
-// One CTA per SM, persistent over whole lists. 128 queries per tile.
-constexpr int kPxThreads = 192;
+// One CTA per SM, persistent over whole lists. 128 queries per tile, gathered
+// by four producer warps (32 rows each: warp 0, which also fetches the items
+// and the k_idx block, and warps 6-8) into three stages; warp 1 issues the
+// UMMAs, warps 2-5 reduce the 128 scores of their row.
+constexpr int kPxThreads = 288;
 constexpr int kPxTile = 16384;  // 128 rows x 64 bf16
-constexpr int kPxSmem = 3 * kPxTile + 1024;
+constexpr int kPxStages = 3;
+constexpr int kPxSmem = (1 + kPxStages) * kPxTile + 1024;
 
 struct PxArgs {
   const __nv_bfloat16* q_idx;
@@ -98,10 +102,9 @@ struct PxArgs {
 struct PxShared {
   uint64_t it_full[2], it_empty[2];
   uint64_t kv_full, kv_empty;
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kPxStages], q_empty[kPxStages];
   uint64_t s_full[2], s_empty[2];
   int4 item[2];
-  int tile_t[128];  // producer scratch: query of each tile position
   uint32_t tmem_base;
   int abort;
 };
@@ -111,17 +114,19 @@ __global__ void __launch_bounds__(kPxThreads, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sKI = smem;
-  uint8_t* sQ = smem + kPxTile;  // 2 tiles
+  uint8_t* sQ = smem + kPxTile;  // kPxStages tiles
   __shared__ PxShared sh;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
-      mbar_init(&sh.it_empty[i], 5);
-      mbar_init(&sh.q_full[i], 32);
-      mbar_init(&sh.q_empty[i], 1);
+      mbar_init(&sh.it_empty[i], 3 + 1 + 4);  // other producers, UMMA, reduction warps
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.s_empty[i], 4);
+    }
+    for (int i = 0; i < kPxStages; ++i) {
+      mbar_init(&sh.q_full[i], 128);  // every producer lane, after its copies
+      mbar_init(&sh.q_empty[i], 1);
     }
     mbar_init(&sh.kv_full, 1);
     mbar_init(&sh.kv_empty, 1);
@@ -139,56 +144,68 @@ __global__ void __launch_bounds__(kPxThreads, 1)
   volatile int* abort_flag = &sh.abort;
   const int n_items = *a.n_items;
 
-  if (warp == 0) {
+  const int pxp = warp == 0 ? 0 : (warp >= 6 ? warp - 5 : -1);  // producer index: rows [32 pxp, 32 pxp + 32)
+  if (pxp >= 0) {
     uint32_t tj = 0;
-    const int chunk = lane & 7;
     for (int it = 0;; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
       int4 item = make_int4(-1, 0, 0, 0);
-      if (lane == 0) {
-        if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 401)) *abort_flag = 1;
-        const int id = atomicAdd(a.counter, 1);
-        if (id < n_items && !*abort_flag) item = a.items[id];
-        sh.item[s] = item;
-        mbar_arrive(&sh.it_full[s]);
+      if (pxp == 0) {
+        if (lane == 0) {
+          if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 401)) *abort_flag = 1;
+          const int id = atomicAdd(a.counter, 1);
+          if (id < n_items && !*abort_flag) item = a.items[id];
+          sh.item[s] = item;
+          mbar_arrive(&sh.it_full[s]);
+        }
+        item.x = __shfl_sync(0xffffffffu, item.x, 0);
+        item.y = __shfl_sync(0xffffffffu, item.y, 0);
+        item.z = __shfl_sync(0xffffffffu, item.z, 0);
+      } else {
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 404)) { *abort_flag = 1; break; }
+        item = sh.item[s];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.it_empty[s]);
       }
-      item.x = __shfl_sync(0xffffffffu, item.x, 0);
-      item.y = __shfl_sync(0xffffffffu, item.y, 0);
-      item.z = __shfl_sync(0xffffffffu, item.z, 0);
       if (item.x < 0) break;
       int b, g, c;
       decode_list(item.x, a.n, a.G, b, g, c);
-      if (lane == 0) {
-        if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 402)) {
-          mbar_arrive_expect_tx(&sh.kv_full, kPxTile);
-          tma_load_2d(sKI, &map_ki, &sh.kv_full, 0, b * a.T + c * 128);
-        } else {
-          *abort_flag = 1;
-        }
-      }
-      __syncwarp();
-      if (*abort_flag) break;
-      const int ntiles = (item.z + 127) / 128;
-      bool ok = true;
-      for (int j = 0; j < ntiles; ++j, ++tj) {
-        const int qs = tj & 1;
-        if (!mbar_wait(&sh.q_empty[qs], ((tj >> 1) & 1) ^ 1, a.err, 403)) { ok = false; break; }
-        const uint32_t dst0 = smem_u32(sQ + qs * kPxTile);
-        for (int p = lane; p < 128; p += 32) {
-          const int idx = j * 128 + p;
-          sh.tile_t[p] = idx < item.z ? (a.entries[item.y + idx] >> 8) : -1;
+      if (pxp == 0) {
+        if (lane == 0) {
+          if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 402)) {
+            mbar_arrive_expect_tx(&sh.kv_full, kPxTile);
+            tma_load_2d(sKI, &map_ki, &sh.kv_full, 0, b * a.T + c * 128);
+          } else {
+            *abort_flag = 1;
+          }
         }
         __syncwarp();
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-          const int r = 4 * i + (lane >> 3);
-          const int tq = sh.tile_t[r];
+        if (*abort_flag) break;
+      }
+      const int ntiles = (item.z + 127) / 128;
+      // lane = row 32 pxp + lane: its query, one tile ahead
+      auto row_t = [&](int j) -> int {
+        const int idx = j * 128 + 32 * pxp + lane;
+        return idx < item.z ? (a.entries[item.y + idx] >> 8) : -1;
+      };
+      int t_own = row_t(0);
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int qs = tj % kPxStages;
+        if (!mbar_wait(&sh.q_empty[qs], ((tj / kPxStages) & 1) ^ 1, a.err, 403)) { ok = false; break; }
+        const uint32_t dst0 = smem_u32(sQ + qs * kPxTile);
+        // 32 rows x 8 chunks: lane -> (row 4 i + lane / 8, chunk lane % 8)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int rl = 4 * i + (lane >> 3), chunk = lane & 7;
+          const int tq = __shfl_sync(0xffffffffu, t_own, rl);
           const bool valid = tq >= 0;
           const __nv_bfloat16* src = a.q_idx + ((((size_t)b * a.T + (valid ? tq : 0)) * a.G + g) * 64 + chunk * 8);
-          cp_async_16_zfill(dst0 + sw128_off(r, chunk), src, valid);
+          cp_async_16_zfill(dst0 + sw128_off(32 * pxp + rl, chunk), src, valid);
         }
         cp_async_commit();
+        if (j + 1 < ntiles) t_own = row_t(j + 1);
         cp_async_wait<0>();
         fence_proxy_async_smem();
         mbar_arrive(&sh.q_full[qs]);
@@ -212,17 +229,17 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         const int ntiles = (item.z + 127) / 128;
         if (!mbar_wait(&sh.kv_full, it & 1, a.err, 412)) { ok = false; break; }
         for (int j = 0; j < ntiles; ++j, ++tj) {
-          const int sb = tj & 1;
-          if (!mbar_wait(&sh.q_full[sb], (tj >> 1) & 1, a.err, 413)) { ok = false; break; }
+          const int sb = tj & 1, qs = tj % kPxStages;
+          if (!mbar_wait(&sh.q_full[qs], (tj / kPxStages) & 1, a.err, 413)) { ok = false; break; }
           if (!mbar_wait(&sh.s_empty[sb], ((tj >> 1) & 1) ^ 1, a.err, 414)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t q0 = smem_u32(sQ + sb * kPxTile);
+          const uint32_t q0 = smem_u32(sQ + qs * kPxTile);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16_ss(tmem + sb * 128, make_sdesc(q0 + ks * 32, 16, 1024, kSw128),
                          make_sdesc(k0 + ks * 32, 16, 1024, kSw128), idesc, ks > 0);
           umma_commit(&sh.s_full[sb]);
-          umma_commit(&sh.q_empty[sb]);
+          umma_commit(&sh.q_empty[qs]);
         }
         umma_commit(&sh.kv_empty);
       }
