@@ -413,6 +413,7 @@ struct BwdShared {
   uint64_t s_full, s_read, dp_full, x_full;  // S^T computed / loaded by the epilogue, dP^T and X^T computed
   uint64_t p_ready, ds_ready, gs_ready, ph2_full;
   uint64_t r_free[2], x_free;  // a tile's dQ^T / dq_idx^T read out of TMEM (by tile parity / every tile)
+  uint64_t pv_free;            // dV += P^T dO of a tile complete: P^T may be overwritten
   uint64_t acc_free;
   uint64_t kl_ready, kl_free;  // KL sums of a tile complete / read and cleared
   RowMeta meta[3];  // one per gather buffer
@@ -482,6 +483,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&sh.r_free[0], 8);
     mbar_init(&sh.r_free[1], 8);
     mbar_init(&sh.x_free, 8);
+    mbar_init(&sh.pv_free, 1);
     mbar_init(&sh.acc_free, 8);
     mbar_init(&sh.kl_ready, 8);
     mbar_init(&sh.kl_free, 1);
@@ -677,31 +679,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (item.x < 0) break;
         const int ntiles = (item.z + npos - 1) / npos;
         if (!mbar_wait(&sh.kv_full, it & 1, a.err, 512)) { ok = false; break; }
-        for (int j = 0; j < ntiles; ++j, ++tj) {
-          const int gb = tj % kNG;
-          if (!mbar_wait(&sh.g_full[gb], (tj / kNG) & 1, a.err, 513)) { ok = false; break; }
-          // region cR[tj & 1] was read out by the epilogue of tile tj - 2
-          if (!mbar_wait(&sh.r_free[tj & 1], ((tj >> 1) & 1) ^ 1, a.err, 514)) { ok = false; break; }
+        // S^T of a tile, into region cR[tile & 1], once its gather buffer is
+        // full and the readout of tile - 2 has freed that region
+        auto issue_s = [&](uint32_t u) -> bool {
+          const int ub = u % kNG;
+          if (!mbar_wait(&sh.g_full[ub], (u / kNG) & 1, a.err, 513)) return false;
+          if (!mbar_wait(&sh.r_free[u & 1], ((u >> 1) & 1) ^ 1, a.err, 514)) return false;
           tc_fence_after();
-          const uint32_t tR = tmem + cR0 + 64 * (tj & 1);
-          const uint32_t goff = gb * kGather;
-          const uint64_t bQ = at(dG, goff), bO = at(dG, goff + kRowTile), bQI = at(dG, goff + 2 * kRowTile);
-          const uint64_t bQt = at(dGt, goff), bOt = at(dGt, goff + kRowTile);
-          // S^T = K Q^T
+          const uint64_t bq = at(dG, ub * kGather);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
             const uint32_t ao = (ks >> 2) * (kKV / 2) + (ks & 3) * 32;
             const uint32_t bo = (ks >> 2) * kRowChunk + (ks & 3) * 32;
-            umma_bf16_ss(tR, at(dK, ao), at(bQ, bo), id_sT, ks > 0);
+            umma_bf16_ss(tmem + cR0 + 64 * (u & 1), at(dK, ao), at(bq, bo), id_sT, ks > 0);
           }
           umma_commit(&sh.s_full);
-          // X^T = KI QI^T, once the previous tile's dq_idx^T has been read
-          if (!mbar_wait(&sh.x_free, (tj & 1) ^ 1, a.err, 519)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) umma_bf16_ss(tmem + cX, at(dKI, ks * 32), at(bQI, ks * 32), id_x, ks > 0);
-          umma_commit(&sh.x_full);
-          // dP^T = V dO^T into the same columns, once every epilogue warp has loaded S^T
+          return true;
+        };
+        // Per tile, in the order the epilogue releases its operands; the next
+        // tile's S^T goes out once this tile's dK / dQ^T are queued, so that it
+        // is computed while the epilogue works on this tile's index branch.
+        bool s_issued = false;  // this tile's S^T went out during the previous tile
+        for (int j = 0; j < ntiles; ++j, ++tj) {
+          const int gb = tj % kNG;
+          if (!s_issued && !issue_s(tj)) { ok = false; break; }
+          s_issued = false;
+          const uint32_t tR = tmem + cR0 + 64 * (tj & 1);
+          const uint32_t goff = gb * kGather;
+          const uint64_t bO = at(dG, goff + kRowTile), bQI = at(dG, goff + 2 * kRowTile);
+          const uint64_t bQt = at(dGt, goff), bOt = at(dGt, goff + kRowTile);
+          // dP^T = V dO^T into S^T's columns, once every epilogue warp has loaded S^T
           if (!mbar_wait(&sh.s_read, tj & 1, a.err, 520)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -711,19 +718,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             umma_bf16_ss(tR, at(dV, ao), at(bO, bo), id_sT, ks > 0);
           }
           umma_commit(&sh.dp_full);
-          // phase 2, released in three steps by the epilogue: P^T (dV), dS^T
-          // (dK, dQ^T), gs^T (dk_idx, dq_idx^T)
+          // dV += P^T dO   (K = 64 rows, 16 per step)
           if (!mbar_wait(&sh.p_ready, tj & 1, a.err, 515)) { ok = false; break; }
           if (j == 0 && !mbar_wait(&sh.acc_free, (it & 1) ^ 1, a.err, 516)) { ok = false; break; }
           tc_fence_after();
           const uint32_t acc = (j > 0) ? 1u : 0u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {  // dV += P^T dO   (K = 64 rows, 16 per step)
+          for (int ks = 0; ks < 4; ++ks) {
             if constexpr (kPTmem)
               umma_bf16_ts(tmem + cDV, tmem + cP + ks * 8, at(bOt, ks * 2048), id_acc, acc | (ks > 0));
             else
               umma_bf16_ss(tmem + cDV, at(dPT, ks * 32), at(bOt, ks * 2048), id_acc, acc | (ks > 0));
           }
+          umma_commit(&sh.pv_free);
+          // X^T = KI QI^T, once the previous tile's dq_idx^T has been read
+          if (!mbar_wait(&sh.x_free, (tj & 1) ^ 1, a.err, 519)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) umma_bf16_ss(tmem + cX, at(dKI, ks * 32), at(bQI, ks * 32), id_x, ks > 0);
+          umma_commit(&sh.x_full);
           if (!mbar_wait(&sh.ds_ready, tj & 1, a.err, 517)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -732,6 +745,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)  // dQ^T = K^T dS^T into cR (dP^T has been loaded)   (K = 128 keys)
             umma_bf16_ss(tR, at(dKt, ks * 2048), at(dDS, ks * 2048), id_tr, ks > 0);
+          if (j + 1 < ntiles) {
+            if (!issue_s(tj + 1)) { ok = false; break; }
+            s_issued = true;
+          }
           if (!mbar_wait(&sh.gs_ready, tj & 1, a.err, 518)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -759,6 +776,69 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const bool kl_writer = warp == 2;   // a quarter-2 warp: no dq_idx^T rows to store
     uint32_t tj = 0;
     bool ok = true;
+    // Tile whose phase-2 results (dQ^T, dq_idx^T) are still in TMEM: they are
+    // read out after the next tile's stage A, so the tensor core computes that
+    // tile's dP^T while this readout runs.
+    bool pend = false;
+    uint32_t p_tj = 0;
+    int p_pos0 = 0, p_b = 0, p_g = 0;
+    // ---- phase-2 readout: dQ^T (lane = d), dq_idx^T (lane = e < 64)
+    // Partials are in tile order: a tile's 64 (query, head) rows are
+    // consecutive. Each warp stages its 32 x 32 slice row-major in the tile's
+    // own gather buffer (free once the phase-2 MMAs are complete) and writes
+    // it with one TMA store; the buffer goes back to the producers when the
+    // stores have read it.
+    auto epi2 = [&]() -> bool {
+      const int pgb = p_tj % kNG;
+      const RowMeta& mp = sh.meta[pgb];
+      if (!mbar_wait(&sh.ph2_full, p_tj & 1, a.err, 524)) return false;
+      tc_fence_after();
+      {
+        uint8_t* gbuf = smem + oG + pgb * kGather;
+        const int prow0 = p_pos0 * hg;  // first dQ partial row of the tile
+        __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(gbuf + (hf * 4 + quarter) * 2048);
+        float* stq = reinterpret_cast<float*>(gbuf + kRowTile + (hf * 2 + (quarter & 1)) * 4096);
+        float dq[32];
+        tmem_ld32(tmem + lane_off + cR0 + 64 * (p_tj & 1) + col0, dq);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __float2bfloat16_rn(dq[i]);
+        if (quarter < 2) {
+          float dqi[kQ];
+          tmem_ld_cols<kQ>(tmem + lane_off + cX + hf * kQ, dqi);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < kQ; ++i) stq[i * 32 + lane] = dqi[i];
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&sh.r_free[p_tj & 1]);  // TMEM read: cR may take tile p_tj + 2's S^T,
+          mbar_arrive(&sh.x_free);            // cX the next tile's X^T
+          tma_store_2d(&map_dq, stg, quarter * 32, prow0 + col0);
+          if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, p_pos0 + hf * kQ);
+          bulk_commit();
+        }
+      }
+      if (kl_writer) {
+        // every epilogue warp has added its KL terms: write the per-query sums
+        if (!mbar_wait(&sh.kl_ready, p_tj & 1, a.err, 526)) return false;
+        for (int q = lane; q < npos; q += 32) {
+          const int e = mp.ent[q * hg];
+          if (e >= 0) a.kl_part[(((size_t)p_b * a.T + (e >> 8)) * a.G + p_g) * a.k + (e & 255)] = sh.kl_acc[q];
+          sh.kl_acc[q] = 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.kl_free);
+      }
+      if (lane == 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&sh.g_empty[pgb]);
+      }
+      __syncwarp();
+      return true;
+    };
     for (int it = 0; ok; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -813,6 +893,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               pv[4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
             }
           }
+          // the previous tile's dV MMA has read P^T
+          if (!mbar_wait(&sh.pv_free, (tj & 1) ^ 1, a.err, 529)) { ok = false; break; }
+          tc_fence_after();
           if constexpr (kPTmem) {
             uint32_t pk[16];  // P^T row of this key, bf16 pairs (low half = even row)
 #pragma unroll
@@ -830,6 +913,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.p_ready);
+        }
+        if (pend) {  // the previous tile's phase-2 readout
+          if (!epi2()) { ok = false; break; }
+          pend = false;
         }
         {  // stage B: dS = P (dP - D) * scale
           float dp[32];
@@ -899,61 +986,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.kl_ready);
         }
-        // ---- phase-2 epilogue: dQ^T (lane = d), dq_idx^T (lane = e < 64)
-        // Partials are in tile order: this tile's 64 (query, head) rows are
-        // consecutive. Each warp stages its 32 x 32 slice row-major in the
-        // tile's own gather buffer (free once the phase-2 MMAs are complete)
-        // and writes it with one TMA store; the buffer goes back to the
-        // producers when the stores have read it.
-        if (!mbar_wait(&sh.ph2_full, tj & 1, a.err, 524)) { ok = false; break; }
-        tc_fence_after();
-        {
-          uint8_t* gbuf = smem + oG + gb * kGather;
-          const int prow0 = (item.w + j * npos) * hg;  // first dQ partial row of the tile
-          const int pos0 = item.w + j * npos;          // first dq_idx partial row
-          __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(gbuf + (hf * 4 + quarter) * 2048);
-          float* stq = reinterpret_cast<float*>(gbuf + kRowTile + (hf * 2 + (quarter & 1)) * 4096);
-          float dq[32];
-          tmem_ld32(tmem + lane_off + cR + col0, dq);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) stg[i * 32 + lane] = __float2bfloat16_rn(dq[i]);
-          if (quarter < 2) {
-            float dqi[kQ];
-            tmem_ld_cols<kQ>(tmem + lane_off + cX + hf * kQ, dqi);
-            tmem_wait_ld();
-#pragma unroll
-            for (int i = 0; i < kQ; ++i) stq[i * 32 + lane] = dqi[i];
-          }
-          tc_fence_before();
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(&sh.r_free[tj & 1]);  // TMEM read: cR may take tile tj + 2's S^T,
-            mbar_arrive(&sh.x_free);          // cX the next tile's X^T
-            tma_store_2d(&map_dq, stg, quarter * 32, prow0 + col0);
-            if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kQ);
-            bulk_commit();
-          }
-        }
-        if (kl_writer) {
-          // every epilogue warp has added its KL terms: write the per-query sums
-          if (!mbar_wait(&sh.kl_ready, tj & 1, a.err, 526)) { ok = false; break; }
-          for (int q = lane; q < npos; q += 32) {
-            const int e = m.ent[q * hg];
-            if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
-            sh.kl_acc[q] = 0.f;
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.kl_free);
-        }
-        if (lane == 0) {
-          bulk_wait_read_all();
-          mbar_arrive(&sh.g_empty[gb]);
-        }
-        __syncwarp();
+        pend = true;  // this tile's dQ^T / dq_idx^T are read out after the next tile's stage A
+        p_tj = tj;
+        p_pos0 = item.w + j * npos;
+        p_b = b;
+        p_g = g;
       }
       if (!ok) break;
+      if (pend) {
+        if (!epi2()) { ok = false; break; }
+        pend = false;
+      }
       // ---- list end: dV, dK, dk_idx accumulators (lane = key); warpgroup hf
       // takes dV/dK columns [64 hf, 64 hf + 64) and dk_idx columns [32 hf, 32 hf + 32)
       {
