@@ -361,17 +361,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = entry >= 0 ? (entry >> 8) - c * 128 : -1;  // last visible key column
         if (!mbar_wait(&sh.s_full[wg], (tj >> 1) & 1, a.err, 323)) { ok = false; break; }
         tc_fence_after();
-        // pass 1: row max over the visible keys
-        float m = -INFINITY;
+        // pass 1: row max over the visible keys (four independent chains;
+        // a warp whose rows all see the whole block skips the mask)
+        const bool full = __all_sync(0xffffffffu, lim >= 127);
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float x[32];
           tmem_ld32(tmem + lane_off + s_col + q * 32, x);
           tmem_wait_ld();
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (q * 32 + i <= lim) m = fmaxf(m, x[i]);
+            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (q * 32 + i <= lim) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+          }
         }
+        const float m = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         const float mm = (m == -INFINITY) ? 0.f : m * a.scale_log2;
         // Tile tj-2 (same warpgroup, same P buffer) is finished first: its O
         // is staged through P buffer wg, so it must leave before P(tj) goes in.
@@ -382,18 +390,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(&sh.p_free[wg], ((tj >> 1) & 1) ^ 1, a.err, 324)) { ok = false; break; }
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
-        // pass 2: P = exp2(s * scale * log2 e - max), row sum, bf16 image
-        float l = 0.f;
+        // pass 2: P = exp2(s * scale * log2 e - max), row sum, bf16 image.
+        // S is released to the tensor core right after its last TMEM load.
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float x[32];
           tmem_ld32(tmem + lane_off + s_col + q * 32, x);
           tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            x[i] = (q * 32 + i <= lim) ? fast_exp2(x[i] * a.scale_log2 - mm) : 0.f;
-            l += x[i];
+          if (q == 3) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.s_empty[wg]);
           }
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = fast_exp2(fmaf(x[i], a.scale_log2, -mm));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              x[i] = (q * 32 + i <= lim) ? fast_exp2(fmaf(x[i], a.scale_log2, -mm)) : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) l4[i & 3] += x[i];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             const int c16 = q * 4 + cc;
@@ -402,17 +421,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                            pack_bf16(x[8 * cc + 4], x[8 * cc + 5]), pack_bf16(x[8 * cc + 6], x[8 * cc + 7]));
           }
         }
-        tc_fence_before();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&sh.s_empty[wg]);
-          mbar_arrive(&sh.p_full[wg]);
-        }
+        if (lane == 0) mbar_arrive(&sh.p_full[wg]);
         pending = true;
         pu = tj;
         pm = mm;
-        pl = l;
+        pl = (l4[0] + l4[1]) + (l4[2] + l4[3]);
         pentry = entry;
         prow0 = (item.w + j * P) * HG;
       }
