@@ -318,11 +318,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&sh.o_full[wg], (pu >> 1) & 1, a.err, 321)) return false;
       tc_fence_after();
       const float inv = pentry >= 0 ? 1.f / pl : 0.f;
+      // each 64-column chunk leaves by its own TMA store (one bulk group
+      // each) as soon as it is staged; pass 2 of the next tile waits for
+      // each chunk's store separately
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float o[32];
         tmem_ld32(tmem + lane_off + o_col + q * 32, o);
         tmem_wait_ld();
+        if (q == 3) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.o_empty[wg]);
+        }
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           const int c16 = q * 4 + c;
@@ -330,18 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv), pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
               pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv), pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
         }
+        if (q & 1) {
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_o, pbuf + (q >> 1) * kChunk + quarter * 4096, (q >> 1) * 64, prow0 + quarter * 32);
+            bulk_commit();
+          }
+        }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.o_empty[wg]);
       if (pentry >= 0) a.lse_part[(size_t)prow0 + row] = (pm + __log2f(pl)) * kLn2;
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&map_o, pbuf + quarter * 4096, 0, prow0 + quarter * 32);
-        tma_store_2d(&map_o, pbuf + kChunk + quarter * 4096, 64, prow0 + quarter * 32);
-        bulk_commit();
-      }
       return true;
     };
     for (int it = 0; ok; ++it) {
@@ -385,11 +391,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // is staged through P buffer wg, so it must leave before P(tj) goes in.
         if (pending && !epilogue()) { ok = false; break; }
         pending = false;
-        // P buffer wg is free once the O MMA of tile tj-2 has read it and this
-        // warp's TMA store of tile tj-2's partial rows has read its staging
+        // P buffer wg is free once the O MMA of tile tj-2 has read it; each
+        // chunk of it once this warp's store of tile tj-2's rows has read it
         if (!mbar_wait(&sh.p_free[wg], ((tj >> 1) & 1) ^ 1, a.err, 324)) { ok = false; break; }
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
         // pass 2: P = exp2(s * scale * log2 e - max), row sum, bf16 image.
         // S is released to the tensor core right after its last TMEM load.
         float l4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -402,6 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.s_empty[wg]);
+          }
+          if (q == 0 || q == 2) {  // chunk q / 2 of the P buffer: its staged O rows have left
+            if (lane == 0) {
+              if (q == 0) bulk_wait_read_but_one();
+              else bulk_wait_read_all();
+            }
+            __syncwarp();
           }
           if (full) {
 #pragma unroll
