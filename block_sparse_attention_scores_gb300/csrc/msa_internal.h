@@ -40,7 +40,7 @@ struct WsLayout {
   size_t px_part = 0;       // fp32  [B,T,G,k]      index-branch partial LSE per slot
   size_t lse_px = 0;        // fp32  [B,T,G]        index-branch LSE over S(g,t)
   size_t dq_part = 0;       // bf16  [padded entries, hg, d] dQ partials, tile order
-  size_t dqi_part = 0;      // fp32  [padded entries, E]     dq_idx partials, tile order
+  size_t dqi_part = 0;      // bf16  [padded entries, E]     dq_idx partials, tile order
   size_t kl_part = 0;       // fp32  [B,T,G,k]      KL partials per slot
   size_t dki_part = 0;      // fp32  [B,G,T,E]      dk_idx per group
   size_t total = 256;

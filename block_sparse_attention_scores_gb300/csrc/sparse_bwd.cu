@@ -399,7 +399,7 @@ struct BwdArgs {
   float* dK;
   float* dV;
   __nv_bfloat16* dq_part;  // [padded entries, hg, d], tile order
-  float* dqi_part;         // [padded entries, E], tile order
+  __nv_bfloat16* dqi_part; // [padded entries, E], tile order
   float* kl_part;          // [B,T,G,k]
   float* dki_part;         // [B,G,T,E]
   int B, T, Hq, G, hg, n, k;
@@ -797,7 +797,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint8_t* gbuf = smem + oG + pgb * kGather;
         const int prow0 = p_pos0 * hg;  // first dQ partial row of the tile
         __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(gbuf + (hf * 4 + quarter) * 2048);
-        float* stq = reinterpret_cast<float*>(gbuf + kRowTile + (hf * 2 + (quarter & 1)) * 4096);
+        __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(gbuf + kRowTile + (hf * 2 + (quarter & 1)) * 4096);
         float dq[32];
         tmem_ld32(tmem + lane_off + cR0 + 64 * (p_tj & 1) + col0, dq);
         tmem_wait_ld();
@@ -808,7 +808,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tmem_ld_cols<kQ>(tmem + lane_off + cX + hf * kQ, dqi);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < kQ; ++i) stq[i * 32 + lane] = dqi[i];
+          for (int i = 0; i < kQ; ++i) stq[i * 32 + lane] = __float2bfloat16_rn(dqi[i]);
         }
         tc_fence_before();
         fence_proxy_async_smem();
@@ -1071,7 +1071,7 @@ __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&
 // dQ values and 2 dq_idx values.
 template <int HG>
 __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
-                                 const __nv_bfloat16* __restrict__ dq_part, const float* __restrict__ dqi_part,
+                                 const __nv_bfloat16* __restrict__ dq_part, const __nv_bfloat16* __restrict__ dqi_part,
                                  const float* __restrict__ kl_part, float* __restrict__ dQ,
                                  float* __restrict__ dq_idx, float* __restrict__ KL, int B, int T, int Hq, int G,
                                  int k, long long max_padded) {
@@ -1110,7 +1110,7 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
         load_bf16_row<kPer>(dq_part + (size_t)r * HG * 128 + lane * kPer, v);
 #pragma unroll
         for (int i = 0; i < kPer; ++i) acc[i] += v[i];
-        const float2 vi = *reinterpret_cast<const float2*>(dqi_part + (size_t)r * 64 + lane * 2);
+        const float2 vi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dqi_part + (size_t)r * 64 + lane * 2));
         a0 += vi.x;
         a1 += vi.y;
       }
@@ -1205,10 +1205,9 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if (!encode_tmap(&mdq, ws + L.dq_part, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const uint64_t dims2[2] = {64, (uint64_t)L.max_padded};
-    const uint64_t strides2[1] = {256};
+    const uint64_t strides2[1] = {128};
     const uint32_t box2[2] = {32, (uint32_t)(32 / p.hg)};  // 32 e x the queries of 32 rows
-    if (!encode_tmap(&mdqi, ws + L.dqi_part, 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+    if (!encode_tmap(&mdqi, ws + L.dqi_part, 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
   static bool attr = false;
@@ -1260,7 +1259,7 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.dK = static_cast<float*>(dK);
   ba.dV = static_cast<float*>(dV);
   ba.dq_part = reinterpret_cast<__nv_bfloat16*>(ws + L.dq_part);
-  ba.dqi_part = reinterpret_cast<float*>(ws + L.dqi_part);
+  ba.dqi_part = reinterpret_cast<__nv_bfloat16*>(ws + L.dqi_part);
   ba.kl_part = reinterpret_cast<float*>(ws + L.kl_part);
   ba.dki_part = reinterpret_cast<float*>(ws + L.dki_part);
   ba.B = p.B;
