@@ -782,6 +782,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool pend = false;
     uint32_t p_tj = 0;
     int p_pos0 = 0, p_b = 0, p_g = 0;
+    // Gather buffer whose staged partials are being stored: it goes back to
+    // the producers once the stores have read it, checked one stage later so
+    // the wait stays off the epilogue's path.
+    int rel_gb = -1;
+    auto release = [&]() {
+      if (rel_gb >= 0) {
+        if (lane == 0) {
+          bulk_wait_read_all();
+          mbar_arrive(&sh.g_empty[rel_gb]);
+        }
+        __syncwarp();
+        rel_gb = -1;
+      }
+    };
     // ---- phase-2 readout: dQ^T (lane = d), dq_idx^T (lane = e < 64)
     // Partials are in tile order: a tile's 64 (query, head) rows are
     // consecutive. Each warp stages its 32 x 32 slice row-major in the tile's
@@ -832,11 +846,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.kl_free);
       }
-      if (lane == 0) {
-        bulk_wait_read_all();
-        mbar_arrive(&sh.g_empty[pgb]);
-      }
-      __syncwarp();
+      rel_gb = pgb;
       return true;
     };
     for (int it = 0; ok; ++it) {
@@ -941,6 +951,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.ds_ready);
         }
+        release();  // the previous tile's gather buffer
         {  // stage C: index branch; X^T and gs^T have one column per query
           float xv[kQ];
           float term[kQ];
@@ -997,6 +1008,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!epi2()) { ok = false; break; }
         pend = false;
       }
+      release();
       // ---- list end: dV, dK, dk_idx accumulators (lane = key); warpgroup hf
       // takes dV/dK columns [64 hf, 64 hf + 64) and dk_idx columns [32 hf, 32 hf + 32)
       {
