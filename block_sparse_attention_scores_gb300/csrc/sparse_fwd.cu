@@ -484,18 +484,24 @@ __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&
 
 // One warp per (b, t, g): merge the k partials of each of the HG heads. The
 // partial of (b, g, t, slot) sits at padded entry rev[(b*G + g)*T + t][slot];
-// its HG head rows are one contiguous HG * 256-byte run. Lane s reads the HG
-// partial LSEs of slots s and s + 32 once; every lane then owns 4 * HG
-// consecutive output values (head lane / (32 / HG)).
+// its HG head rows are one contiguous HG * 256-byte run. Lane s owns slots s
+// and s + 32: it reads their partial LSEs, and once the row's LSEs are known
+// it writes their partial rows and merge weights e^{lse_s - LSE} to shared
+// memory; every lane then owns 4 * HG consecutive output values (head
+// lane / (32 / HG)) and sums the partial rows with one shared load per slot.
+constexpr int kMergeThreads = 256;
 template <int HG>
-__global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
-                                 const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
-                                 __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int B, int T, int Hq, int G,
-                                 int k, long long max_padded) {
+__global__ void __launch_bounds__(kMergeThreads)
+    fwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
+                     const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
+                     __nv_bfloat16* __restrict__ O, float* __restrict__ LSE, int B, int T, int Hq, int G, int k,
+                     long long max_padded) {
   constexpr int kPer = 4 * HG;  // output values per lane
   constexpr int kLanesPerHead = 32 / HG;
+  __shared__ int s_row[kMergeThreads / 32][64];
+  __shared__ float s_wgt[kMergeThreads / 32][64][HG];
   const long long rows = (long long)B * T * G;
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int my_head = lane / kLanesPerHead;
   for (long long w = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; w < rows;
        w += ((long long)gridDim.x * blockDim.x) >> 5) {
@@ -531,26 +537,29 @@ __global__ void fwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
       lse[h] = mx + logf(z);
     }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int sidx = lane + 32 * u;
+      if (sidx < k) {
+        s_row[wib][sidx] = rv_own[u];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) s_wgt[wib][sidx][h] = rv_own[u] >= 0 ? expf(l_own[u][h] - lse[h]) : 0.f;
+      }
+    }
+    __syncwarp();
     float acc[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+    for (int sidx = 0; sidx < k; ++sidx) {
+      const int r = s_row[wib][sidx];
+      if (r < 0) continue;
+      const float wgt = s_wgt[wib][sidx][my_head];
+      float v[kPer];
+      load_bf16_row<kPer>(o_part + (size_t)r * HG * 128 + lane * kPer, v);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      for (int src = 0; src < 32 && 32 * u + src < k; ++src) {
-        const int r = __shfl_sync(0xffffffffu, rv_own[u], src);
-        if (r < 0) continue;
-        float wgt = 0.f;
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float lh = __shfl_sync(0xffffffffu, l_own[u][h], src);
-          if (h == my_head) wgt = expf(lh - lse[h]);
-        }
-        float v[kPer];
-        load_bf16_row<kPer>(o_part + (size_t)r * HG * 128 + lane * kPer, v);
-#pragma unroll
-        for (int i = 0; i < kPer; ++i) acc[i] += wgt * v[i];
-      }
+      for (int i = 0; i < kPer; ++i) acc[i] = fmaf(wgt, v[i], acc[i]);
     }
+    __syncwarp();  // the next row rewrites this warp's slot table
     const size_t orow0 = ((size_t)b * T + t) * Hq + g * HG;
     uint2* dst = reinterpret_cast<uint2*>(O + orow0 * 128 + lane * kPer);
 #pragma unroll
@@ -636,10 +645,10 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
   const int32_t* rev = reinterpret_cast<const int32_t*>(ws + L.rev);
   __nv_bfloat16* Ob = static_cast<__nv_bfloat16*>(O);
   switch (p.hg) {
-    case 1: fwd_merge_kernel<1><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-    case 2: fwd_merge_kernel<2><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-    case 4: fwd_merge_kernel<4><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-    default: fwd_merge_kernel<8><<<grid, 256, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    case 1: fwd_merge_kernel<1><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    case 2: fwd_merge_kernel<2><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    case 4: fwd_merge_kernel<4><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    default: fwd_merge_kernel<8><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
   }
   return cudaGetLastError();
 }
