@@ -1,6 +1,6 @@
 """Parity of msa_bwd (CUDA) with the fp64 oracle, given identical block_idx.
 
-dQ, dK, dV, dq_idx, dk_idx (bf16) and KL (fp32): max |err| <= 2e-2 and cosine
+dQ, dK, dV, dq_idx, dk_idx and KL (all fp32 outputs): max |err| <= 2e-2 and cosine
 >= 0.999. The GPU backward consumes the GPU forward's O and LSE (inputs of the
 CUDA path); the oracle recomputes everything from Q, K, V, dO, q_idx, k_idx.
 Small shapes compare every element; larger workloads compare sampled queries
