@@ -332,6 +332,29 @@ def run_gpu(args, w):
     total_ms = dist_max(total_ms, dev)
     ms_step = total_ms / args.steps
 
+    # ---- IndexShare: a layer that reuses an earlier layer's selection and
+    # block map (built once, outside the timed region) runs only the mapped
+    # forward and backward
+    msa.msa_block_map(s, bi, ws, stream)
+    for _ in range(2):
+        msa.msa_sparse_fwd_mapped(s, d_in["Q"], d_in["K"], d_in["V"], bi, O, LSE, ws, stream)
+        msa.msa_bwd_mapped(s, d_in["Q"], d_in["K"], d_in["V"], O, d_in["dO"], LSE, d_in["q_idx"], d_in["k_idx"], bi,
+                           1.0, out["dQ"], out["dK"], out["dV"], out["dq_idx"], out["dk_idx"], out["KL"], ws, stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(args.steps):
+        msa.msa_sparse_fwd_mapped(s, d_in["Q"], d_in["K"], d_in["V"], bi, O, LSE, ws, stream)
+        msa.msa_bwd_mapped(s, d_in["Q"], d_in["K"], d_in["V"], O, d_in["dO"], LSE, d_in["q_idx"], d_in["k_idx"], bi,
+                           1.0, out["dQ"], out["dK"], out["dV"], out["dq_idx"], out["dk_idx"], out["KL"], ws, stream)
+    g1.record(stream)
+    torch.cuda.synchronize()
+    share_ms = dist_max(g0.elapsed_time(g1) / args.steps, dev)
+    msa.msa_check_device_status(ws, stream)
+
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).
     # Every step copies its inputs host->device from pinned memory and its
     # outputs (gradients, KL, O) device->host. The copies run on their own
@@ -424,6 +447,10 @@ def run_gpu(args, w):
                             "move while step i computes"},
             "clocks": clk,
             "gpu_launches": launches,
+            "index_share": {"ms_per_layer": share_ms, "tokens_per_s": aggregate_tokens_per_s(w, world, share_ms),
+                            "tflops": (fl["fwd"] + fl["bwd"]) / (share_ms * 1e-3) / 1e12,
+                            "note": "a layer reusing an earlier layer's block_idx and block map "
+                                    "(msa_block_map once): msa_sparse_fwd_mapped + msa_bwd_mapped"},
         }
         if world == 1 and not args.no_cpu_baseline:
             v, desc, cores = oracle_sample(w, args.cpu_seconds)

@@ -32,7 +32,7 @@ MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD = 0, 1, 2
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
             "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version",
-            "msa_index_topk_noalloc")
+            "msa_index_topk_noalloc", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped")
 
 
 class MsaError(RuntimeError):
@@ -82,7 +82,11 @@ def load_library():
     lib.msa_index_topk.argtypes = [S, P, P, P, P, ctypes.c_size_t, P]
     lib.msa_sparse_fwd.argtypes = [S, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     lib.msa_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, P, P, ctypes.c_size_t, P]
-    for f in (lib.msa_index_topk, lib.msa_sparse_fwd, lib.msa_bwd):
+    lib.msa_sparse_fwd_mapped.argtypes = lib.msa_sparse_fwd.argtypes
+    lib.msa_bwd_mapped.argtypes = lib.msa_bwd.argtypes
+    lib.msa_block_map.argtypes = [S, P, P, ctypes.c_size_t, P]
+    for f in (lib.msa_index_topk, lib.msa_sparse_fwd, lib.msa_bwd, lib.msa_sparse_fwd_mapped, lib.msa_bwd_mapped,
+              lib.msa_block_map):
         f.restype = ctypes.c_int
     lib.msa_last_error.argtypes = []
     lib.msa_last_error.restype = ctypes.c_char_p
@@ -164,6 +168,20 @@ def msa_sparse_fwd(shape, Q, K, V, block_idx, O, LSE, workspace, stream=None, wo
                                          _ptr(O), _ptr(LSE), _ptr(workspace), wb, _stream(stream)))
 
 
+def msa_block_map(shape, block_idx, workspace, stream=None, workspace_bytes=None) -> None:
+    """Build the shared block map of block_idx in a MSA_WS_BWD-sized workspace (IndexShare)."""
+    wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
+    _check(load_library().msa_block_map(ctypes.byref(_shape(shape)), _ptr(block_idx), _ptr(workspace), wb,
+                                        _stream(stream)))
+
+
+def msa_sparse_fwd_mapped(shape, Q, K, V, block_idx, O, LSE, workspace, stream=None, workspace_bytes=None) -> None:
+    wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
+    _check(load_library().msa_sparse_fwd_mapped(ctypes.byref(_shape(shape)), _ptr(Q), _ptr(K), _ptr(V),
+                                                _ptr(block_idx), _ptr(O), _ptr(LSE), _ptr(workspace), wb,
+                                                _stream(stream)))
+
+
 def msa_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, dK, dV, dq_idx, dk_idx, KL,
             workspace, stream=None, workspace_bytes=None) -> None:
     wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
@@ -171,6 +189,15 @@ def msa_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, 
                                   _ptr(LSE), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), float(kl_weight), _ptr(dQ),
                                   _ptr(dK), _ptr(dV), _ptr(dq_idx), _ptr(dk_idx), _ptr(KL), _ptr(workspace), wb,
                                   _stream(stream)))
+
+
+def msa_bwd_mapped(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, dK, dV, dq_idx, dk_idx, KL,
+                   workspace, stream=None, workspace_bytes=None) -> None:
+    wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
+    _check(load_library().msa_bwd_mapped(ctypes.byref(_shape(shape)), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),
+                                         _ptr(LSE), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx), float(kl_weight),
+                                         _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(dq_idx), _ptr(dk_idx), _ptr(KL),
+                                         _ptr(workspace), wb, _stream(stream)))
 
 
 def msa_selftest_wait_timeout(workspace, limit_us: int, stream=None) -> None:

@@ -100,6 +100,7 @@ WsLayout ws_layout(const Prob& p, int which) {
     L.max_items = max_work_items(p, 1, 16);
     L.items = take((size_t)L.max_items * 16);
     L.n_items = take(16);
+    if (which == MSA_WS_BWD) L.items2 = take((size_t)L.max_items * 16);
   }
   if (which == MSA_WS_FWD) {
     L.o_part = take((size_t)L.max_padded * p.hg * p.d * 2);
@@ -193,7 +194,7 @@ using namespace msa;
 
 extern "C" {
 
-int32_t msa_version(void) { return (1 << 16) | 0; }
+int32_t msa_version(void) { return (1 << 16) | 1; }
 
 int64_t msa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -223,9 +224,9 @@ msa_status msa_index_topk(const msa_shape* shape, const void* q_idx, const void*
   return cuda_status(launch_index_topk(p, q_idx, k_idx, block_idx, workspace, L, st), "index top-k launch");
 }
 
-msa_status msa_sparse_fwd(const msa_shape* shape, const void* Q, const void* K, const void* V,
-                          const int32_t* block_idx, void* O, float* LSE, void* workspace, size_t workspace_bytes,
-                          msa_stream_t stream) {
+static msa_status sparse_fwd_impl(const msa_shape* shape, const void* Q, const void* K, const void* V,
+                                  const int32_t* block_idx, void* O, float* LSE, void* workspace,
+                                  size_t workspace_bytes, msa_stream_t stream, bool mapped) {
   Prob p;
   WsLayout L;
   msa_status s;
@@ -236,18 +237,32 @@ msa_status msa_sparse_fwd(const msa_shape* shape, const void* Q, const void* K, 
   if ((s = check_ptr(block_idx, "block_idx", 4)) != MSA_OK) return s;
   if ((s = check_ptr(O, "O", 16)) != MSA_OK) return s;
   if ((s = check_ptr(LSE, "LSE", 4)) != MSA_OK) return s;
-  if ((s = check_ws(p, MSA_WS_FWD, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  // a shared map lives in a backward-sized workspace (it holds both item lists)
+  if ((s = check_ws(p, mapped ? MSA_WS_BWD : MSA_WS_FWD, workspace, workspace_bytes, &L)) != MSA_OK) return s;
   if ((s = check_device()) != MSA_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(workspace);
   if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
-  return cuda_status(launch_sparse_fwd(p, Q, K, V, block_idx, O, LSE, w, L, st), "sparse forward launch");
+  return cuda_status(launch_sparse_fwd(p, Q, K, V, block_idx, O, LSE, w, L, st, mapped), "sparse forward launch");
 }
 
-msa_status msa_bwd(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
-                   const void* dO, const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
-                   float kl_weight, float* dQ, float* dK, float* dV, float* dq_idx, float* dk_idx, float* KL,
-                   void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+msa_status msa_sparse_fwd(const msa_shape* shape, const void* Q, const void* K, const void* V,
+                          const int32_t* block_idx, void* O, float* LSE, void* workspace, size_t workspace_bytes,
+                          msa_stream_t stream) {
+  return sparse_fwd_impl(shape, Q, K, V, block_idx, O, LSE, workspace, workspace_bytes, stream, false);
+}
+
+msa_status msa_sparse_fwd_mapped(const msa_shape* shape, const void* Q, const void* K, const void* V,
+                                 const int32_t* block_idx, void* O, float* LSE, void* workspace,
+                                 size_t workspace_bytes, msa_stream_t stream) {
+  return sparse_fwd_impl(shape, Q, K, V, block_idx, O, LSE, workspace, workspace_bytes, stream, true);
+}
+
+static msa_status bwd_impl(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
+                           const void* dO, const float* LSE, const void* q_idx, const void* k_idx,
+                           const int32_t* block_idx, float kl_weight, float* dQ, float* dK, float* dV, float* dq_idx,
+                           float* dk_idx, float* KL, void* workspace, size_t workspace_bytes, msa_stream_t stream,
+                           bool mapped) {
   Prob p;
   WsLayout L;
   msa_status s;
@@ -266,8 +281,42 @@ msa_status msa_bwd(const msa_shape* shape, const void* Q, const void* K, const v
   uint8_t* w = static_cast<uint8_t*>(workspace);
   if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
   return cuda_status(launch_bwd(p, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, dK, dV, dq_idx,
-                                dk_idx, KL, w, L, st),
+                                dk_idx, KL, w, L, st, mapped),
                      "backward launch");
+}
+
+msa_status msa_bwd(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
+                   const void* dO, const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
+                   float kl_weight, float* dQ, float* dK, float* dV, float* dq_idx, float* dk_idx, float* KL,
+                   void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return bwd_impl(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, dK, dV, dq_idx, dk_idx, KL,
+                  workspace, workspace_bytes, stream, false);
+}
+
+msa_status msa_bwd_mapped(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
+                          const void* dO, const float* LSE, const void* q_idx, const void* k_idx,
+                          const int32_t* block_idx, float kl_weight, float* dQ, float* dK, float* dV, float* dq_idx,
+                          float* dk_idx, float* KL, void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  return bwd_impl(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, dQ, dK, dV, dq_idx, dk_idx, KL,
+                  workspace, workspace_bytes, stream, true);
+}
+
+msa_status msa_block_map(const msa_shape* shape, const int32_t* block_idx, void* workspace, size_t workspace_bytes,
+                         msa_stream_t stream) {
+  Prob p;
+  WsLayout L;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_ptr(block_idx, "block_idx", 4)) != MSA_OK) return s;
+  if ((s = check_ws(p, MSA_WS_BWD, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  // lists padded to whole forward tiles (a multiple of the backward tile)
+  const int fq = fwd_tile_queries(p);
+  return cuda_status(build_block_map2(p, block_idx, w, L, fq, (long long)fq * kFwdTilesPerItem, 1LL << 30, true, st),
+                     "block map launch");
 }
 
 msa_status msa_selftest_wait_timeout(void* workspace, int32_t limit_us, msa_stream_t stream) {

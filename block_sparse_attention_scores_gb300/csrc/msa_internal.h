@@ -33,6 +33,7 @@ struct WsLayout {
   size_t rev = 0;           // int32 [B*G*T*k] padded entry index of (b, g, t, slot)
   size_t entries = 0;       // int32 [B*G*T*k] (t << 8 | slot), grouped by list
   size_t items = 0;         // int4  [max_items] work items (list, tile range)
+  size_t items2 = 0;        // int4  [max_items] the backward's items of a shared map (msa_block_map)
   size_t n_items = 0;       // int32 [4]       number of work items per kernel
   size_t o_part = 0;        // bf16  [padded entries, hg, d] forward partial outputs (normalised), tile order
   size_t lse_part = 0;      // fp32  [padded entries, hg]    forward partial log-sum-exp
@@ -72,13 +73,28 @@ cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_id
 cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L,
                             int rows_per_tile, int tiles_per_item, cudaStream_t st);
 
-cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
-                              void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st);
+// The same map with lists padded to pad_rows entries and two item lists: the
+// forward's in `items` (n_items[0]) and, when two_lists, the backward's in
+// `items2` (n_items[1]), so both kernels can run on it without rebuilding it.
+cudaError_t build_block_map2(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L, int pad_rows,
+                             long long per_item_a, long long per_item_b, bool two_lists, cudaStream_t st);
 
+// Queries per forward tile / per backward tile, and the forward's tiles per item.
+inline int fwd_tile_queries(const Prob& p) { return 128 / p.hg; }
+inline int bwd_tile_queries(const Prob& p) { return 64 / p.hg; }
+constexpr int kFwdTilesPerItem = 32;
+
+// mapped: use the map (and the forward's items) that build_block_map2 left
+// in the workspace instead of building one.
+cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
+                              void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st,
+                              bool mapped = false);
+
+// mapped: use the map and the backward's items (items2) left by build_block_map2.
 cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                        const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
                        float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
-                       uint8_t* ws, const WsLayout& L, cudaStream_t st);
+                       uint8_t* ws, const WsLayout& L, cudaStream_t st, bool mapped = false);
 
 cudaError_t launch_selftest_wait_timeout(int* err, long long limit_ns, cudaStream_t st);
 

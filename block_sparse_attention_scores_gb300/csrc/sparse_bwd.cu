@@ -1160,10 +1160,10 @@ __global__ void dki_merge_kernel(const float* __restrict__ dki_part, float* __re
 cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                        const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
                        float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
-                       uint8_t* ws, const WsLayout& L, cudaStream_t st) {
-  const int npos = 64 / p.hg;  // queries per backward tile (64 (query, head) rows)
-  cudaError_t e = build_block_map(p, block_idx, ws, L, npos, (1 << 30) / npos, st);
-  if (e != cudaSuccess) return e;
+                       uint8_t* ws, const WsLayout& L, cudaStream_t st, bool mapped) {
+  const int npos = bwd_tile_queries(p);  // queries per backward tile (64 (query, head) rows)
+  cudaError_t e;
+  if (!mapped && (e = build_block_map(p, block_idx, ws, L, npos, (1 << 30) / npos, st)) != cudaSuccess) return e;
   int* err = reinterpret_cast<int*>(ws + L.err);
   int* counters = reinterpret_cast<int*>(ws + L.counters);
   float* drow = reinterpret_cast<float*>(ws + L.drow);
@@ -1241,8 +1241,9 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   PxArgs pa;
   pa.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
   pa.entries = reinterpret_cast<const int32_t*>(ws + L.entries);
-  pa.items = reinterpret_cast<const int4*>(ws + L.items);
-  pa.n_items = reinterpret_cast<const int*>(ws + L.n_items);
+  // a shared map keeps the backward's items (whole lists) in items2 / n_items[1]
+  pa.items = reinterpret_cast<const int4*>(ws + (mapped ? L.items2 : L.items));
+  pa.n_items = reinterpret_cast<const int*>(ws + L.n_items) + (mapped ? 1 : 0);
   pa.counter = counters + 2;
   pa.err = err;
   pa.px_part = px_part;

@@ -578,10 +578,11 @@ __global__ void __launch_bounds__(kMergeThreads)
 }  // namespace
 
 cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const void* V, const int32_t* block_idx,
-                              void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st) {
-  const int pos_per_tile = 128 / p.hg;
-  cudaError_t e = build_block_map(p, block_idx, ws, L, pos_per_tile, 32, st);
-  if (e != cudaSuccess) return e;
+                              void* O, float* LSE, uint8_t* ws, const WsLayout& L, cudaStream_t st, bool mapped) {
+  const int pos_per_tile = fwd_tile_queries(p);
+  cudaError_t e;
+  if (!mapped && (e = build_block_map(p, block_idx, ws, L, pos_per_tile, kFwdTilesPerItem, st)) != cudaSuccess)
+    return e;
   CUtensorMap mk, mv;
   const uint64_t dims[3] = {(uint64_t)p.d, (uint64_t)p.G, (uint64_t)p.BT()};
   const uint64_t strides[2] = {(uint64_t)p.d * 2, (uint64_t)p.G * p.d * 2};

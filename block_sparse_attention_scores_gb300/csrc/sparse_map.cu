@@ -145,38 +145,16 @@ __device__ __forceinline__ int block_scan_excl(int v, int* warp_sums, int* carry
   return excl;
 }
 
-// Single CTA. Exclusive scans of list lengths (entry offsets) and of list
-// lengths padded to whole tiles (partial-output row offsets), both in list
-// order; then of work items in block-id-major order, and the items:
-// int4 {list, first entry, entries, padded offset of the first entry}.
-__global__ void __launch_bounds__(1024) map_scan_kernel(const int* __restrict__ count, int L, int BG, int n,
-                                                        int rows_per_tile, int tiles_per_item,
-                                                        int* __restrict__ off, int* __restrict__ poff,
-                                                        int4* __restrict__ items, int max_items,
-                                                        int* __restrict__ n_items, int* err) {
-  __shared__ int warp_sums[32];
-  __shared__ int carry, pcarry;
+// Work items of one kernel, in block-id-major order (the order of decreasing
+// expected list length): int4 {list, first entry, entries, padded offset of
+// the first entry}, at most per_item entries each. Called by one CTA of 1024
+// threads; `carry` is block-uniform scratch.
+__device__ void emit_items(const int* __restrict__ count, const int* __restrict__ off,
+                           const int* __restrict__ poff, int L, int BG, int n, int per_item,
+                           int4* __restrict__ items, int max_items, int* __restrict__ n_items, int* err,
+                           int* warp_sums, int* carry) {
   const int tid = threadIdx.x;
-  const long long per_item_ll = (long long)rows_per_tile * tiles_per_item;
-  const int per_item = per_item_ll > (1 << 30) ? (1 << 30) : (int)per_item_ll;
-  if (tid == 0) carry = pcarry = 0;
-  __syncthreads();
-  for (int base = 0; base < L; base += 1024) {
-    const int i = base + tid;
-    const int v = i < L ? count[i] : 0;
-    const int pv = (v + rows_per_tile - 1) / rows_per_tile * rows_per_tile;
-    const int e = block_scan_excl(v, warp_sums, &carry);
-    const int pe = block_scan_excl(pv, warp_sums, &pcarry);
-    if (i < L) {
-      off[i] = e;
-      poff[i] = pe;
-    }
-  }
-  if (tid == 0) {
-    off[L] = carry;
-    poff[L] = pcarry;
-    carry = 0;
-  }
+  if (tid == 0) *carry = 0;
   __syncthreads();
   for (int base = 0; base < L; base += 1024) {
     const int j = base + tid;  // block-id-major index
@@ -186,7 +164,7 @@ __global__ void __launch_bounds__(1024) map_scan_kernel(const int* __restrict__ 
       lid = bg * n + c;
       v = (count[lid] + per_item - 1) / per_item;
     }
-    const int first = block_scan_excl(v, warp_sums, &carry);
+    const int first = block_scan_excl(v, warp_sums, carry);
     if (j < L) {
       const int len = count[lid], start = off[lid], pstart = poff[lid];
       for (int q = 0; q < v; ++q) {
@@ -200,7 +178,44 @@ __global__ void __launch_bounds__(1024) map_scan_kernel(const int* __restrict__ 
       }
     }
   }
-  if (tid == 0) *n_items = min(carry, max_items);
+  if (tid == 0) *n_items = min(*carry, max_items);
+  __syncthreads();
+}
+
+// Single CTA. Exclusive scans of list lengths (entry offsets) and of list
+// lengths padded to whole tiles of pad_rows entries (partial-output row
+// offsets), both in list order; then the work items of one kernel, and of a
+// second one when items_b is given (a map shared by the forward and the
+// backward).
+__global__ void __launch_bounds__(1024) map_scan_kernel(const int* __restrict__ count, int L, int BG, int n,
+                                                        int pad_rows, int per_item_a, int per_item_b,
+                                                        int* __restrict__ off, int* __restrict__ poff,
+                                                        int4* __restrict__ items_a, int4* __restrict__ items_b,
+                                                        int max_items, int* __restrict__ n_items, int* err) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry, pcarry;
+  const int tid = threadIdx.x;
+  if (tid == 0) carry = pcarry = 0;
+  __syncthreads();
+  for (int base = 0; base < L; base += 1024) {
+    const int i = base + tid;
+    const int v = i < L ? count[i] : 0;
+    const int pv = (v + pad_rows - 1) / pad_rows * pad_rows;
+    const int e = block_scan_excl(v, warp_sums, &carry);
+    const int pe = block_scan_excl(pv, warp_sums, &pcarry);
+    if (i < L) {
+      off[i] = e;
+      poff[i] = pe;
+    }
+  }
+  if (tid == 0) {
+    off[L] = carry;
+    poff[L] = pcarry;
+  }
+  __syncthreads();
+  emit_items(count, off, poff, L, BG, n, per_item_a, items_a, max_items, n_items, err, warp_sums, &carry);
+  if (items_b) emit_items(count, off, poff, L, BG, n, per_item_b, items_b, max_items, n_items + 1, err, warp_sums,
+                          &carry);
 }
 
 // One CTA (128 threads = rows) per (b, g, qb): entries in query order and
@@ -237,6 +252,11 @@ __global__ void __launch_bounds__(128) map_chunk_scatter_kernel(const int32_t* _
 
 cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L,
                             int rows_per_tile, int tiles_per_item, cudaStream_t st) {
+  return build_block_map2(p, block_idx, ws, L, rows_per_tile, rows_per_tile * tiles_per_item, 0, false, st);
+}
+
+cudaError_t build_block_map2(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L, int pad_rows,
+                             long long per_item_a, long long per_item_b, bool two_lists, cudaStream_t st) {
   const int lists = p.B * p.G * p.n;
   int* count = reinterpret_cast<int*>(ws + L.list_count);
   int* off = reinterpret_cast<int*>(ws + L.list_off);
@@ -264,8 +284,10 @@ cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws
   map_chunk_count_kernel<<<chunks, 128, mask_bytes, st>>>(block_idx, p.T, p.n, p.k, chunk, err);
   map_chunk_scan_kernel<<<(int)std::min<long long>(((long long)lists * 32 + 255) / 256, 16LL * num_sms()), 256, 0,
                           st>>>(lists, p.n, chunk, count);
-  map_scan_kernel<<<1, 1024, 0, st>>>(count, lists, p.B * p.G, p.n, rows_per_tile, tiles_per_item, off, poff,
-                                      items, L.max_items, n_items, err);
+  auto clamp = [](long long v) { return v > (1 << 30) ? (1 << 30) : (int)v; };
+  int4* items_b = two_lists ? reinterpret_cast<int4*>(ws + L.items2) : nullptr;
+  map_scan_kernel<<<1, 1024, 0, st>>>(count, lists, p.B * p.G, p.n, pad_rows, clamp(per_item_a), clamp(per_item_b),
+                                      off, poff, items, items_b, L.max_items, n_items, err);
   map_chunk_scatter_kernel<<<chunks, 128, mask_bytes, st>>>(block_idx, p.T, p.n, p.k, chunk, off, poff, entries,
                                                              rev, err);
   count_launches(4);

@@ -196,6 +196,31 @@ MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K,
 MSA_API msa_status msa_index_topk_noalloc(const msa_shape *shape, const void *q_idx, const void *k_idx,
                                           int32_t *block_idx, int32_t check, msa_stream_t stream);
 
+/* IndexShare: one selection shared by several layers (dothoosh.com "how
+ * Flash-MSA cuts million-token training cost", "Current limits and future
+ * scaling": sharing the proxy (index) heads across layers, so later layers
+ * reuse an earlier layer's block indices). msa_block_map
+ * builds the inverted block -> query map of `block_idx` once, into a
+ * MSA_WS_BWD-sized `workspace`, with the work items of both the forward and
+ * the backward; msa_sparse_fwd_mapped and msa_bwd_mapped then run on that map
+ * instead of building their own (same arguments, results and errors as
+ * msa_sparse_fwd and msa_bwd). The map stays valid for as long as `block_idx`
+ * and the workspace's map region are unchanged: msa_index_topk,
+ * msa_sparse_fwd and msa_bwd on the same workspace overwrite it, the mapped
+ * calls do not. The caller guarantees that the `block_idx` passed to the
+ * mapped calls is the one the map was built from; rows that fail validation
+ * are reported by msa_block_map (device error word). */
+MSA_API msa_status msa_block_map(const msa_shape *shape, const int32_t *block_idx, void *workspace,
+                                 size_t workspace_bytes, msa_stream_t stream);
+MSA_API msa_status msa_sparse_fwd_mapped(const msa_shape *shape, const void *Q, const void *K, const void *V,
+                                         const int32_t *block_idx, void *O, float *LSE, void *workspace,
+                                         size_t workspace_bytes, msa_stream_t stream);
+MSA_API msa_status msa_bwd_mapped(const msa_shape *shape, const void *Q, const void *K, const void *V,
+                                  const void *O, const void *dO, const float *LSE, const void *q_idx,
+                                  const void *k_idx, const int32_t *block_idx, float kl_weight, float *dQ, float *dK,
+                                  float *dV, float *dq_idx, float *dk_idx, float *KL, void *workspace,
+                                  size_t workspace_bytes, msa_stream_t stream);
+
 /* Message describing the last non-OK status returned on this thread. */
 MSA_API const char *msa_last_error(void);
 
