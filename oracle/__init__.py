@@ -55,6 +55,9 @@ def _load():
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         lib.oracle_index_topk.argtypes = [ctypes.POINTER(OShape), P, P, ctypes.c_int, P, I64, P, P, P]
+        lib.oracle_e4m3.argtypes = [ctypes.c_double]
+        lib.oracle_e4m3.restype = ctypes.c_double
+        lib.oracle_quantize_fp8.argtypes = [ctypes.POINTER(OShape), P, P, P, P, P, P]
         lib.oracle_sparse_fwd.argtypes = [ctypes.POINTER(OShape), P, P, P, ctypes.c_int, P, P, I64, P, P]
         lib.oracle_bwd_rows.argtypes = [ctypes.POINTER(OShape), P, P, P, P, P, P, ctypes.c_int, P, P, I64,
                                         P, P, P]
@@ -135,6 +138,35 @@ def index_topk(s: OShape, q_idx, k_idx, rows=None, want_pool=False):
     lib.oracle_index_topk(ctypes.byref(s), qp, kp, dt, rp, n, bi.ctypes.data, gap.ctypes.data,
                           pool.ctypes.data if pool is not None else None)
     return bi, gap, pool
+
+
+def e4m3(x):
+    """E4M3 (FN) rounding, ties to even, saturating at +-448, of each value of x (float64 array)."""
+    lib = _load()
+    x = np.asarray(x, dtype=np.float64)
+    return np.array([lib.oracle_e4m3(float(v)) for v in x.ravel()], dtype=np.float64).reshape(x.shape)
+
+
+def quantize_fp8(s: OShape, q_idx, k_idx):
+    """FP8 index inputs: (q_deq [B,T,G,E], k_deq [B,T,E] float64 = quantized values times their scales,
+    sq [B,T,G] float32, sk [B,n_blocks] float32). q_idx, k_idx are bf16 bit patterns (uint16)."""
+    lib = _load()
+    q = np.ascontiguousarray(q_idx, dtype=np.uint16)
+    k = np.ascontiguousarray(k_idx, dtype=np.uint16)
+    nb = (s.T + s.Bk - 1) // s.Bk
+    q_deq = np.empty((s.B, s.T, s.G, s.d_idx), dtype=np.float64)
+    k_deq = np.empty((s.B, s.T, s.d_idx), dtype=np.float64)
+    sq = np.empty((s.B, s.T, s.G), dtype=np.float32)
+    sk = np.empty((s.B, nb), dtype=np.float32)
+    lib.oracle_quantize_fp8(ctypes.byref(s), q.ctypes.data, k.ctypes.data, q_deq.ctypes.data, k_deq.ctypes.data,
+                            sq.ctypes.data, sk.ctypes.data)
+    return q_deq, k_deq, sq, sk
+
+
+def index_topk_fp8(s: OShape, q_idx, k_idx, rows=None, want_pool=False):
+    """Steps 1-3 on the FP8 index inputs (quantize_fp8): same returns as index_topk."""
+    q_deq, k_deq, _, _ = quantize_fp8(s, q_idx, k_idx)
+    return index_topk(s, q_deq, k_deq, rows=rows, want_pool=want_pool)
 
 
 def sparse_fwd(s: OShape, Q, K, V, block_idx, rows=None):

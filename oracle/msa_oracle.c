@@ -144,6 +144,97 @@ int oracle_index_topk(const oshape *s, const void *q_idx, const void *k_idx, int
     return 0;
 }
 
+/* ---------------------------------------------------------------- FP8 index inputs */
+/*
+ * Low-precision indexer (dothoosh.com "how Flash-MSA cuts million-token
+ * training cost", "Current limits and future scaling": training the indexer
+ * in low precision, as at inference). Steps 1-3 run on FP8 (E4M3) copies of
+ * the index queries and keys. The pages fix no format details; the reading
+ * taken here:
+ *   - E4M3 "FN" values (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ *     bits, subnormals, no infinities, largest finite 448), rounding to
+ *     nearest with ties to even, saturating at +-448;
+ *   - one scale per q_idx row (b, t, g) and one per 128-key block of k_idx
+ *     (b, c): amax = max |x| (fp32), x is multiplied by 448 / amax (fp32
+ *     division, then fp32 multiply) and rounded to E4M3; the scale is
+ *     amax / 448 (fp32), 1 when amax = 0;
+ *   - scores s = scale_idx * (q8 * sq) . (k8 * sk): the quantized values
+ *     times their scales, exactly, in double.
+ */
+double oracle_e4m3(double x) {
+    if (isnan(x)) return x;
+    const double a = fabs(x);
+    if (a >= 448.0) return copysign(448.0, x);
+    if (a == 0.0) return x;
+    int e;
+    frexp(a, &e);                  /* a = m 2^e, m in [1/2, 1): leading bit 2^(e-1) */
+    int lead = e - 1;
+    if (lead < -6) lead = -6;      /* subnormals: spacing 2^-9 */
+    const double ulp = ldexp(1.0, lead - 3);
+    const double y = nearbyint(a / ulp) * ulp;  /* round to nearest, ties to even */
+    return copysign(y, x);
+}
+
+/* amax (fp32) -> (multiplier 448 / amax, scale amax / 448), both fp32 */
+static void fp8_scales(float amax, float *mul, float *scale) {
+    if (amax > 0.0f) {
+        *mul = 448.0f / amax;
+        *scale = amax / 448.0f;
+    } else {
+        *mul = 1.0f;
+        *scale = 1.0f;
+    }
+}
+
+static inline float ldf_bf16(const void *p, size_t i) {
+    uint32_t u = (uint32_t)((const uint16_t *)p)[i] << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * q_idx [B,T,G,E], k_idx [B,T,E] as bf16 bits. Writes the dequantized values
+ * q8 * sq -> q_deq [B,T,G,E] and k8 * sk -> k_deq [B,T,E] (doubles), and the
+ * scales sq [B,T,G], sk [B, n_blocks] (fp32).
+ */
+int oracle_quantize_fp8(const oshape *s, const void *q_idx, const void *k_idx, double *q_deq, double *k_deq,
+                        float *sq, float *sk) {
+    const int B = s->B, T = s->T, G = s->G, E = s->d_idx, Bk = s->Bk;
+    const int nb = (T + Bk - 1) / Bk;
+    const int64_t qrows = (int64_t)B * T * G;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < qrows; r++) {
+        float amax = 0.0f;
+        for (int e = 0; e < E; e++) amax = fmaxf(amax, fabsf(ldf_bf16(q_idx, (size_t)r * E + e)));
+        float mul, scale;
+        fp8_scales(amax, &mul, &scale);
+        sq[r] = scale;
+        for (int e = 0; e < E; e++) {
+            const float v = ldf_bf16(q_idx, (size_t)r * E + e) * mul;
+            q_deq[(size_t)r * E + e] = oracle_e4m3((double)v) * (double)scale;
+        }
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t bc = 0; bc < (int64_t)B * nb; bc++) {
+        const int b = (int)(bc / nb), c = (int)(bc % nb);
+        const int j0 = c * Bk, j1 = imin((c + 1) * Bk, T);
+        float amax = 0.0f;
+        for (int j = j0; j < j1; j++)
+            for (int e = 0; e < E; e++) amax = fmaxf(amax, fabsf(ldf_bf16(k_idx, ((size_t)b * T + j) * E + e)));
+        float mul, scale;
+        fp8_scales(amax, &mul, &scale);
+        sk[bc] = scale;
+        for (int j = j0; j < j1; j++)
+            for (int e = 0; e < E; e++) {
+                const size_t i = ((size_t)b * T + j) * E + e;
+                const float v = ldf_bf16(k_idx, i) * mul;
+                k_deq[i] = oracle_e4m3((double)v) * (double)scale;
+            }
+    }
+    return 0;
+}
+
 /* ---------------------------------------------------------------- step 4 */
 /* Selected, causally visible tokens of (b,g,t), ascending; duplicates in the
  * block list count once. Returns |S|. tok must hold k*Bk entries. */
