@@ -28,11 +28,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmsa_gb300.so")
 
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUDA, MSA_ERR_DEVICE = range(6)
-MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD = 0, 1, 2
+MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD, MSA_WS_TOPK_FP8 = 0, 1, 2, 3
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
             "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version",
-            "msa_index_topk_noalloc", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped")
+            "msa_index_topk_noalloc", "msa_index_topk_fp8", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped")
 
 
 class MsaError(RuntimeError):
@@ -82,6 +82,8 @@ def load_library():
     lib.msa_index_topk.argtypes = [S, P, P, P, P, ctypes.c_size_t, P]
     lib.msa_sparse_fwd.argtypes = [S, P, P, P, P, P, P, P, ctypes.c_size_t, P]
     lib.msa_bwd.argtypes = [S, P, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.msa_index_topk_fp8.argtypes = lib.msa_index_topk.argtypes
+    lib.msa_index_topk_fp8.restype = ctypes.c_int
     lib.msa_sparse_fwd_mapped.argtypes = lib.msa_sparse_fwd.argtypes
     lib.msa_bwd_mapped.argtypes = lib.msa_bwd.argtypes
     lib.msa_block_map.argtypes = [S, P, P, ctypes.c_size_t, P]
@@ -154,6 +156,13 @@ def msa_index_topk(shape, q_idx, k_idx, block_idx, workspace, stream=None, works
     wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
     _check(load_library().msa_index_topk(ctypes.byref(_shape(shape)), _ptr(q_idx), _ptr(k_idx), _ptr(block_idx),
                                          _ptr(workspace), wb, _stream(stream)))
+
+
+def msa_index_topk_fp8(shape, q_idx, k_idx, block_idx, workspace, stream=None, workspace_bytes=None) -> None:
+    """msa_index_topk on E4M3 copies of q_idx and k_idx (workspace sized with MSA_WS_TOPK_FP8)."""
+    wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
+    _check(load_library().msa_index_topk_fp8(ctypes.byref(_shape(shape)), _ptr(q_idx), _ptr(k_idx),
+                                             _ptr(block_idx), _ptr(workspace), wb, _stream(stream)))
 
 
 def msa_index_topk_noalloc(shape, q_idx, k_idx, block_idx, check: bool = True, stream=None) -> None:

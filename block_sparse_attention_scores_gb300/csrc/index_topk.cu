@@ -22,6 +22,8 @@
 //   warp 0      TMA producer: q tile per item, k_idx tiles into a 4-stage ring
 //   warp 1      TMEM owner and UMMA issuer (one thread), 2 accumulators
 //   warps 2..5  epilogue: tcgen05.ld, block max, running top-k, output
+#include <cuda_fp8.h>
+
 #include "msa_internal.h"
 #include "sm100.cuh"
 
@@ -30,7 +32,7 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kStages = 4;
-constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16 (the FP8 path uses half of each tile)
 constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
 
 struct TopkArgs {
@@ -39,6 +41,7 @@ struct TopkArgs {
   int32_t* block_idx;
   int* counter;
   int* err;
+  const float* k_scale;  // FP8 path: dequantization scale of each (b, key block)
 };
 
 struct TopkShared {
@@ -78,9 +81,15 @@ __device__ __forceinline__ void topk_insert(float (&val)[CAP], int (&idx)[CAP], 
   }
 }
 
-template <int CAP>
+// FP8: q and k tiles are E4M3 (128 rows x 64 bytes, 64-byte swizzle), the
+// MMAs are kind::f8f6f4 (K = 32 per instruction), and each block's max is
+// multiplied by its key-block scale before it enters the top-k (the query
+// row's own scale is positive and common to all its blocks: it cannot change
+// the selection).
+template <int CAP, bool FP8>
 __global__ void __launch_bounds__(kThreads, 2)
     index_topk_kernel(TopkArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
+  constexpr int kLoadBytes = FP8 ? kTileBytes / 2 : kTileBytes;  // bytes a q or k tile load brings
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;                   // 2 x 16 KB
@@ -132,13 +141,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         int b, g, qb;
         decode_item(item, a.B, a.G, a.n, b, g, qb);
         if (!mbar_wait(&sh.q_empty[s], ph ^ 1, a.err, 102)) { *abort_flag = 1; break; }
-        mbar_arrive_expect_tx(&sh.q_full[s], kTileBytes);
+        mbar_arrive_expect_tx(&sh.q_full[s], kLoadBytes);
         tma_load_3d(sQ + s * kTileBytes, &map_q, &sh.q_full[s], 0, g, b * a.T + qb * 128);
         bool ok = true;
         for (int c = 0; c < qb; ++c, ++kc) {
           const int st = kc % kStages;
           if (!mbar_wait(&sh.k_empty[st], ((kc / kStages) & 1) ^ 1, a.err, 103)) { ok = false; break; }
-          mbar_arrive_expect_tx(&sh.k_full[st], kTileBytes);
+          mbar_arrive_expect_tx(&sh.k_full[st], kLoadBytes);
           tma_load_2d(sK + st * kTileBytes, &map_k, &sh.k_full[st], 0, b * a.T + c * 128);
         }
         if (!ok) { *abort_flag = 1; break; }
@@ -147,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- UMMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = make_idesc_bf16(128, 128, false, false);
+      constexpr uint32_t idesc = FP8 ? make_idesc_e4m3(128, 128) : make_idesc_bf16(128, 128, false, false);
       uint32_t kc = 0, ac = 0;
       for (int it = 0;; ++it) {
         const int s = it & 1;
@@ -169,11 +178,20 @@ __global__ void __launch_bounds__(kThreads, 2)
           if (!mbar_wait(&sh.acc_empty[ab], ((ac >> 1) & 1) ^ 1, a.err, 114)) { ok = false; break; }
           tc_fence_after();
           const uint32_t kaddr = smem_u32(sK + st * kTileBytes);
+          if constexpr (FP8) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t ad = make_sdesc(qaddr + ks * 32, 16, 1024, kSw128);
-            const uint64_t bd = make_sdesc(kaddr + ks * 32, 16, 1024, kSw128);
-            umma_bf16_ss(tmem + ab * 128, ad, bd, idesc, ks > 0);
+            for (int ks = 0; ks < 2; ++ks) {  // K = 64 bytes = 2 x 32 E4M3 values
+              const uint64_t ad = make_sdesc(qaddr + ks * 32, 16, 512, kSw64);
+              const uint64_t bd = make_sdesc(kaddr + ks * 32, 16, 512, kSw64);
+              umma_e4m3_ss(tmem + ab * 128, ad, bd, idesc, ks > 0);
+            }
+          } else {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = make_sdesc(qaddr + ks * 32, 16, 1024, kSw128);
+              const uint64_t bd = make_sdesc(kaddr + ks * 32, 16, 1024, kSw128);
+              umma_bf16_ss(tmem + ab * 128, ad, bd, idesc, ks > 0);
+            }
           }
           umma_commit(&sh.k_empty[st]);
           umma_commit(&sh.acc_full[ab]);
@@ -226,7 +244,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);
-        topk_insert<CAP>(val, idx, fmaxf(m0, m1), c);
+        float mx = fmaxf(m0, m1);
+        if constexpr (FP8) mx *= a.k_scale[(size_t)b * a.n + c];
+        topk_insert<CAP>(val, idx, mx, c);
       }
       if (!ok) { *abort_flag = 1; break; }
       // keep the best k-1, order them by block id, append the own block
@@ -262,16 +282,66 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (warp == 1) tmem_dealloc(tmem, 256);
 }
 
-template <int CAP>
+template <int CAP, bool FP8>
 cudaError_t launch_cap(const Prob& p, const TopkArgs& args, const CUtensorMap& mq, const CUtensorMap& mk,
                        cudaStream_t st) {
-  auto kern = index_topk_kernel<CAP>;
+  auto kern = index_topk_kernel<CAP, FP8>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = min(args.num_items, 2 * num_sms());
   kern<<<grid, kThreads, kSmemBytes, st>>>(args, mq, mk);
   count_launches(1);
   return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- FP8 index inputs
+// E4M3 copies of the index queries (one scale per (b, t, g) row) and keys
+// (one scale per (b, 128-key block)): x * (448 / amax) rounded to nearest
+// (ties to even) with saturation; the dequantization scale is amax / 448.
+__device__ __forceinline__ uint16_t to_e4m3x2(float lo, float hi) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+
+// One warp per q_idx row of 64 values.
+__global__ void quant_q_kernel(const __nv_bfloat16* __restrict__ q, uint16_t* __restrict__ q8, long long rows) {
+  const int lane = threadIdx.x & 31;
+  for (long long r = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; r < rows;
+       r += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const float2 v = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162*>(q + r * 64)[lane]);
+    float amax = fmaxf(fabsf(v.x), fabsf(v.y));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float mul = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+    q8[r * 32 + lane] = to_e4m3x2(__fmul_rn(v.x, mul), __fmul_rn(v.y, mul));
+  }
+}
+
+// One 256-thread CTA per (b, key block): 128 rows x 64 values.
+__global__ void __launch_bounds__(256) quant_k_kernel(const __nv_bfloat16* __restrict__ k, uint16_t* __restrict__ k8,
+                                                      float* __restrict__ k_scale, int T, int n) {
+  __shared__ float wmax[8];
+  const int bc = blockIdx.x, b = bc / n, c = bc % n;
+  const size_t base = ((size_t)b * T + (size_t)c * 128) * 64;  // 128 x 64 bf16 = 4096 pairs
+  const __nv_bfloat162* src = reinterpret_cast<const __nv_bfloat162*>(k + base);
+  float2 v[16];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    v[i] = __bfloat1622float2(src[threadIdx.x + 256 * i]);
+    amax = fmaxf(amax, fmaxf(fabsf(v[i].x), fabsf(v[i].y)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = wmax[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) amax = fmaxf(amax, wmax[i]);
+  const float mul = amax > 0.f ? __fdiv_rn(448.f, amax) : 1.f;
+  if (threadIdx.x == 0) k_scale[bc] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  uint16_t* dst = k8 + base / 2;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) dst[threadIdx.x + 256 * i] = to_e4m3x2(__fmul_rn(v[i].x, mul), __fmul_rn(v[i].y, mul));
 }
 
 }  // namespace
@@ -306,11 +376,58 @@ cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_id
   args.err = reinterpret_cast<int*>(w + L.err);
   cudaError_t e = cudaMemsetAsync(args.counter, 0, sizeof(int), st);
   if (e != cudaSuccess) return e;
+  args.k_scale = nullptr;
   const int need = p.k - 1;
-  if (need <= 4) return launch_cap<4>(p, args, mq, mk, st);
-  if (need <= 16) return launch_cap<16>(p, args, mq, mk, st);
-  if (need <= 32) return launch_cap<32>(p, args, mq, mk, st);
-  return launch_cap<64>(p, args, mq, mk, st);
+  if (need <= 4) return launch_cap<4, false>(p, args, mq, mk, st);
+  if (need <= 16) return launch_cap<16, false>(p, args, mq, mk, st);
+  if (need <= 32) return launch_cap<32, false>(p, args, mq, mk, st);
+  return launch_cap<64, false>(p, args, mq, mk, st);
+}
+
+cudaError_t launch_index_topk_fp8(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
+                                  const WsLayout& L, cudaStream_t st) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint16_t* q8 = reinterpret_cast<uint16_t*>(w + L.q8);
+  uint16_t* k8 = reinterpret_cast<uint16_t*>(w + L.k8);
+  float* ks = reinterpret_cast<float*>(w + L.k_scale);
+  const long long qrows = (long long)p.B * p.T * p.G;
+  quant_q_kernel<<<(int)std::min<long long>((qrows * 32 + 255) / 256, 16LL * num_sms()), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(q_idx), q8, qrows);
+  quant_k_kernel<<<p.B * p.n, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(k_idx), k8, ks, p.T, p.n);
+  count_launches(2);
+  CUtensorMap mq, mk;
+  {
+    const uint64_t dims[3] = {64, (uint64_t)p.G, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {64, (uint64_t)p.G * 64};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap(&mq, q8, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {64, (uint64_t)p.BT()};
+    const uint64_t strides[1] = {64};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap(&mk, k8, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_DATA_TYPE_UINT8))
+      return cudaErrorInvalidValue;
+  }
+  TopkArgs args;
+  args.B = p.B;
+  args.T = p.T;
+  args.G = p.G;
+  args.n = p.n;
+  args.k = p.k;
+  args.num_items = p.B * p.G * p.n;
+  args.block_idx = block_idx;
+  args.counter = reinterpret_cast<int*>(w + L.counters);
+  args.err = reinterpret_cast<int*>(w + L.err);
+  args.k_scale = ks;
+  cudaError_t e = cudaMemsetAsync(args.counter, 0, sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  const int need = p.k - 1;
+  if (need <= 4) return launch_cap<4, true>(p, args, mq, mk, st);
+  if (need <= 16) return launch_cap<16, true>(p, args, mq, mk, st);
+  if (need <= 32) return launch_cap<32, true>(p, args, mq, mk, st);
+  return launch_cap<64, true>(p, args, mq, mk, st);
 }
 
 }  // namespace msa

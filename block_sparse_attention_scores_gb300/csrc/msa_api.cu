@@ -88,7 +88,14 @@ WsLayout ws_layout(const Prob& p, int which) {
   };
   const size_t lists = (size_t)p.B * p.G * p.n;
   const size_t rows = (size_t)p.B * p.T;
-  if (which >= MSA_WS_FWD) {
+  if (which == MSA_WS_TOPK_FP8) {
+    L.q8 = take(rows * p.G * p.E);
+    L.k8 = take(rows * p.E);
+    L.k_scale = take((size_t)p.B * p.n * 4);
+    L.total = off;
+    return L;
+  }
+  if (which == MSA_WS_FWD || which == MSA_WS_BWD) {
     L.list_count = take(lists * 4);
     L.list_off = take((lists + 1) * 4);
     L.chunk_off = take((size_t)p.B * p.G * ((size_t)p.n * (p.n + 1) / 2) * 4);
@@ -202,7 +209,7 @@ const char* msa_last_error(void) { return g_err; }
 
 size_t msa_workspace_size(const msa_shape* shape, int which) {
   Prob p;
-  if (which < MSA_WS_TOPK || which > MSA_WS_BWD) return 0;
+  if (which < MSA_WS_TOPK || which > MSA_WS_TOPK_FP8) return 0;
   if (validate(shape, &p) != MSA_OK) return 0;
   return ws_layout(p, which).total;
 }
@@ -222,6 +229,23 @@ msa_status msa_index_topk(const msa_shape* shape, const void* q_idx, const void*
   uint8_t* w = static_cast<uint8_t*>(workspace);
   if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
   return cuda_status(launch_index_topk(p, q_idx, k_idx, block_idx, workspace, L, st), "index top-k launch");
+}
+
+msa_status msa_index_topk_fp8(const msa_shape* shape, const void* q_idx, const void* k_idx, int32_t* block_idx,
+                              void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Prob p;
+  WsLayout L;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_ptr(q_idx, "q_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(k_idx, "k_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(block_idx, "block_idx", 16)) != MSA_OK) return s;
+  if ((s = check_ws(p, MSA_WS_TOPK_FP8, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_index_topk_fp8(p, q_idx, k_idx, block_idx, workspace, L, st), "FP8 index top-k launch");
 }
 
 static msa_status sparse_fwd_impl(const msa_shape* shape, const void* Q, const void* K, const void* V,

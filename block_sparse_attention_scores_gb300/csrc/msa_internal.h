@@ -44,6 +44,9 @@ struct WsLayout {
   size_t dqi_part = 0;      // bf16  [padded entries, E]     dq_idx partials, tile order
   size_t kl_part = 0;       // fp32  [B,T,G,k]      KL partials per slot
   size_t dki_part = 0;      // fp32  [B,G,T,E]      dk_idx per group
+  size_t q8 = 0;            // e4m3  [B,T,G,E]      FP8 index queries (MSA_WS_TOPK_FP8)
+  size_t k8 = 0;            // e4m3  [B,T,E]        FP8 index keys
+  size_t k_scale = 0;       // fp32  [B,n]          dequantization scale per key block
   size_t total = 256;
   int max_items = 0;
   long long max_padded = 0;  // capacity in padded entries (queries x slots, tile-padded per list)
@@ -67,6 +70,8 @@ void count_launches(int n);
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
                               const WsLayout& L, cudaStream_t st);
+cudaError_t launch_index_topk_fp8(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
+                                  const WsLayout& L, cudaStream_t st);
 
 // Inverted block -> query lists and work items (rows_per_tile * tiles_per_item
 // entries per item).

@@ -87,11 +87,12 @@ typedef struct msa_shape {
 } msa_shape;
 
 /* Which entry point a workspace is sized for. */
-enum { MSA_WS_TOPK = 0, MSA_WS_FWD = 1, MSA_WS_BWD = 2 };
+enum { MSA_WS_TOPK = 0, MSA_WS_FWD = 1, MSA_WS_BWD = 2, MSA_WS_TOPK_FP8 = 3 };
 
 /* Bytes of device workspace the entry point `which` needs for `shape`
  * (0 if the shape is invalid or unsupported). A workspace sized for
- * MSA_WS_BWD also serves the other two. */
+ * MSA_WS_BWD also serves MSA_WS_TOPK and MSA_WS_FWD; MSA_WS_TOPK_FP8 is
+ * sized on its own (its E4M3 copies start right after the header). */
 MSA_API size_t msa_workspace_size(const msa_shape *shape, int which);
 
 /*
@@ -112,6 +113,22 @@ MSA_API size_t msa_workspace_size(const msa_shape *shape, int which);
  */
 MSA_API msa_status msa_index_topk(const msa_shape *shape, const void *q_idx, const void *k_idx, int32_t *block_idx,
                           void *workspace, size_t workspace_bytes, msa_stream_t stream);
+
+/* msa_index_topk with a low-precision indexer (dothoosh.com "how Flash-MSA
+ * cuts million-token training cost", "Current limits and future scaling":
+ * training the indexer in low precision, as at inference). The index scores
+ * are computed from E4M3 copies of q_idx and k_idx made inside the call: one
+ * scale per q_idx row (b, t, g) and one per 128-key block of k_idx (b, c);
+ * each value is multiplied by 448 / amax in fp32 and rounded to the nearest
+ * E4M3 value (ties to even, saturating at +-448); the scale is amax / 448
+ * (1 when amax = 0). Pooling and selection are those of msa_index_topk on
+ * the scores (q8 * sq) . (k8 * sk) * scale_idx, so block_idx can differ from
+ * msa_index_topk's where quantization reorders blocks. `workspace` is sized
+ * with MSA_WS_TOPK_FP8 (it holds the E4M3 copies: B*T*(G+1)*d_idx bytes plus
+ * one float per key block); same arguments and errors as msa_index_topk. */
+MSA_API msa_status msa_index_topk_fp8(const msa_shape *shape, const void *q_idx, const void *k_idx,
+                                      int32_t *block_idx, void *workspace, size_t workspace_bytes,
+                                      msa_stream_t stream);
 
 /*
  * Main branch forward (itinai.ru "Two-stage process": exact softmax over the
