@@ -63,22 +63,25 @@ __device__ __forceinline__ void decode_item(int item, int B, int G, int n, int& 
 }
 
 // Insert (v, c) into a list sorted by (value desc, id asc). Ids arrive in
-// increasing order, so an equal value never displaces an earlier entry.
+// increasing order, so (v, c) goes after every entry >= v: slot i takes
+// (v, c) if v beats entry i but not entry i-1, entry i-1 if v beats both, and
+// keeps its own entry otherwise. Every slot is decided from the old list at
+// once (no chain through the slots), and the entries below the insertion point
+// move down one slot in order, so among equal values the lower ids stay first
+// and the last one falls off.
 template <int CAP>
 __device__ __forceinline__ void topk_insert(float (&val)[CAP], int (&idx)[CAP], float v, int c) {
   if (!(v > val[CAP - 1])) return;
-  float cv = v;
-  int ci = c;
+  bool gt[CAP];
 #pragma unroll
-  for (int i = 0; i < CAP; ++i) {
-    const bool sw = cv > val[i];
-    const float tv = val[i];
-    const int ti = idx[i];
-    val[i] = sw ? cv : tv;
-    idx[i] = sw ? ci : ti;
-    cv = sw ? tv : cv;
-    ci = sw ? ti : ci;
+  for (int i = 0; i < CAP; ++i) gt[i] = v > val[i];
+#pragma unroll
+  for (int i = CAP - 1; i > 0; --i) {
+    val[i] = gt[i] ? (gt[i - 1] ? val[i - 1] : v) : val[i];
+    idx[i] = gt[i] ? (gt[i - 1] ? idx[i - 1] : c) : idx[i];
   }
+  val[0] = gt[0] ? v : val[0];
+  idx[0] = gt[0] ? c : idx[0];
 }
 
 // FP8: q and k tiles are E4M3 (128 rows x 64 bytes, 64-byte swizzle), the

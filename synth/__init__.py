@@ -30,7 +30,7 @@ import numpy as np
 SEED_BASE = 20260712
 
 # tensor ids of the counter-based streams
-TID_Q, TID_K, TID_V, TID_DO, TID_QIDX, TID_KIDX, TID_KMEAN, TID_BLOCKIDX = range(1, 9)
+TID_Q, TID_K, TID_V, TID_DO, TID_QIDX, TID_KIDX, TID_KMEAN, TID_BLOCKIDX, TID_TIES = range(1, 10)
 
 _GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
@@ -196,6 +196,33 @@ def k_idx_bf16(w: Workload) -> np.ndarray:
     blk = np.arange(w.T) // w.Bk
     x = z + np.float32(0.5) * m[:, blk, :]
     return f32_to_bf16_bits(x.astype(np.float32)).reshape(w.B, w.T, w.d_idx)
+
+
+def tied_index_inputs(w: Workload):
+    """Index inputs whose pooled block scores tie exactly, with no rounding anywhere.
+
+    q_idx entries are multiples of 1/8 in [-2, 2]. Every key of block c is
+    a_c * u, with u one shared vector of multiples of 1/8 in [-1, 1] (one entry
+    exactly 1) and a_c drawn from {1, 2, 4}. All products and sums of the index
+    scores are then exact in fp32 and fp64, and so are the E4M3 codes of the
+    keys (the per-block scale absorbs a_c). Blocks with the same a_c thus have
+    bit-identical pooled scores for every query, and distinct levels differ by a
+    factor of 2. Returns (q_idx [B,T,G,d_idx], k_idx [B,T,d_idx]) as bf16 bit patterns.
+    """
+    key = stream_key(w.seed, TID_TIES)
+    nq = w.B * w.T * w.G * w.d_idx
+    hq = hash_at(key, np.arange(nq, dtype=np.uint64))
+    q = ((hq % np.uint64(33)).astype(np.int64) - 16).astype(np.float32) / np.float32(8)
+    hu = hash_at(key, np.arange(nq, nq + w.d_idx, dtype=np.uint64))
+    u = ((hu % np.uint64(17)).astype(np.int64) - 8).astype(np.float32) / np.float32(8)
+    u[0] = 1.0
+    nb = w.B * w.n_blocks
+    ha = hash_at(key, np.arange(nq + w.d_idx, nq + w.d_idx + nb, dtype=np.uint64))
+    a = np.array([1.0, 2.0, 4.0], dtype=np.float32)[(ha % np.uint64(3)).astype(np.intp)].reshape(w.B, w.n_blocks)
+    blk = np.arange(w.T) // w.Bk
+    k = a[:, blk, None] * u[None, None, :]
+    return (f32_to_bf16_bits(q).reshape(w.B, w.T, w.G, w.d_idx),
+            f32_to_bf16_bits(k.astype(np.float32)).reshape(w.B, w.T, w.d_idx))
 
 
 def synthetic_block_idx(w: Workload, seed_offset: int = 0) -> np.ndarray:

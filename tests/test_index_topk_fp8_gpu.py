@@ -66,3 +66,28 @@ def test_fp8_workspace_kind(msa):
     s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
     need = msa.msa_workspace_size(s, msa.MSA_WS_TOPK_FP8)
     assert need >= w.B * w.T * (w.G + 1) * w.d_idx + w.B * w.n_blocks * 4
+
+
+@pytest.mark.parametrize("cfg", [
+    synth.CONFIGS[0].with_(T=4096, G=2, Hq=16, k=16, name="ties_k16"),
+    synth.CONFIGS[0].with_(T=8192, G=1, Hq=8, k=33, name="ties_k33"),
+], ids=["k16", "k33"])
+def test_index_topk_fp8_exact_ties(msa, cfg):
+    """tied_index_inputs through the FP8 path: the keys of every block share one
+    set of E4M3 codes and the block scales differ by powers of two, so equal
+    levels tie exactly; every row must match the oracle's FP8 selection."""
+    import torch
+
+    q_idx, k_idx = synth.tied_index_inputs(cfg)
+    s = msa.Shape(B=cfg.B, T=cfg.T, Hq=cfg.Hq, G=cfg.G, k=cfg.k)
+    ws = msa.alloc_workspace(s, msa.MSA_WS_TOPK_FP8)
+    got = torch.empty((cfg.B, cfg.G, cfg.T, cfg.k), dtype=torch.int32, device="cuda")
+    msa.msa_index_topk_fp8(s, to_dev(q_idx), to_dev(k_idx), got, ws)
+    msa.msa_check_device_status(ws)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    want, gap, _ = oracle.index_topk_fp8(oracle.shape_of(cfg), q_idx, k_idx)
+    want = want.reshape(got.shape)
+    bad = int((got != want).any(axis=-1).sum())
+    print(f"{cfg.name}: rows={want.shape[0] * want.shape[2]} tied at the boundary={(gap == 0).sum()} mismatches={bad}")
+    assert bad == 0

@@ -60,6 +60,30 @@ def test_index_topk_config1_full(msa):
     assert bad == 0
 
 
+@pytest.mark.parametrize("cfg", [
+    synth.CONFIGS[0].with_(T=4096, G=2, Hq=2, k=5, name="ties_k5"),
+    synth.CONFIGS[0].with_(T=4096, G=2, Hq=16, k=16, name="ties_k16"),
+    synth.CONFIGS[0].with_(T=8192, G=1, Hq=8, k=33, name="ties_k33"),
+    synth.CONFIGS[0].with_(T=12288, G=1, Hq=8, k=64, name="ties_k64"),
+], ids=["k5", "k16", "k33", "k64"])
+def test_index_topk_exact_ties(msa, cfg):
+    """Pooled scores that tie exactly (tied_index_inputs): every row must match the
+    oracle bit for bit, ties included: equal scores go to the lower block id."""
+    import torch
+
+    q_idx, k_idx = synth.tied_index_inputs(cfg)
+    s = msa.Shape(B=cfg.B, T=cfg.T, Hq=cfg.Hq, G=cfg.G, k=cfg.k)
+    ws = msa.alloc_workspace(s, msa.MSA_WS_TOPK)
+    got = msa.index_topk(s, to_dev(q_idx), to_dev(k_idx), workspace=ws)
+    msa.msa_check_device_status(ws)
+    torch.cuda.synchronize()
+    got = got.cpu().numpy()
+    want, gap, _ = oracle.full_topk(oracle.shape_of(cfg), q_idx, k_idx)
+    bad = int((got != want).any(axis=-1).sum())
+    print(f"{cfg.name}: rows={got.shape[1] * got.shape[2]} tied at the boundary={(gap == 0).sum()} mismatches={bad}")
+    assert bad == 0
+
+
 def _sampled_rows(w, n_per_group, seed):
     rng = np.random.default_rng(seed)
     rows = []

@@ -122,6 +122,35 @@ def test_topk_constructed_ties_pick_lowest_block():
             assert bi[t].tolist() == [1, 2, own], t
 
 
+def _tied_closed_form(w, q_idx, k_idx):
+    """Selection for tied_index_inputs by the tie rule alone: every earlier block c
+    scores a_c * (q . u) / sqrt(d_idx); order by (score desc, block asc)."""
+    q = _f64(q_idx)
+    kk = _f64(k_idx)
+    u = kk[0, 0] / (kk[0, 0, 0])          # the shared vector (u[0] == 1)
+    a = kk[:, ::w.Bk, 0]                  # a_c per (b, block)
+    out = np.full((w.B, w.G, w.T, w.k), -1, dtype=np.int32)
+    for b in range(w.B):
+        for g in range(w.G):
+            s0 = q[b, :, g] @ u
+            for t in range(w.T):
+                own = t // w.Bk
+                cand = sorted(range(own), key=lambda c: (-a[b, c] * s0[t], c))[: min(w.k - 1, own)]
+                sel = sorted(cand + [own])
+                out[b, g, t, : len(sel)] = sel
+    return out
+
+
+@pytest.mark.parametrize("k", [2, 4, 7])
+def test_topk_exact_tie_levels_match_tie_rule(k):
+    # many exact ties at every rank, including larger values arriving after runs of equal ones
+    w = synth.CONFIGS[0].with_(T=1024, G=2, Hq=2, k=k, name="tied")
+    q_idx, k_idx = synth.tied_index_inputs(w)
+    bi, gap, _ = oracle.full_topk(oracle.shape_of(w), q_idx, k_idx)
+    assert np.array_equal(bi, _tied_closed_form(w, q_idx, k_idx))
+    assert (gap[..., 3 * w.Bk:] == 0).mean() > 0.1  # many rows have a tie at the k-boundary
+
+
 # ------------------------------------------------------------------ forward
 def test_fwd_handworked_fixture():
     g = json.load(open(os.path.join(GOLDEN, "fwd_handworked.json")))
