@@ -414,6 +414,59 @@ def run_gpu(args, w):
     e2e_ms = dist_max(f0.elapsed_time(f1) / args.steps, dev)
     msa.msa_check_device_status(ws, stream)
 
+    # ---- FP8 index top-k (E4M3 copies of q_idx and k_idx, kind::f8f6f4 MMAs) on the same inputs
+    ws8 = msa.alloc_workspace(s, msa.MSA_WS_TOPK_FP8, dev)
+    bi8 = torch.empty_like(bi)
+    for _ in range(2):
+        msa.msa_index_topk_fp8(s, d_in["q_idx"], d_in["k_idx"], bi8, ws8, stream)
+    torch.cuda.synchronize()
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(args.steps):
+        msa.msa_index_topk_fp8(s, d_in["q_idx"], d_in["k_idx"], bi8, ws8, stream)
+    h1.record(stream)
+    torch.cuda.synchronize()
+    fp8_ms = dist_max(h0.elapsed_time(h1) / args.steps, dev)
+    msa.msa_check_device_status(ws8, stream)
+    del ws8, bi8
+
+    # ---- indexer warmup: full causal attention (every visible block selected)
+    # and the KL against the dense teacher, at B = 2, T = 8192 (all 64 blocks)
+    wu = synth.CONFIGS[1].with_(B=2, k=64, name="warmup_b2_t8192_hq32_g8_all_blocks")
+    su = msa.Shape(B=wu.B, T=wu.T, Hq=wu.Hq, G=wu.G, d=wu.d, d_idx=wu.d_idx, Bk=wu.Bk, k=wu.k)
+    hu = synth.make_inputs(rank_workload(wu, rank))
+    du = {n: torch.from_numpy(np.ascontiguousarray(hu[n]).view(np.int16)).view(torch.bfloat16).to(dev) for n in hu}
+    wsu = msa.alloc_workspace(su, msa.MSA_WS_BWD, dev)
+    biu = torch.empty((wu.B, wu.G, wu.T, wu.k), dtype=torch.int32, device=dev)
+    Ou = torch.empty_like(du["Q"])
+    LSEu = torch.empty((wu.B, wu.T, wu.Hq), dtype=torch.float32, device=dev)
+    outu = {n: torch.empty(du[src].shape, **f32) for n, src in (("dQ", "Q"), ("dK", "K"), ("dV", "V"),
+                                                                  ("dq_idx", "q_idx"), ("dk_idx", "k_idx"))}
+    outu["KL"] = torch.empty((wu.B, wu.G, wu.T), **f32)
+
+    def warmup_step():
+        msa.msa_warmup_block_idx(su, biu, stream)
+        msa.msa_sparse_fwd(su, du["Q"], du["K"], du["V"], biu, Ou, LSEu, wsu, stream)
+        msa.msa_bwd(su, du["Q"], du["K"], du["V"], Ou, du["dO"], LSEu, du["q_idx"], du["k_idx"], biu, 1.0,
+                    outu["dQ"], outu["dK"], outu["dV"], outu["dq_idx"], outu["dk_idx"], outu["KL"], wsu, stream)
+
+    for _ in range(args.warmup):
+        warmup_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    u0 = torch.cuda.Event(enable_timing=True)
+    u1 = torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(args.steps):
+        warmup_step()
+    u1.record(stream)
+    torch.cuda.synchronize()
+    warm_ms = dist_max(u0.elapsed_time(u1) / args.steps, dev)
+    msa.msa_check_device_status(wsu, stream)
+    del wsu, du, Ou, LSEu, outu, biu
+
     if rank == 0:
         fl = counted_flops(w)
         peaks, src = measured_peaks()
@@ -451,6 +504,14 @@ def run_gpu(args, w):
                             "tflops": (fl["fwd"] + fl["bwd"]) / (share_ms * 1e-3) / 1e12,
                             "note": "a layer reusing an earlier layer's block_idx and block map "
                                     "(msa_block_map once): msa_sparse_fwd_mapped + msa_bwd_mapped"},
+            "index_topk_fp8": {"ms": fp8_ms, "tflops": fl["index"] / (fp8_ms * 1e-3) / 1e12,
+                               "note": "msa_index_topk_fp8: E4M3 q_idx (per row) and k_idx (per block) with "
+                                       "kind::f8f6f4 MMAs; same workload as index_topk"},
+            "indexer_warmup": {"workload": wu.name, "ms_per_step": warm_ms,
+                       "tokens_per_s": aggregate_tokens_per_s(wu, world, warm_ms),
+                       "tflops": (counted_flops(wu)["fwd"] + counted_flops(wu)["bwd"]) / (warm_ms * 1e-3) / 1e12,
+                       "note": "indexer warmup: msa_warmup_block_idx (every visible block) + msa_sparse_fwd + "
+                               "msa_bwd = dense causal attention and the dense-teacher KL"},
         }
         if world == 1 and not args.no_cpu_baseline:
             v, desc, cores = oracle_sample(w, args.cpu_seconds)

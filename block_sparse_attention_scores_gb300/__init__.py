@@ -32,7 +32,8 @@ MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD, MSA_WS_TOPK_FP8 = 0, 1, 2, 3
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
             "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version",
-            "msa_index_topk_noalloc", "msa_index_topk_fp8", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped")
+            "msa_index_topk_noalloc", "msa_index_topk_fp8", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped",
+            "msa_warmup_block_idx")
 
 
 class MsaError(RuntimeError):
@@ -87,8 +88,9 @@ def load_library():
     lib.msa_sparse_fwd_mapped.argtypes = lib.msa_sparse_fwd.argtypes
     lib.msa_bwd_mapped.argtypes = lib.msa_bwd.argtypes
     lib.msa_block_map.argtypes = [S, P, P, ctypes.c_size_t, P]
+    lib.msa_warmup_block_idx.argtypes = [S, P, P]
     for f in (lib.msa_index_topk, lib.msa_sparse_fwd, lib.msa_bwd, lib.msa_sparse_fwd_mapped, lib.msa_bwd_mapped,
-              lib.msa_block_map):
+              lib.msa_block_map, lib.msa_warmup_block_idx):
         f.restype = ctypes.c_int
     lib.msa_last_error.argtypes = []
     lib.msa_last_error.restype = ctypes.c_char_p
@@ -184,6 +186,11 @@ def msa_block_map(shape, block_idx, workspace, stream=None, workspace_bytes=None
                                         _stream(stream)))
 
 
+def msa_warmup_block_idx(shape, block_idx, stream=None) -> None:
+    """Full causal selection (every visible block) into block_idx [B,G,T,k] for the indexer warmup."""
+    _check(load_library().msa_warmup_block_idx(ctypes.byref(_shape(shape)), _ptr(block_idx), _stream(stream)))
+
+
 def msa_sparse_fwd_mapped(shape, Q, K, V, block_idx, O, LSE, workspace, stream=None, workspace_bytes=None) -> None:
     wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
     _check(load_library().msa_sparse_fwd_mapped(ctypes.byref(_shape(shape)), _ptr(Q), _ptr(K), _ptr(V),
@@ -234,6 +241,15 @@ def index_topk(shape: Shape, q_idx, k_idx, workspace=None, stream=None):
     ws = workspace if workspace is not None else alloc_workspace(shape, MSA_WS_TOPK, q_idx.device)
     bi = torch.empty((shape.B, shape.G, shape.T, shape.k), dtype=torch.int32, device=q_idx.device)
     msa_index_topk(shape, q_idx, k_idx, bi, ws, stream)
+    return bi
+
+
+def warmup_block_idx(shape: Shape, device="cuda", stream=None):
+    """Allocate block_idx [B,G,T,k] int32 and fill it with msa_warmup_block_idx."""
+    import torch
+
+    bi = torch.empty((shape.B, shape.G, shape.T, shape.k), dtype=torch.int32, device=device)
+    msa_warmup_block_idx(shape, bi, stream)
     return bi
 
 

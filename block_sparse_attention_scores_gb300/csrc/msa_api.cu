@@ -201,7 +201,7 @@ using namespace msa;
 
 extern "C" {
 
-int32_t msa_version(void) { return (1 << 16) | 1; }
+int32_t msa_version(void) { return (1 << 16) | 2; }
 
 int64_t msa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -341,6 +341,18 @@ msa_status msa_block_map(const msa_shape* shape, const int32_t* block_idx, void*
   const int fq = fwd_tile_queries(p);
   return cuda_status(build_block_map2(p, block_idx, w, L, fq, (long long)fq * kFwdTilesPerItem, 1LL << 30, true, st),
                      "block map launch");
+}
+
+msa_status msa_warmup_block_idx(const msa_shape* shape, int32_t* block_idx, msa_stream_t stream) {
+  Prob p;
+  msa_status s;
+  if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if (p.k < p.n)
+    return fail(MSA_ERR_UNSUPPORTED, "full attention needs k >= T / Bk = %d blocks (k=%d)", p.n, p.k);
+  if ((s = check_ptr(block_idx, "block_idx", 4)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  return cuda_status(launch_warmup_block_idx(p, block_idx, reinterpret_cast<cudaStream_t>(stream)),
+                     "warmup block_idx launch");
 }
 
 msa_status msa_selftest_wait_timeout(void* workspace, int32_t limit_us, msa_stream_t stream) {

@@ -73,6 +73,9 @@ cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_id
 cudaError_t launch_index_topk_fp8(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
                                   const WsLayout& L, cudaStream_t st);
 
+// Full causal selection (every visible block) for the indexer warmup.
+cudaError_t launch_warmup_block_idx(const Prob& p, int32_t* block_idx, cudaStream_t st);
+
 // Inverted block -> query lists and work items (rows_per_tile * tiles_per_item
 // entries per item).
 cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L,

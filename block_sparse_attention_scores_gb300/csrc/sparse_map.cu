@@ -248,6 +248,19 @@ __global__ void __launch_bounds__(128) map_chunk_scatter_kernel(const int32_t* _
   }
 }
 
+// Selection of full causal attention: row (b, g, t) lists the blocks
+// 0 .. t / Bk ascending, then -1 (k >= number of blocks, checked by the caller).
+__global__ void warmup_block_idx_kernel(int32_t* __restrict__ block_idx, long long rows, int T, int Bk, int k) {
+  const long long total = rows * k;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / k;
+    const int slot = (int)(i - row * k);
+    const int own = (int)(row % T) / Bk;
+    block_idx[i] = slot <= own ? slot : -1;
+  }
+}
+
 }  // namespace
 
 cudaError_t build_block_map(const Prob& p, const int32_t* block_idx, uint8_t* ws, const WsLayout& L,
@@ -291,6 +304,14 @@ cudaError_t build_block_map2(const Prob& p, const int32_t* block_idx, uint8_t* w
   map_chunk_scatter_kernel<<<chunks, 128, mask_bytes, st>>>(block_idx, p.T, p.n, p.k, chunk, off, poff, entries,
                                                              rev, err);
   count_launches(4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_warmup_block_idx(const Prob& p, int32_t* block_idx, cudaStream_t st) {
+  const long long rows = (long long)p.B * p.G * p.T;
+  const int grid = (int)std::min<long long>((rows * p.k + 255) / 256, 8LL * num_sms());
+  warmup_block_idx_kernel<<<grid, 256, 0, st>>>(block_idx, rows, p.T, p.Bk, p.k);
+  count_launches(1);
   return cudaGetLastError();
 }
 

@@ -238,6 +238,18 @@ MSA_API msa_status msa_bwd_mapped(const msa_shape *shape, const void *Q, const v
                                   float *dV, float *dq_idx, float *dk_idx, float *KL, void *workspace,
                                   size_t workspace_bytes, msa_stream_t stream);
 
+/* Indexer warmup (itinai.ru "How to solve the memory problem with MiniMax
+ * Sparse Attention", "Training sparse attention": the first iterations run
+ * full attention so that the indexer learns before it routes). Writes into
+ * `block_idx` [B,G,T,k] int32 (device, caller-owned) the selection of full
+ * causal attention: row (b, g, t) holds the blocks 0 .. t / Bk ascending,
+ * then -1. Given it, msa_sparse_fwd computes dense causal attention and
+ * msa_bwd the KL of the index branch against the dense teacher (the head mean
+ * of the full attention weights) over every visible token, with its gradients
+ * to q_idx and k_idx. No index scores are computed and no workspace is used.
+ * MSA_ERR_UNSUPPORTED unless k >= T / Bk (so at most T = 64 * Bk). */
+MSA_API msa_status msa_warmup_block_idx(const msa_shape *shape, int32_t *block_idx, msa_stream_t stream);
+
 /* Message describing the last non-OK status returned on this thread. */
 MSA_API const char *msa_last_error(void);
 

@@ -73,3 +73,13 @@ def test_validation_happens_before_any_device_work(lib):
     with pytest.raises(lib.MsaError) as e:
         lib.msa_sparse_fwd(bad, 4096, 4096, 4096, 4096, 4096, 4096, 4096, stream=0, workspace_bytes=1 << 30)
     assert e.value.status == lib.MSA_ERR_UNSUPPORTED
+
+
+def test_warmup_selection_validates_before_device_work(lib):
+    # full attention needs every visible block: k >= T / Bk
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_warmup_block_idx(lib.Shape(B=1, T=1024, Hq=8, G=2, k=4), 4096, stream=0)
+    assert e.value.status == lib.MSA_ERR_UNSUPPORTED and "k >= T / Bk" in str(e.value)
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_warmup_block_idx(lib.Shape(B=1, T=1024, Hq=8, G=2, k=8), 0, stream=0)
+    assert e.value.status == lib.MSA_ERR_INVALID_ARG and "block_idx" in str(e.value)

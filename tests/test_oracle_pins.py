@@ -151,6 +151,50 @@ def test_topk_exact_tie_levels_match_tie_rule(k):
     assert (gap[..., 3 * w.Bk:] == 0).mean() > 0.1  # many rows have a tie at the k-boundary
 
 
+def test_warmup_selection_is_dense_causal_attention_with_dense_teacher_kl():
+    """Indexer warmup (full attention while the indexer learns): with every
+    visible block selected, the oracle's forward, backward and KL equal torch
+    autograd (fp64) of the dense formulation -- causal softmax attention, and
+    the KL of the index softmax against the detached head mean of the attention
+    weights, both over all visible tokens."""
+    torch = pytest.importorskip("torch")
+    w = _small(T=64, Bk=8, Hq=4, G=2, d=8, d_idx=4, k=8, B=2)  # k = T / Bk
+    inp = synth.make_inputs(w)
+    s = oracle.shape_of(w, kl_weight=0.7)
+    bi, _, _ = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])
+    t = np.arange(w.T)
+    want_sel = np.where(np.arange(w.k)[None, :] <= (t // w.Bk)[:, None], np.arange(w.k)[None, :], -1)
+    assert np.array_equal(bi.reshape(w.B, w.G, w.T, w.k), np.broadcast_to(want_sel, (w.B, w.G, w.T, w.k)))
+    names = ("Q", "K", "V", "dO", "q_idx", "k_idx")
+    O_ref, LSE_ref = oracle.sparse_fwd(s, inp["Q"], inp["K"], inp["V"], bi)
+    ref = oracle.full_bwd(s, *[inp[n] for n in names], bi)
+
+    x = {n: torch.tensor(_f64(inp[n]), requires_grad=n != "dO") for n in names}
+    hg = w.Hq // w.G
+    mask = torch.tril(torch.ones(w.T, w.T, dtype=torch.bool))
+    Kh = x["K"].repeat_interleave(hg, dim=2)
+    Vh = x["V"].repeat_interleave(hg, dim=2)
+    S = torch.einsum("bthd,bshd->bhts", x["Q"], Kh) / math.sqrt(w.d)
+    S = S.masked_fill(~mask, -math.inf)
+    P = torch.softmax(S, dim=-1)
+    O = torch.einsum("bhts,bshd->bthd", P, Vh)
+    LSE = torch.logsumexp(S, dim=-1).permute(0, 2, 1)
+    Spx = torch.einsum("btge,bse->bgts", x["q_idx"], x["k_idx"]) / math.sqrt(w.d_idx)
+    logp_px = torch.log_softmax(Spx.masked_fill(~mask, -math.inf), dim=-1)
+    p_main = P.detach().reshape(w.B, w.G, hg, w.T, w.T).mean(dim=2)
+    term = torch.where(mask, p_main * (torch.log(torch.where(mask, p_main, 1.0)) - torch.where(mask, logp_px, 0.0)),
+                       0.0)
+    KL = term.sum(dim=-1)
+    ((O * x["dO"]).sum() + 0.7 * KL.sum()).backward()
+
+    np.testing.assert_allclose(O_ref.reshape(O.shape), O.detach().numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(LSE_ref.reshape(LSE.shape), LSE.detach().numpy(), rtol=1e-9, atol=1e-11)
+    np.testing.assert_allclose(ref["KL"].reshape(KL.shape), KL.detach().numpy(), rtol=1e-9, atol=1e-11)
+    for name, grad in (("dQ", x["Q"].grad), ("dK", x["K"].grad), ("dV", x["V"].grad),
+                       ("dq_idx", x["q_idx"].grad), ("dk_idx", x["k_idx"].grad)):
+        np.testing.assert_allclose(ref[name].reshape(grad.shape), grad.numpy(), rtol=1e-8, atol=1e-10, err_msg=name)
+
+
 # ------------------------------------------------------------------ forward
 def test_fwd_handworked_fixture():
     g = json.load(open(os.path.join(GOLDEN, "fwd_handworked.json")))
