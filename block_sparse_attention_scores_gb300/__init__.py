@@ -29,11 +29,12 @@ LIB_PATH = os.path.join(_HERE, "libmsa_gb300.so")
 
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUDA, MSA_ERR_DEVICE = range(6)
 MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD, MSA_WS_TOPK_FP8 = 0, 1, 2, 3
+MSA_TIME_INDEX_TOPK, MSA_TIME_SPARSE_FWD, MSA_TIME_BWD = 0, 1, 2
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
             "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version",
             "msa_index_topk_noalloc", "msa_index_topk_fp8", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped",
-            "msa_warmup_block_idx")
+            "msa_warmup_block_idx", "msa_set_timing_events")
 
 
 class MsaError(RuntimeError):
@@ -89,8 +90,9 @@ def load_library():
     lib.msa_bwd_mapped.argtypes = lib.msa_bwd.argtypes
     lib.msa_block_map.argtypes = [S, P, P, ctypes.c_size_t, P]
     lib.msa_warmup_block_idx.argtypes = [S, P, P]
+    lib.msa_set_timing_events.argtypes = [ctypes.c_int32, P, P]
     for f in (lib.msa_index_topk, lib.msa_sparse_fwd, lib.msa_bwd, lib.msa_sparse_fwd_mapped, lib.msa_bwd_mapped,
-              lib.msa_block_map, lib.msa_warmup_block_idx):
+              lib.msa_block_map, lib.msa_warmup_block_idx, lib.msa_set_timing_events):
         f.restype = ctypes.c_int
     lib.msa_last_error.argtypes = []
     lib.msa_last_error.restype = ctypes.c_char_p
@@ -189,6 +191,17 @@ def msa_block_map(shape, block_idx, workspace, stream=None, workspace_bytes=None
 def msa_warmup_block_idx(shape, block_idx, stream=None) -> None:
     """Full causal selection (every visible block) into block_idx [B,G,T,k] for the indexer warmup."""
     _check(load_library().msa_warmup_block_idx(ctypes.byref(_shape(shape)), _ptr(block_idx), _stream(stream)))
+
+
+def msa_set_timing_events(which: int, start=None, stop=None) -> None:
+    """Record two CUDA events (torch.cuda.Event with enable_timing, already
+    recorded once so that they exist, or raw handles) around every launch of
+    kernel `which`; no events stops the recording."""
+    def handle(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    _check(load_library().msa_set_timing_events(int(which), handle(start), handle(stop)))
 
 
 def msa_sparse_fwd_mapped(shape, Q, K, V, block_idx, O, LSE, workspace, stream=None, workspace_bytes=None) -> None:

@@ -292,7 +292,9 @@ cudaError_t launch_cap(const Prob& p, const TopkArgs& args, const CUtensorMap& m
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int grid = min(args.num_items, 2 * num_sms());
+  timing_begin(MSA_TIME_INDEX_TOPK, st);
   kern<<<grid, kThreads, kSmemBytes, st>>>(args, mq, mk);
+  timing_end(MSA_TIME_INDEX_TOPK, st);
   count_launches(1);
   return cudaGetLastError();
 }

@@ -195,13 +195,22 @@ static msa_status cuda_status(cudaError_t e, const char* what) {
   return fail(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+cudaEvent_t g_timing[3][2] = {};  // caller's events per timed kernel (msa_set_timing_events)
+
+void timing_begin(int which, cudaStream_t st) {
+  if (g_timing[which][0]) cudaEventRecord(g_timing[which][0], st);
+}
+void timing_end(int which, cudaStream_t st) {
+  if (g_timing[which][1]) cudaEventRecord(g_timing[which][1], st);
+}
+
 }  // namespace msa
 
 using namespace msa;
 
 extern "C" {
 
-int32_t msa_version(void) { return (1 << 16) | 2; }
+int32_t msa_version(void) { return (1 << 16) | 3; }
 
 int64_t msa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -353,6 +362,16 @@ msa_status msa_warmup_block_idx(const msa_shape* shape, int32_t* block_idx, msa_
   if ((s = check_device()) != MSA_OK) return s;
   return cuda_status(launch_warmup_block_idx(p, block_idx, reinterpret_cast<cudaStream_t>(stream)),
                      "warmup block_idx launch");
+}
+
+msa_status msa_set_timing_events(int32_t which, void* start_event, void* stop_event) {
+  if (which < MSA_TIME_INDEX_TOPK || which > MSA_TIME_BWD)
+    return fail(MSA_ERR_INVALID_ARG, "which=%d is not a timed kernel", which);
+  if ((start_event == nullptr) != (stop_event == nullptr))
+    return fail(MSA_ERR_INVALID_ARG, "give both events or neither");
+  g_timing[which][0] = static_cast<cudaEvent_t>(start_event);
+  g_timing[which][1] = static_cast<cudaEvent_t>(stop_event);
+  return MSA_OK;
 }
 
 msa_status msa_selftest_wait_timeout(void* workspace, int32_t limit_us, msa_stream_t stream) {

@@ -67,6 +67,11 @@ int num_sms();
 // Count of kernels launched by the library (msa_kernel_launches).
 void count_launches(int n);
 
+// Caller-owned events recorded around a main kernel (msa_set_timing_events):
+// which = MSA_TIME_INDEX_TOPK, MSA_TIME_SPARSE_FWD or MSA_TIME_BWD.
+void timing_begin(int which, cudaStream_t st);
+void timing_end(int which, cudaStream_t st);
+
 // Launchers (return cudaSuccess or the launch error).
 cudaError_t launch_index_topk(const Prob& p, const void* q_idx, const void* k_idx, int32_t* block_idx, void* ws,
                               const WsLayout& L, cudaStream_t st);

@@ -1287,12 +1287,14 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.scale_idx_log2 = p.scale_idx * kLog2e;
   ba.scale_idx = p.scale_idx;
   ba.kl_weight = kl_weight;
+  timing_begin(MSA_TIME_BWD, st);
   switch (p.hg) {
     case 1: bwd_kernel<1><<<sms, kBwdThreads, BwdLayout<1>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
     case 2: bwd_kernel<2><<<sms, kBwdThreads, BwdLayout<2>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
     case 4: bwd_kernel<4><<<sms, kBwdThreads, BwdLayout<4>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
     default: bwd_kernel<8><<<sms, kBwdThreads, BwdLayout<8>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
   }
+  timing_end(MSA_TIME_BWD, st);
   count_launches(6);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {

@@ -633,12 +633,14 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
         return e;
     attr = true;
   }
+  timing_begin(MSA_TIME_SPARSE_FWD, st);
   switch (p.hg) {
     case 1: sparse_fwd_kernel<1><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
     case 2: sparse_fwd_kernel<2><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
     case 4: sparse_fwd_kernel<4><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
     default: sparse_fwd_kernel<8><<<num_sms(), kThreads, kSmemBytes, st>>>(a, mk, mv, mo, mq); break;
   }
+  timing_end(MSA_TIME_SPARSE_FWD, st);
   count_launches(2);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const long long rows = (long long)p.B * p.T * p.G;

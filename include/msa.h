@@ -267,6 +267,23 @@ MSA_API msa_status msa_check_device_status(const void *workspace, msa_stream_t s
  * wait every kernel uses, without faulting or hanging the GPU. */
 MSA_API msa_status msa_selftest_wait_timeout(void *workspace, int32_t limit_us, msa_stream_t stream);
 
+/* Kernel timing for benchmarks. The main kernel of one stage: */
+enum {
+  MSA_TIME_INDEX_TOPK = 0, /* index_topk_kernel (msa_index_topk, msa_index_topk_fp8, the no-workspace call) */
+  MSA_TIME_SPARSE_FWD = 1, /* sparse_fwd_kernel (msa_sparse_fwd, msa_sparse_fwd_mapped), not the map or merge */
+  MSA_TIME_BWD = 2         /* bwd_kernel (msa_bwd, msa_bwd_mapped), not the pre-passes or merges */
+};
+
+/* While set, every launch of kernel `which` is bracketed by
+ * cudaEventRecord(start_event) and cudaEventRecord(stop_event) on the call's
+ * stream, so that the caller can read the kernel's own duration with
+ * cudaEventElapsedTime. The events are the caller's cudaEvent_t handles (created
+ * with timing enabled, on this device) and stay the caller's; each launch
+ * re-records them. Both NULL stops the recording. The setting is process-wide
+ * and not synchronised between threads. MSA_ERR_INVALID_ARG for an unknown
+ * `which` or for exactly one NULL event. */
+MSA_API msa_status msa_set_timing_events(int32_t which, void *start_event, void *stop_event);
+
 /* Number of kernels this library has launched in the calling process since it
  * was loaded (monotonic; for accounting in benchmarks and tests). */
 MSA_API int64_t msa_kernel_launches(void);

@@ -83,3 +83,13 @@ def test_warmup_selection_validates_before_device_work(lib):
     with pytest.raises(lib.MsaError) as e:
         lib.msa_warmup_block_idx(lib.Shape(B=1, T=1024, Hq=8, G=2, k=8), 0, stream=0)
     assert e.value.status == lib.MSA_ERR_INVALID_ARG and "block_idx" in str(e.value)
+
+
+def test_timing_events_validate_without_device(lib):
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_set_timing_events(3, None, None)
+    assert e.value.status == lib.MSA_ERR_INVALID_ARG
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_set_timing_events(lib.MSA_TIME_BWD, 4096, None)
+    assert e.value.status == lib.MSA_ERR_INVALID_ARG
+    lib.msa_set_timing_events(lib.MSA_TIME_BWD, None, None)  # clearing is always fine
