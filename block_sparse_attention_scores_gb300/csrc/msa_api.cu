@@ -29,11 +29,15 @@ void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed);
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-int num_sms() {
-  static int cached[64] = {0};
+int device_slot() {
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
+  return (dev < 0 || dev >= kMaxDevices) ? 0 : dev;
+}
+
+int num_sms() {
+  static int cached[kMaxDevices] = {0};
+  const int dev = device_slot();
   if (!cached[dev]) {
     int n = 0;
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);

@@ -64,6 +64,11 @@ bool encode_tmap(CUtensorMap* map, void* base, int rank, const uint64_t* dims, c
 
 int num_sms();
 
+// Current device id, clamped to [0, kMaxDevices): index of per-device state
+// such as kernel attributes, which belong to each device's context.
+constexpr int kMaxDevices = 64;
+int device_slot();
+
 // Count of kernels launched by the library (msa_kernel_launches).
 void count_launches(int n);
 

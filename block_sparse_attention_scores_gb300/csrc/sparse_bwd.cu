@@ -1222,8 +1222,9 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if (!encode_tmap(&mdqi, ws + L.dqi_part, 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kMaxDevices] = {};  // kernel attributes are per device context
+  const int dslot = device_slot();
+  if (!attr[dslot]) {
     if ((e = cudaFuncSetAttribute(px_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPxSmem)) !=
         cudaSuccess)
       return e;
@@ -1236,7 +1237,7 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
         (e = cudaFuncSetAttribute(bwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   BwdLayout<8>::kSmem)) != cudaSuccess)
       return e;
-    attr = true;
+    attr[dslot] = true;
   }
   PxArgs pa;
   pa.q_idx = static_cast<const __nv_bfloat16*>(q_idx);

@@ -626,12 +626,13 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
   a.pos_per_tile = pos_per_tile;
   a.scale_log2 = p.scale * kLog2e;
   if ((e = cudaMemsetAsync(a.counter, 0, sizeof(int), st)) != cudaSuccess) return e;
-  static bool attr = false;
-  if (!attr) {
+  static bool attr[kMaxDevices] = {};  // kernel attributes are per device context
+  const int dslot = device_slot();
+  if (!attr[dslot]) {
     for (auto f : {sparse_fwd_kernel<1>, sparse_fwd_kernel<2>, sparse_fwd_kernel<4>, sparse_fwd_kernel<8>})
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes)) != cudaSuccess)
         return e;
-    attr = true;
+    attr[dslot] = true;
   }
   timing_begin(MSA_TIME_SPARSE_FWD, st);
   switch (p.hg) {

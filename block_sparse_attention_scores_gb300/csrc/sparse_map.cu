@@ -285,14 +285,15 @@ cudaError_t build_block_map2(const Prob& p, const int32_t* block_idx, uint8_t* w
   if ((e = cudaMemsetAsync(rev, 0xff, (size_t)p.B * p.G * p.T * p.k * 4, st)) != cudaSuccess) return e;
   const int chunks = p.B * p.G * p.n;  // one per (b, g, query block)
   const int mask_bytes = p.n * 16;     // bitmaps of blocks 0..qb, 128 rows each
-  static int attr_bytes = 0;
-  if (mask_bytes > 48 * 1024 && mask_bytes > attr_bytes) {
+  static int attr_bytes[kMaxDevices] = {};  // kernel attributes are per device context
+  const int dslot = device_slot();
+  if (mask_bytes > 48 * 1024 && mask_bytes > attr_bytes[dslot]) {
     if ((e = cudaFuncSetAttribute(map_chunk_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   mask_bytes)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(map_chunk_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   mask_bytes)) != cudaSuccess)
       return e;
-    attr_bytes = mask_bytes;
+    attr_bytes[dslot] = mask_bytes;
   }
   map_chunk_count_kernel<<<chunks, 128, mask_bytes, st>>>(block_idx, p.T, p.n, p.k, chunk, err);
   map_chunk_scan_kernel<<<(int)std::min<long long>(((long long)lists * 32 + 255) / 256, 16LL * num_sms()), 256, 0,
