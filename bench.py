@@ -57,6 +57,17 @@ def counted_flops(w):
     return dict(index=idx, fwd=fwd, bwd=bwd + kl, total=idx + fwd + bwd + kl)
 
 
+def fwd_algorithmic_bytes(w) -> int:
+    """HBM bytes the forward kernel must move: per (b, g, t, selected block) and
+    head, the gathered Q row (d bf16), the partial O row (d bf16) and the
+    partial LSE (fp32)."""
+    pairs = 0
+    for c in range(w.n_blocks):  # queries of block c keep min(k, c + 1) blocks
+        pairs += w.Bk * min(w.k, c + 1)
+    hg = w.Hq // w.G
+    return pairs * w.B * w.G * hg * (2 * w.d * 2 + 4)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -500,6 +511,16 @@ def run_gpu(args, w):
         dom_flops = stage_flops[dom]
         dom_file = {"index_topk": "index_topk.cu", "sparse_fwd": "sparse_fwd.cu", "bwd": "sparse_bwd.cu"}[dom]
         achieved = dom_flops / (kernel_ms[dom] * 1e-3) / 1e12
+        kernels_line = {kname[n]: {"ms": kernel_ms[n], "tflops": stage_flops[n] / (kernel_ms[n] * 1e-3) / 1e12,
+                                   "frac_bf16_peak": stage_flops[n] / (kernel_ms[n] * 1e-3) / 1e12 / peak_sus}
+                        for n in kernel_ms}
+        # the forward kernel moves, per (query, selected block) and head, a gathered Q row (256 B), a partial
+        # O row (256 B) and a partial LSE (4 B): HBM-bound against the measured copy rate
+        fb = fwd_algorithmic_bytes(w)
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
+        kernels_line["sparse_fwd_kernel"].update({
+            "algorithmic_gb": fb / 1e9, "gbs": fb / (kernel_ms["sparse_fwd"] * 1e-3) / 1e9,
+            "frac_hbm": fb / (kernel_ms["sparse_fwd"] * 1e-3) / 1e9 / hbm})
         tr = traffic_record(dom_file)
         line = {
             "metric": METRIC, "value": aggregate_tokens_per_s(w, world, ms_step), "unit": "tokens/s", "n_gpus": world,
@@ -511,8 +532,7 @@ def run_gpu(args, w):
             "tflops": tflops, "frac_bf16_peak": tflops / peak_sus,
             "fwd_tokens_per_s": tokens / ((pm["index_topk"] + pm["sparse_fwd"]) * 1e-3),
             "phases_ms": pm,
-            "kernels": {kname[n]: {"ms": kernel_ms[n], "tflops": stage_flops[n] / (kernel_ms[n] * 1e-3) / 1e12}
-                        for n in kernel_ms},
+            "kernels": kernels_line,
             "counted_flops_per_step": fl["total"] * world,
             "roofline": {"kernel": f"{kname[dom]} ({dom_file}), CUDA events around each launch",
                          "bound": "tensor", "achieved": achieved,

@@ -31,3 +31,14 @@ def test_selected_pairs_equal_a_direct_count():
             if c >= 0:
                 direct += min(w.Bk, row_t - c * w.Bk + 1)
     assert direct == bench.n_selected(w)
+
+
+def test_forward_algorithmic_bytes_closed_form():
+    import bench
+
+    for w in (synth.CONFIGS[1], synth.CONFIGS[3], synth.CONFIGS[0].with_(T=640, k=8)):
+        n, k, hg = w.n_blocks, w.k, w.Hq // w.G
+        # queries of block c keep min(k, c + 1) blocks: k(k+1)/2 + (n - k) k pairs per query row of a block when n >= k
+        per = k * (k + 1) // 2 + (n - k) * k if n >= k else n * (n + 1) // 2
+        pairs = w.Bk * per * w.B * w.G
+        assert bench.fwd_algorithmic_bytes(w) == pairs * hg * (2 * w.d * 2 + 4)
