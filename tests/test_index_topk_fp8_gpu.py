@@ -91,3 +91,26 @@ def test_index_topk_fp8_exact_ties(msa, cfg):
     bad = int((got != want).any(axis=-1).sum())
     print(f"{cfg.name}: rows={want.shape[0] * want.shape[2]} tied at the boundary={(gap == 0).sum()} mismatches={bad}")
     assert bad == 0
+
+
+@pytest.mark.parametrize("cfg_id,n_per_group", [(3, 64), (4, 24)])
+def test_index_topk_fp8_large_configs_sampled(msa, cfg_id, n_per_group):
+    """The full-size workloads (T = 131072 and T = 2^20), in the launch
+    configuration the bench times: sampled rows (first and last positions,
+    block edges, random positions) against the oracle's FP8 selection."""
+    w = synth.CONFIGS[cfg_id]
+    inp, got = _run(msa, w)
+    rng = np.random.default_rng(100 + cfg_id)
+    rows = []
+    for b in range(w.B):
+        for g in range(w.G):
+            t = np.concatenate([np.arange(0, 3), np.arange(w.T - 3, w.T), rng.integers(0, w.T, n_per_group),
+                                ((rng.integers(1, w.n_blocks, 8) * w.Bk)[:, None] + np.array([-1, 0])).ravel()])
+            rows.append((b * w.G + g) * w.T + np.unique(t))
+    rows = np.concatenate(rows)
+    b, g, t = rows // (w.G * w.T), (rows // w.T) % w.G, rows % w.T
+    valid_selection(got[:, :, : min(w.T, 4096)], min(w.T, 4096), w.Bk)
+    want, gap, _ = oracle.index_topk_fp8(oracle.shape_of(w), inp["q_idx"], inp["k_idx"], rows=rows)
+    n, ties, bad, bad_tie = compare_block_idx(got[b, g, t], want, gap)
+    print(f"config{cfg_id}: sampled rows={n} near_ties={ties} mismatches(outside ties)={bad} (in ties)={bad_tie}")
+    assert bad == 0
