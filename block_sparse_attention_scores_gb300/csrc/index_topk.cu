@@ -17,10 +17,11 @@
 // its block max with 127 fmax and inserts (max, c) into a register top-(k-1).
 // The own block needs no score: it is always kept.
 //
-// Warp roles (192 threads, 2 CTAs per SM, persistent over work items handed
+// Warp roles (192 threads, 2 CTAs per SM or 4 (below), persistent over work items handed
 // out largest-qb-first by an atomic counter):
 //   warp 0      TMA producer: q tile per item, k_idx tiles into a 4-stage ring
 //   warp 1      TMEM owner and UMMA issuer (one thread), 2 accumulators
+//               (FP8 with k <= 17: 1 accumulator, 4 CTAs per SM)
 //   warps 2..5  epilogue: tcgen05.ld, block max, running top-k, output
 #include <cuda_fp8.h>
 
@@ -34,6 +35,13 @@ constexpr int kThreads = 192;
 constexpr int kStages = 4;
 constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16 (the FP8 path uses half of each tile)
 constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
+constexpr int kSmem8 = (2 + kStages) * (kTileBytes / 2) + 1024;  // FP8: 8 KB tiles
+// CTAs per SM. FP8 with a short top-k list (k <= 17) runs four CTAs per SM
+// with one TMEM accumulator each: 16 epilogue warps per SM instead of 8, since
+// the epilogue, not the MMA, sets the pace; longer lists need the registers
+// of two CTAs per SM.
+template <int CAP, bool FP8>
+__host__ __device__ constexpr int topk_ctas() { return (FP8 && CAP <= 16) ? 4 : 2; }
 
 struct TopkArgs {
   int B, T, G, n, k;
@@ -90,13 +98,15 @@ __device__ __forceinline__ void topk_insert(float (&val)[CAP], int (&idx)[CAP], 
 // row's own scale is positive and common to all its blocks: it cannot change
 // the selection).
 template <int CAP, bool FP8>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, topk_ctas<CAP, FP8>())
     index_topk_kernel(TopkArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
   constexpr int kLoadBytes = FP8 ? kTileBytes / 2 : kTileBytes;  // bytes a q or k tile load brings
+  constexpr int kTB = kLoadBytes;                                 // stage spacing in shared memory
+  constexpr int NACC = topk_ctas<CAP, FP8>() == 4 ? 1 : 2;        // TMEM accumulators (128 columns each)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;                   // 2 x 16 KB
-  uint8_t* sK = smem + 2 * kTileBytes;  // kStages x 16 KB
+  uint8_t* sQ = smem;           // 2 q tiles
+  uint8_t* sK = smem + 2 * kTB;  // kStages k tiles
   __shared__ TopkShared sh;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -117,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sh.tmem_base, 256);
+    tmem_alloc(&sh.tmem_base, NACC * 128);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -145,13 +155,13 @@ __global__ void __launch_bounds__(kThreads, 2)
         decode_item(item, a.B, a.G, a.n, b, g, qb);
         if (!mbar_wait(&sh.q_empty[s], ph ^ 1, a.err, 102)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&sh.q_full[s], kLoadBytes);
-        tma_load_3d(sQ + s * kTileBytes, &map_q, &sh.q_full[s], 0, g, b * a.T + qb * 128);
+        tma_load_3d(sQ + s * kTB, &map_q, &sh.q_full[s], 0, g, b * a.T + qb * 128);
         bool ok = true;
         for (int c = 0; c < qb; ++c, ++kc) {
           const int st = kc % kStages;
           if (!mbar_wait(&sh.k_empty[st], ((kc / kStages) & 1) ^ 1, a.err, 103)) { ok = false; break; }
           mbar_arrive_expect_tx(&sh.k_full[st], kLoadBytes);
-          tma_load_2d(sK + st * kTileBytes, &map_k, &sh.k_full[st], 0, b * a.T + c * 128);
+          tma_load_2d(sK + st * kTB, &map_k, &sh.k_full[st], 0, b * a.T + c * 128);
         }
         if (!ok) { *abort_flag = 1; break; }
       }
@@ -172,15 +182,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         decode_item(item, a.B, a.G, a.n, b, g, qb);
         if (!mbar_wait(&sh.q_full[s], ph, a.err, 112)) { *abort_flag = 1; break; }
         tc_fence_after();
-        const uint32_t qaddr = smem_u32(sQ + s * kTileBytes);
+        const uint32_t qaddr = smem_u32(sQ + s * kTB);
         bool ok = true;
         for (int c = 0; c < qb; ++c, ++kc, ++ac) {
           const int st = kc % kStages;
-          const int ab = ac & 1;
+          const int ab = ac % NACC;
           if (!mbar_wait(&sh.k_full[st], (kc / kStages) & 1, a.err, 113)) { ok = false; break; }
-          if (!mbar_wait(&sh.acc_empty[ab], ((ac >> 1) & 1) ^ 1, a.err, 114)) { ok = false; break; }
+          if (!mbar_wait(&sh.acc_empty[ab], ((ac / NACC) & 1) ^ 1, a.err, 114)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t kaddr = smem_u32(sK + st * kTileBytes);
+          const uint32_t kaddr = smem_u32(sK + st * kTB);
           if constexpr (FP8) {
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {  // K = 64 bytes = 2 x 32 E4M3 values
@@ -228,8 +238,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       bool ok = true;
       for (int c = 0; c < qb; ++c, ++ac) {
-        const int ab = ac & 1;
-        if (!mbar_wait(&sh.acc_full[ab], (ac >> 1) & 1, a.err, 122)) { ok = false; break; }
+        const int ab = ac % NACC;
+        if (!mbar_wait(&sh.acc_full[ab], (ac / NACC) & 1, a.err, 122)) { ok = false; break; }
         tc_fence_after();
         float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
@@ -282,18 +292,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tmem, 256);
+  if (warp == 1) tmem_dealloc(tmem, NACC * 128);
 }
 
 template <int CAP, bool FP8>
 cudaError_t launch_cap(const Prob& p, const TopkArgs& args, const CUtensorMap& mq, const CUtensorMap& mk,
                        cudaStream_t st) {
   auto kern = index_topk_kernel<CAP, FP8>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  constexpr int smem_bytes = FP8 ? kSmem8 : kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  const int grid = min(args.num_items, 2 * num_sms());
+  const int grid = min(args.num_items, topk_ctas<CAP, FP8>() * num_sms());
   timing_begin(MSA_TIME_INDEX_TOPK, st);
-  kern<<<grid, kThreads, kSmemBytes, st>>>(args, mq, mk);
+  kern<<<grid, kThreads, smem_bytes, st>>>(args, mq, mk);
   timing_end(MSA_TIME_INDEX_TOPK, st);
   count_launches(1);
   return cudaGetLastError();
