@@ -147,7 +147,7 @@ static msa_status validate(const msa_shape* s, Prob* p) {
     return fail(MSA_ERR_UNSUPPORTED, "Hq/G=%d: heads per group must be 1, 2, 4 or 8", hg);
   if (s->T % 128) return fail(MSA_ERR_UNSUPPORTED, "T=%d is not a multiple of 128", s->T);
   if (s->T > (1 << 20)) return fail(MSA_ERR_UNSUPPORTED, "T=%d exceeds 2^20", s->T);
-  if (s->k > 64) return fail(MSA_ERR_UNSUPPORTED, "k=%d exceeds 64", s->k);
+  if (s->k > 128) return fail(MSA_ERR_UNSUPPORTED, "k=%d exceeds 128", s->k);
   if ((long long)s->B * s->T > (1LL << 30)) return fail(MSA_ERR_UNSUPPORTED, "B*T too large");
   const float sc = s->scale > 0 ? s->scale : 1.0f / sqrtf((float)s->d);
   const float sci = s->scale_idx > 0 ? s->scale_idx : 1.0f / sqrtf((float)s->d_idx);
@@ -165,6 +165,12 @@ static msa_status validate(const msa_shape* s, Prob* p) {
   p->n = s->T / s->Bk;
   p->scale = sc;
   p->scale_idx = sci;
+  return MSA_OK;
+}
+
+// The index top-k keeps its list in registers: at most 64 blocks per row.
+static msa_status check_topk_k(const Prob& p) {
+  if (p.k > 64) return fail(MSA_ERR_UNSUPPORTED, "index top-k keeps at most 64 blocks (k=%d)", p.k);
   return MSA_OK;
 }
 
@@ -224,6 +230,7 @@ size_t msa_workspace_size(const msa_shape* shape, int which) {
   Prob p;
   if (which < MSA_WS_TOPK || which > MSA_WS_TOPK_FP8) return 0;
   if (validate(shape, &p) != MSA_OK) return 0;
+  if ((which == MSA_WS_TOPK || which == MSA_WS_TOPK_FP8) && p.k > 64) return 0;
   return ws_layout(p, which).total;
 }
 
@@ -233,6 +240,7 @@ msa_status msa_index_topk(const msa_shape* shape, const void* q_idx, const void*
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_topk_k(p)) != MSA_OK) return s;
   if ((s = check_ptr(q_idx, "q_idx", 16)) != MSA_OK) return s;
   if ((s = check_ptr(k_idx, "k_idx", 16)) != MSA_OK) return s;
   if ((s = check_ptr(block_idx, "block_idx", 16)) != MSA_OK) return s;
@@ -250,6 +258,7 @@ msa_status msa_index_topk_fp8(const msa_shape* shape, const void* q_idx, const v
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_topk_k(p)) != MSA_OK) return s;
   if ((s = check_ptr(q_idx, "q_idx", 16)) != MSA_OK) return s;
   if ((s = check_ptr(k_idx, "k_idx", 16)) != MSA_OK) return s;
   if ((s = check_ptr(block_idx, "block_idx", 16)) != MSA_OK) return s;
@@ -443,6 +452,7 @@ extern "C" msa_status msa_index_topk_noalloc(const msa_shape* shape, const void*
   Prob p;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
+  if ((s = check_topk_k(p)) != MSA_OK) return s;
   if ((s = check_ptr(q_idx, "q_idx", 16)) != MSA_OK) return s;
   if ((s = check_ptr(k_idx, "k_idx", 16)) != MSA_OK) return s;
   if ((s = check_ptr(block_idx, "block_idx", 16)) != MSA_OK) return s;

@@ -1081,7 +1081,7 @@ __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&
 // (dQ: HG contiguous rows entry*HG + h; dq_idx: row entry); KL partials at
 // (b, t, g, slot). One warp per (b, t, g); every lane owns 4 * HG consecutive
 // dQ values and 2 dq_idx values.
-template <int HG>
+template <int HG, int NSL>  // NSL slots per lane: k <= 32 NSL
 __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
                                  const __nv_bfloat16* __restrict__ dq_part, const __nv_bfloat16* __restrict__ dqi_part,
                                  const float* __restrict__ kl_part, float* __restrict__ dQ,
@@ -1096,10 +1096,10 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
     const long long bt = w / G;
     const int t = (int)(bt % T), b = (int)(bt / T);
     const size_t sel_row = (((size_t)b * G + g) * T + t) * k;
-    int rv_own[2];
+    int rv_own[NSL];
     float kl_own = 0.f;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < NSL; ++u) {
       const int sidx = lane + 32 * u;
       int r = -1;
       if (sidx < k && block_idx[sel_row + sidx] >= 0) {
@@ -1114,7 +1114,7 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
     for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
     float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < NSL; ++u) {
       for (int src = 0; src < 32 && 32 * u + src < k; ++src) {
         const int r = __shfl_sync(0xffffffffu, rv_own[u], src);
         if (r < 0) continue;
@@ -1153,6 +1153,18 @@ __global__ void dki_merge_kernel(const float* __restrict__ dki_part, float* __re
     }
     *reinterpret_cast<float2*>(dk_idx + bt * 64 + e2 * 2) = make_float2(s0, s1);
   }
+}
+
+// Two slots per lane up to k = 64, four up to k = 128.
+template <int HG>
+void bwd_merge(const Prob& p, const int32_t* block_idx, const int32_t* rev, const BwdArgs& ba, float* dQ,
+               float* dq_idx, float* KL, long long max_padded, int grid, cudaStream_t st) {
+  if (p.k <= 64)
+    bwd_merge_kernel<HG, 2><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQ, dq_idx, KL,
+                                                   p.B, p.T, p.Hq, p.G, p.k, max_padded);
+  else
+    bwd_merge_kernel<HG, 4><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQ, dq_idx, KL,
+                                                   p.B, p.T, p.Hq, p.G, p.k, max_padded);
 }
 
 }  // namespace
@@ -1304,10 +1316,10 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     float* dQf = static_cast<float*>(dQ);
     float* dqif = static_cast<float*>(dq_idx);
     switch (p.hg) {
-      case 1: bwd_merge_kernel<1><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-      case 2: bwd_merge_kernel<2><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-      case 4: bwd_merge_kernel<4><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-      default: bwd_merge_kernel<8><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQf, dqif, KL, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+      case 1: bwd_merge<1>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
+      case 2: bwd_merge<2>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
+      case 4: bwd_merge<4>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
+      default: bwd_merge<8>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
     }
   }
   const long long n2 = (long long)p.B * p.T * 32;

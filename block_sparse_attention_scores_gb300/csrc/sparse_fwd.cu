@@ -490,7 +490,7 @@ __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&
 // memory; every lane then owns 4 * HG consecutive output values (head
 // lane / (32 / HG)) and sums the partial rows with one shared load per slot.
 constexpr int kMergeThreads = 256;
-template <int HG>
+template <int HG, int NSL>  // NSL slots per lane: k <= 32 NSL
 __global__ void __launch_bounds__(kMergeThreads)
     fwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
                      const __nv_bfloat16* __restrict__ o_part, const float* __restrict__ lse_part,
@@ -498,8 +498,8 @@ __global__ void __launch_bounds__(kMergeThreads)
                      long long max_padded) {
   constexpr int kPer = 4 * HG;  // output values per lane
   constexpr int kLanesPerHead = 32 / HG;
-  __shared__ int s_row[kMergeThreads / 32][64];
-  __shared__ float s_wgt[kMergeThreads / 32][64][HG];
+  __shared__ int s_row[kMergeThreads / 32][32 * NSL];
+  __shared__ float s_wgt[kMergeThreads / 32][32 * NSL][HG];
   const long long rows = (long long)B * T * G;
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int my_head = lane / kLanesPerHead;
@@ -511,10 +511,10 @@ __global__ void __launch_bounds__(kMergeThreads)
     const size_t sel_row = (((size_t)b * G + g) * T + t) * k;
     // a slot counts only if the map placed it (rows that failed validation
     // keep -1 and are left unspecified, with the error word set)
-    float l_own[2][HG];
-    int rv_own[2];
+    float l_own[NSL][HG];
+    int rv_own[NSL];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < NSL; ++u) {
       const int sidx = lane + 32 * u;
       int r = -1;
       if (sidx < k && block_idx[sel_row + sidx] >= 0) {
@@ -528,17 +528,20 @@ __global__ void __launch_bounds__(kMergeThreads)
     float lse[HG];
 #pragma unroll
     for (int h = 0; h < HG; ++h) {
-      float mx = fmaxf(l_own[0][h], l_own[1][h]);
+      float mx = l_own[0][h];
+#pragma unroll
+      for (int u = 1; u < NSL; ++u) mx = fmaxf(mx, l_own[u][h]);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      float z = (l_own[0][h] > -INFINITY ? expf(l_own[0][h] - mx) : 0.f) +
-                (l_own[1][h] > -INFINITY ? expf(l_own[1][h] - mx) : 0.f);
+      float z = 0.f;
+#pragma unroll
+      for (int u = 0; u < NSL; ++u) z += l_own[u][h] > -INFINITY ? expf(l_own[u][h] - mx) : 0.f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
       lse[h] = mx + logf(z);
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < NSL; ++u) {
       const int sidx = lane + 32 * u;
       if (sidx < k) {
         s_row[wib][sidx] = rv_own[u];
@@ -573,6 +576,18 @@ __global__ void __launch_bounds__(kMergeThreads)
       LSE[orow0 + lane] = v;
     }
   }
+}
+
+// Two slots per lane up to k = 64, four up to k = 128.
+template <int HG>
+void fwd_merge(const Prob& p, const int32_t* block_idx, const int32_t* rev, const __nv_bfloat16* o_part,
+               const float* lse_part, __nv_bfloat16* O, float* LSE, long long max_padded, int grid, cudaStream_t st) {
+  if (p.k <= 64)
+    fwd_merge_kernel<HG, 2><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, o_part, lse_part, O, LSE, p.B, p.T, p.Hq,
+                                                             p.G, p.k, max_padded);
+  else
+    fwd_merge_kernel<HG, 4><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, o_part, lse_part, O, LSE, p.B, p.T, p.Hq,
+                                                             p.G, p.k, max_padded);
 }
 
 }  // namespace
@@ -649,10 +664,10 @@ cudaError_t launch_sparse_fwd(const Prob& p, const void* Q, const void* K, const
   const int32_t* rev = reinterpret_cast<const int32_t*>(ws + L.rev);
   __nv_bfloat16* Ob = static_cast<__nv_bfloat16*>(O);
   switch (p.hg) {
-    case 1: fwd_merge_kernel<1><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-    case 2: fwd_merge_kernel<2><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-    case 4: fwd_merge_kernel<4><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
-    default: fwd_merge_kernel<8><<<grid, kMergeThreads, 0, st>>>(block_idx, rev, a.o_part, a.lse_part, Ob, LSE, p.B, p.T, p.Hq, p.G, p.k, L.max_padded); break;
+    case 1: fwd_merge<1>(p, block_idx, rev, a.o_part, a.lse_part, Ob, LSE, L.max_padded, grid, st); break;
+    case 2: fwd_merge<2>(p, block_idx, rev, a.o_part, a.lse_part, Ob, LSE, L.max_padded, grid, st); break;
+    case 4: fwd_merge<4>(p, block_idx, rev, a.o_part, a.lse_part, Ob, LSE, L.max_padded, grid, st); break;
+    default: fwd_merge<8>(p, block_idx, rev, a.o_part, a.lse_part, Ob, LSE, L.max_padded, grid, st); break;
   }
   return cudaGetLastError();
 }

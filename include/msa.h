@@ -40,8 +40,11 @@
  *   Head h belongs to group h / (Hq / G).
  * - Supported shapes (MSA_ERR_UNSUPPORTED otherwise): d = 128, d_idx = 64,
  *   Bk = 128, Hq / G in {1, 2, 4, 8} with Hq % G == 0, T % 128 == 0,
- *   1 <= T <= 2^20, 1 <= k <= 64, B >= 1, scale and scale_idx > 0 after
- *   defaulting. Kernels need an sm_100-family GPU (built for sm_103a).
+ *   1 <= T <= 2^20, 1 <= k <= 128, B >= 1, scale and scale_idx > 0 after
+ *   defaulting; the index top-k (msa_index_topk, msa_index_topk_fp8,
+ *   msa_index_topk_noalloc, and the MSA_WS_TOPK / MSA_WS_TOPK_FP8 workspace
+ *   sizes) keeps at most k = 64 blocks per row. Kernels need an sm_100-family
+ *   GPU (built for sm_103a).
  * - Device-side checks (bounded waits, block ids out of range) write an error
  *   word in the workspace; msa_check_device_status() reads it.
  */
@@ -247,7 +250,7 @@ MSA_API msa_status msa_bwd_mapped(const msa_shape *shape, const void *Q, const v
  * msa_bwd the KL of the index branch against the dense teacher (the head mean
  * of the full attention weights) over every visible token, with its gradients
  * to q_idx and k_idx. No index scores are computed and no workspace is used.
- * MSA_ERR_UNSUPPORTED unless k >= T / Bk (so at most T = 64 * Bk). */
+ * MSA_ERR_UNSUPPORTED unless k >= T / Bk (so at most T = 128 * Bk). */
 MSA_API msa_status msa_warmup_block_idx(const msa_shape *shape, int32_t *block_idx, msa_stream_t stream);
 
 /* Message describing the last non-OK status returned on this thread. */

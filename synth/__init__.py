@@ -253,7 +253,7 @@ def synthetic_block_idx(w: Workload, seed_offset: int = 0) -> np.ndarray:
         chosen = np.empty((r.size, kk), dtype=np.int64)
         for i in range(kk):
             j = C - kk + i
-            h = hash_at(key, r.astype(np.uint64) * np.uint64(64) + np.uint64(i))
+            h = hash_at(key, r.astype(np.uint64) * np.uint64(max(64, k)) + np.uint64(i))
             cand = (h % (j + 1).astype(np.uint64)).astype(np.int64)
             dup = (chosen[:, :i] == cand[:, None]).any(axis=1) if i else np.zeros(r.size, bool)
             chosen[:, i] = np.where(dup, j, cand)

@@ -47,7 +47,7 @@ def test_workspace_sizes(lib):
     assert lib.msa_workspace_size(s, 7) == 0
 
 
-@pytest.mark.parametrize("kw", [dict(d=64), dict(d_idx=32), dict(Bk=64), dict(T=1000), dict(k=65),
+@pytest.mark.parametrize("kw", [dict(d=64), dict(d_idx=32), dict(Bk=64), dict(T=1000), dict(k=129),
                                 dict(Hq=12, G=4), dict(Hq=7, G=2), dict(T=0), dict(B=0), dict(T=(1 << 20) + 128)])
 def test_unsupported_shapes_have_no_workspace(lib, kw):
     base = dict(B=1, T=1024, Hq=8, G=2, k=4)
@@ -93,3 +93,19 @@ def test_timing_events_validate_without_device(lib):
         lib.msa_set_timing_events(lib.MSA_TIME_BWD, 4096, None)
     assert e.value.status == lib.MSA_ERR_INVALID_ARG
     lib.msa_set_timing_events(lib.MSA_TIME_BWD, None, None)  # clearing is always fine
+
+
+def test_selection_width_limits(lib):
+    # the forward and backward take up to 128 blocks per row; the index top-k keeps at most 64
+    s = lib.Shape(B=1, T=16384, Hq=8, G=2, k=128)
+    assert lib.msa_workspace_size(s, lib.MSA_WS_BWD) > 0
+    assert lib.msa_workspace_size(s, lib.MSA_WS_FWD) > 0
+    assert lib.msa_workspace_size(s, lib.MSA_WS_TOPK) == 0
+    assert lib.msa_workspace_size(s, lib.MSA_WS_TOPK_FP8) == 0
+    assert lib.msa_workspace_size(lib.Shape(B=1, T=16384, Hq=8, G=2, k=64), lib.MSA_WS_TOPK) > 0
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_index_topk(s, 4096, 4096, 4096, 4096, stream=0, workspace_bytes=1 << 30)
+    assert e.value.status == lib.MSA_ERR_UNSUPPORTED and "at most 64" in str(e.value)
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_index_topk_fp8(s, 4096, 4096, 4096, 4096, stream=0, workspace_bytes=1 << 30)
+    assert e.value.status == lib.MSA_ERR_UNSUPPORTED
