@@ -102,3 +102,22 @@ def test_fp8_selection_equals_bf16_selection_on_the_e4m3_grid():
     bi8, _, _ = oracle.index_topk_fp8(s, qb, kb)
     bi16, _, _ = oracle.index_topk(s, qb, kb)
     assert np.array_equal(bi8, bi16)
+
+
+def test_all_zero_row_and_block_quantize_with_scale_one_and_tie_to_lowest_blocks():
+    # amax = 0: scale 1 and zero codes; a zero query row scores 0 against every
+    # block, so the tie rule alone decides: the own block plus the lowest ids
+    w = synth.CONFIGS[0].with_(T=1024, k=4)
+    inp = synth.make_inputs(w, which=("q_idx", "k_idx"))
+    q = inp["q_idx"].copy()
+    k = inp["k_idx"].copy()
+    q[0, 700, 1] = 0  # bf16 +0 bits
+    k[0, 256:384] = 0  # key block 2
+    s = oracle.shape_of(w)
+    q_deq, k_deq, sq, sk = oracle.quantize_fp8(s, q, k)
+    assert sq[0, 700, 1] == 1.0 and np.all(q_deq[0, 700, 1] == 0.0)
+    assert sk[0, 2] == 1.0 and np.all(k_deq[0, 256:384] == 0.0)
+    bi, gap, _ = oracle.index_topk_fp8(s, q, k)
+    row = bi.reshape(w.B, w.G, w.T, w.k)[0, 1, 700]
+    assert row.tolist() == [0, 1, 2, 700 // w.Bk]
+    assert gap.reshape(w.B, w.G, w.T)[0, 1, 700] == 0.0
