@@ -227,7 +227,7 @@ int64_t msa_kernel_launches(void) { return g_launches.load(std::memory_order_rel
 const char* msa_last_error(void) { return g_err; }
 
 size_t msa_workspace_size(const msa_shape* shape, int which) {
-  Prob p;
+  Prob p{};
   if (which < MSA_WS_TOPK || which > MSA_WS_TOPK_FP8) return 0;
   if (validate(shape, &p) != MSA_OK) return 0;
   if ((which == MSA_WS_TOPK || which == MSA_WS_TOPK_FP8) && p.k > 64) return 0;
@@ -236,7 +236,7 @@ size_t msa_workspace_size(const msa_shape* shape, int which) {
 
 msa_status msa_index_topk(const msa_shape* shape, const void* q_idx, const void* k_idx, int32_t* block_idx,
                           void* workspace, size_t workspace_bytes, msa_stream_t stream) {
-  Prob p;
+  Prob p{};
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
@@ -254,7 +254,7 @@ msa_status msa_index_topk(const msa_shape* shape, const void* q_idx, const void*
 
 msa_status msa_index_topk_fp8(const msa_shape* shape, const void* q_idx, const void* k_idx, int32_t* block_idx,
                               void* workspace, size_t workspace_bytes, msa_stream_t stream) {
-  Prob p;
+  Prob p{};
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
@@ -273,7 +273,7 @@ msa_status msa_index_topk_fp8(const msa_shape* shape, const void* q_idx, const v
 static msa_status sparse_fwd_impl(const msa_shape* shape, const void* Q, const void* K, const void* V,
                                   const int32_t* block_idx, void* O, float* LSE, void* workspace,
                                   size_t workspace_bytes, msa_stream_t stream, bool mapped) {
-  Prob p;
+  Prob p{};
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
@@ -309,7 +309,7 @@ static msa_status bwd_impl(const msa_shape* shape, const void* Q, const void* K,
                            const int32_t* block_idx, float kl_weight, float* dQ, float* dK, float* dV, float* dq_idx,
                            float* dk_idx, float* KL, void* workspace, size_t workspace_bytes, msa_stream_t stream,
                            bool mapped) {
-  Prob p;
+  Prob p{};
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
@@ -349,7 +349,7 @@ msa_status msa_bwd_mapped(const msa_shape* shape, const void* Q, const void* K, 
 
 msa_status msa_block_map(const msa_shape* shape, const int32_t* block_idx, void* workspace, size_t workspace_bytes,
                          msa_stream_t stream) {
-  Prob p;
+  Prob p{};
   WsLayout L;
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
@@ -366,7 +366,7 @@ msa_status msa_block_map(const msa_shape* shape, const int32_t* block_idx, void*
 }
 
 msa_status msa_warmup_block_idx(const msa_shape* shape, int32_t* block_idx, msa_stream_t stream) {
-  Prob p;
+  Prob p{};
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
   if (p.k < p.n)
@@ -449,7 +449,7 @@ msa_status noalloc_scratch(void** out) {
 
 extern "C" msa_status msa_index_topk_noalloc(const msa_shape* shape, const void* q_idx, const void* k_idx,
                                              int32_t* block_idx, int32_t check, msa_stream_t stream) {
-  Prob p;
+  Prob p{};
   msa_status s;
   if ((s = validate(shape, &p)) != MSA_OK) return s;
   if ((s = check_topk_k(p)) != MSA_OK) return s;
