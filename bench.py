@@ -57,15 +57,21 @@ def counted_flops(w):
     return dict(index=idx, fwd=fwd, bwd=bwd + kl, total=idx + fwd + bwd + kl)
 
 
-def fwd_algorithmic_bytes(w) -> int:
-    """HBM bytes the forward kernel must move: per (b, g, t, selected block) and
-    head, the gathered Q row (d bf16), the partial O row (d bf16) and the
-    partial LSE (fp32)."""
-    pairs = 0
-    for c in range(w.n_blocks):  # queries of block c keep min(k, c + 1) blocks
-        pairs += w.Bk * min(w.k, c + 1)
-    hg = w.Hq // w.G
-    return pairs * w.B * w.G * hg * (2 * w.d * 2 + 4)
+def algorithmic_bytes(w) -> dict:
+    """HBM bytes each entry point must move at least: every input read once and
+    every output written once, in the library's storage types (bf16 inputs and
+    O; int32 block_idx; fp32 LSE, KL and gradients)."""
+    bt, hq, G, d, E, k = w.B * w.T, w.Hq, w.G, w.d, w.d_idx, w.k
+    q = bt * hq * d * 2            # Q, dO, O (bf16)
+    kv = bt * G * d * 2            # K, V (bf16)
+    qi, ki = bt * G * E * 2, bt * E * 2
+    bi = bt * G * k * 4
+    lse = bt * hq * 4
+    index = qi + ki + bi
+    fwd = q + 2 * kv + bi + q + lse
+    bwd = (q + 2 * kv + q + q + lse + qi + ki + bi     # Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx
+           + 2 * q + 2 * (2 * kv) + 2 * qi + 2 * ki + bt * G * 4)  # dQ, dK, dV, dq_idx, dk_idx (fp32), KL
+    return dict(index=index, fwd=fwd, bwd=bwd, total=index + fwd + bwd)
 
 
 def measured_peaks():
@@ -220,6 +226,35 @@ def oracle_sample(w, seconds: float, seed: int = 0):
             f"{c} (selected {E} times) through the per-block backward; whole step extrapolated by row and "
             f"selection counts ({t_rows + t_block:.1f} s measured)")
     return w.B * w.T / total, desc, oracle.num_threads()
+
+
+def selection_check(w, host, rows, got, tie_eps=1e-4):
+    """The step's block_idx on sampled rows (b, g, t) against the oracle's
+    selection from the same seeded q_idx, k_idx: bit-exact except rows whose
+    oracle k-th / (k+1)-th pooled scores are closer than tie_eps (counted)."""
+    import numpy as np
+
+    import oracle
+
+    want, gap, _ = oracle.index_topk(oracle.shape_of(w), host["q_idx"], host["k_idx"], rows=rows)
+    diff = np.any(np.asarray(got) != want, axis=1)
+    tie = gap < tie_eps
+    return {"rows": int(len(rows)), "near_ties": int(tie.sum()), "mismatch_outside_ties": int((diff & ~tie).sum()),
+            "mismatch_in_ties": int((diff & tie).sum()), "tie_eps": tie_eps,
+            "note": "192 random rows plus the last 64 queries of group 0, batch 0, compared with oracle steps 1-3"}
+
+
+def oracle_single_thread(w, seconds: float):
+    """The same oracle sample as the cpu_baseline, on one host thread."""
+    import oracle
+
+    n = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        v, desc, _ = oracle_sample(w, seconds, seed=1)
+    finally:
+        oracle.set_num_threads(n)
+    return v, desc
 
 
 def run_reference(args, w):
@@ -443,6 +478,22 @@ def run_gpu(args, w):
     torch.cuda.synchronize()
     e2e_ms = dist_max(f0.elapsed_time(f1) / args.steps, dev)
     msa.msa_check_device_status(ws, stream)
+    # the same host->device copies by themselves: this box's pinned-copy rate
+    torch.cuda.synchronize()
+    c0 = torch.cuda.Event(enable_timing=True)
+    c1 = torch.cuda.Event(enable_timing=True)
+    c0.record(s_in)
+    for i in range(args.steps):
+        with torch.cuda.stream(s_in):
+            for n in h_in:
+                d_e2e[i & 1][n].copy_(h_in[n], non_blocking=True)
+    c1.record(s_in)
+    torch.cuda.synchronize()
+    h2d_ms = c0.elapsed_time(c1) / args.steps
+    # rows of this step's selection for the sampled check against the oracle (rank 0, after timing)
+    sel_rows = np.random.default_rng(7).integers(0, w.B * w.G * w.T, 192)
+    sel_rows = np.concatenate([sel_rows, np.arange(w.T - 64, w.T)])  # the last queries see every block
+    sel_got = bi.reshape(-1, w.k)[torch.from_numpy(sel_rows).to(dev)].cpu().numpy()
 
     # ---- FP8 index top-k (E4M3 copies of q_idx and k_idx, kind::f8f6f4 MMAs) on the same inputs
     ws8 = msa.alloc_workspace(s, msa.MSA_WS_TOPK_FP8, dev)
@@ -499,29 +550,36 @@ def run_gpu(args, w):
 
     if rank == 0:
         fl = counted_flops(w)
+        ab = algorithmic_bytes(w)
         peaks, src = measured_peaks()
         tokens = w.B * w.T * world
         tflops = fl["total"] / (ms_step * 1e-3) / 1e12
         pm = {k: statistics.mean(v) for k, v in phase.items()}
-        peak_sus = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+        # Denominators: the burst bf16 figure (a kernel or a step of tens of ms at full SM clock), with the
+        # sustained one (seconds of back-to-back GEMMs under the power cap) reported beside it.
+        peak = float(peaks.get("bf16_tflops", 1900.0))
+        peak_sus = float(peaks.get("bf16_tflops_sustained", peak))
+        hbm = float(peaks.get("hbm_gbs", 6800.0))
         # dominant kernel of the step, timed alone (events recorded by the library around its launches)
         stage_flops = {"index_topk": fl["index"], "sparse_fwd": fl["fwd"], "bwd": fl["bwd"]}
+        stage_bytes = {"index_topk": ab["index"], "sparse_fwd": ab["fwd"], "bwd": ab["bwd"]}
         kname = {"index_topk": "index_topk_kernel", "sparse_fwd": "sparse_fwd_kernel", "bwd": "bwd_kernel"}
+        kfile = {"index_topk": "index_topk.cu", "sparse_fwd": "sparse_fwd.cu", "bwd": "sparse_bwd.cu"}
         dom = max(kernel_ms, key=kernel_ms.get)
-        dom_flops = stage_flops[dom]
-        dom_file = {"index_topk": "index_topk.cu", "sparse_fwd": "sparse_fwd.cu", "bwd": "sparse_bwd.cu"}[dom]
-        achieved = dom_flops / (kernel_ms[dom] * 1e-3) / 1e12
-        kernels_line = {kname[n]: {"ms": kernel_ms[n], "tflops": stage_flops[n] / (kernel_ms[n] * 1e-3) / 1e12,
-                                   "frac_bf16_peak": stage_flops[n] / (kernel_ms[n] * 1e-3) / 1e12 / peak_sus}
-                        for n in kernel_ms}
-        # the forward kernel moves, per (query, selected block) and head, a gathered Q row (256 B), a partial
-        # O row (256 B) and a partial LSE (4 B): HBM-bound against the measured copy rate
-        fb = fwd_algorithmic_bytes(w)
-        hbm = float(peaks.get("hbm_gbs", 6800.0))
-        kernels_line["sparse_fwd_kernel"].update({
-            "algorithmic_gb": fb / 1e9, "gbs": fb / (kernel_ms["sparse_fwd"] * 1e-3) / 1e9,
-            "frac_hbm": fb / (kernel_ms["sparse_fwd"] * 1e-3) / 1e9 / hbm})
-        tr = traffic_record(dom_file)
+        achieved = stage_flops[dom] / (kernel_ms[dom] * 1e-3) / 1e12
+        kernels_line = {}
+        for n in kernel_ms:
+            sec = kernel_ms[n] * 1e-3
+            tr_n = traffic_record(kfile[n])
+            kernels_line[kname[n]] = {
+                "ms": kernel_ms[n], "tflops": stage_flops[n] / sec / 1e12,
+                "frac_bf16_peak": stage_flops[n] / sec / 1e12 / peak,
+                "algorithmic_gb": stage_bytes[n] / 1e9,
+                "algorithmic_gbs": stage_bytes[n] / sec / 1e9,
+                "dram_gb_measured": tr_n["bytes_per_launch"] / 1e9 if tr_n else None,
+                "dram_gbs_measured": tr_n["bytes_per_launch"] / sec / 1e9 if tr_n else None,
+                "frac_hbm_measured": tr_n["bytes_per_launch"] / sec / 1e9 / hbm if tr_n else None}
+        tr = traffic_record(kfile[dom])
         line = {
             "metric": METRIC, "value": aggregate_tokens_per_s(w, world, ms_step), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
@@ -529,22 +587,28 @@ def run_gpu(args, w):
             "config": config_dict(w, world),
             "step": "msa_index_topk -> msa_block_map -> msa_sparse_fwd_mapped -> msa_bwd_mapped (one block map "
                     "of the step's selection serves both passes)",
-            "tflops": tflops, "frac_bf16_peak": tflops / peak_sus,
+            "tflops": tflops, "frac_bf16_peak": tflops / peak, "frac_bf16_peak_sustained": tflops / peak_sus,
             "fwd_tokens_per_s": tokens / ((pm["index_topk"] + pm["sparse_fwd"]) * 1e-3),
             "phases_ms": pm,
             "kernels": kernels_line,
             "counted_flops_per_step": fl["total"] * world,
-            "roofline": {"kernel": f"{kname[dom]} ({dom_file}), CUDA events around each launch",
+            "algorithmic_bytes_per_step": ab["total"] * world,
+            "roofline": {"kernel": f"{kname[dom]} ({kfile[dom]}), CUDA events around each launch",
                          "bound": "tensor", "achieved": achieved,
-                         "peak": peak_sus, "unit": "TFLOP/s", "frac": achieved / peak_sus,
-                         "peak_source": f"{src} bf16 sustained (MEASURED_PEAKS.json)" if src == "measured"
-                         else "fallback 1.7 PFLOP/s sustained",
-                         "traffic": tr["bytes_per_launch"] if tr else None},
+                         "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": (f"{src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)" if src == "measured"
+                                         else "fallback 1.9 PFLOP/s bf16 burst"),
+                         "peak_sustained": peak_sus, "frac_sustained": achieved / peak_sus,
+                         "traffic": tr["bytes_per_launch"] if tr else None,
+                         "algorithmic_bytes": stage_bytes[dom],
+                         "traffic_over_algorithmic": tr["bytes_per_launch"] / stage_bytes[dom] if tr else None},
             "e2e": {"value": aggregate_tokens_per_s(w, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                    "h2d_gbs_alone": h2d / (h2d_ms * 1e-3) / 1e9, "h2d_ms_alone": h2d_ms,
                     "note": "per step: all inputs host->device (pinned) and the KL loss device->host, on their own "
                             "streams, double-buffered: step i+1's inputs and step i's loss move while step i "
-                            "computes"},
+                            "computes; the gradients and O stay on the device. h2d_*_alone: the same copies "
+                            "timed by themselves on this box"},
             "clocks": clk,
             "gpu_launches": launches,
             "index_share": {"ms_per_layer": share_ms, "tokens_per_s": aggregate_tokens_per_s(w, world, share_ms),
@@ -561,8 +625,11 @@ def run_gpu(args, w):
                                "msa_bwd = dense causal attention and the dense-teacher KL"},
         }
         if world == 1 and not args.no_cpu_baseline:
+            line["selection_check"] = selection_check(w, host, sel_rows, sel_got)
             v, desc, cores = oracle_sample(w, args.cpu_seconds)
             line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc}
+            v1, desc1 = oracle_single_thread(w, args.cpu_seconds / 4)
+            line["cpu_baseline"]["single_thread"] = {"value": v1, "unit": "tokens/s", "cores": 1, "sample": desc1}
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

@@ -29,8 +29,8 @@
 //                       dV += P^T dO, dK += dS^T Q, dk_idx += gs^T QI (TMEM,
 //                       across all tiles of the block), dQ^T = K_c^T dS^T and
 //                       dq_idx^T = KI_c^T gs^T (per tile, to slot partials)
-//   bwd_merge_kernel  dQ, dq_idx, KL = sums of the slot partials
-//   dki_merge_kernel  dk_idx = sum over groups
+//   bwd_merge_kernel  dQ, dq_idx, KL = sums of the slot partials; dk_idx = sum
+//                     over groups of the per-group dk_idx rows
 #include "msa_internal.h"
 #include "sm100.cuh"
 
@@ -1080,13 +1080,15 @@ __device__ __forceinline__ void load_bf16_row(const __nv_bfloat16* src, float (&
 // The partials of (b, g, t, slot) sit at padded entry rev[(b*G + g)*T + t][slot]
 // (dQ: HG contiguous rows entry*HG + h; dq_idx: row entry); KL partials at
 // (b, t, g, slot). One warp per (b, t, g); every lane owns 4 * HG consecutive
-// dQ values and 2 dq_idx values.
+// dQ values and 2 dq_idx values. The warp of group 0 also writes dk_idx[b, t]
+// as the sum over groups of the backward kernel's per-group rows.
 template <int HG, int NSL>  // NSL slots per lane: k <= 32 NSL
 __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const int32_t* __restrict__ rev,
                                  const __nv_bfloat16* __restrict__ dq_part, const __nv_bfloat16* __restrict__ dqi_part,
-                                 const float* __restrict__ kl_part, float* __restrict__ dQ,
-                                 float* __restrict__ dq_idx, float* __restrict__ KL, int B, int T, int Hq, int G,
-                                 int k, long long max_padded) {
+                                 const float* __restrict__ kl_part, const float* __restrict__ dki_part,
+                                 float* __restrict__ dQ, float* __restrict__ dq_idx, float* __restrict__ KL,
+                                 float* __restrict__ dk_idx, int B, int T, int Hq, int G, int k,
+                                 long long max_padded) {
   constexpr int kPer = 4 * HG;
   const long long rows = (long long)B * T * G;
   const int lane = threadIdx.x & 31;
@@ -1134,37 +1136,28 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) kl_own += __shfl_xor_sync(0xffffffffu, kl_own, o);
     if (lane == 0) KL[((size_t)b * G + g) * T + t] = kl_own;
-  }
-}
-
-// dk_idx[b,t,:] = sum_g dki_part[b,g,t,:]
-__global__ void dki_merge_kernel(const float* __restrict__ dki_part, float* __restrict__ dk_idx, int B,
-                                 int T, int G) {
-  const long long n2 = (long long)B * T * 32;  // pairs of elements
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n2; i += (long long)gridDim.x * blockDim.x) {
-    const long long bt = i / 32;
-    const int e2 = (int)(i % 32);
-    const int b = (int)(bt / T), t = (int)(bt % T);
-    float s0 = 0.f, s1 = 0.f;
-    for (int g = 0; g < G; ++g) {
-      const float2 v = *reinterpret_cast<const float2*>(dki_part + (((size_t)b * G + g) * T + t) * 64 + e2 * 2);
-      s0 += v.x;
-      s1 += v.y;
+    if (g == 0) {  // dk_idx[b,t,:] = sum_g dki_part[b,g,t,:], groups in ascending order
+      float s0 = 0.f, s1 = 0.f;
+      for (int gg = 0; gg < G; ++gg) {
+        const float2 v = *reinterpret_cast<const float2*>(dki_part + (((size_t)b * G + gg) * T + t) * 64 + lane * 2);
+        s0 += v.x;
+        s1 += v.y;
+      }
+      *reinterpret_cast<float2*>(dk_idx + bt * 64 + lane * 2) = make_float2(s0, s1);
     }
-    *reinterpret_cast<float2*>(dk_idx + bt * 64 + e2 * 2) = make_float2(s0, s1);
   }
 }
 
 // Two slots per lane up to k = 64, four up to k = 128.
 template <int HG>
 void bwd_merge(const Prob& p, const int32_t* block_idx, const int32_t* rev, const BwdArgs& ba, float* dQ,
-               float* dq_idx, float* KL, long long max_padded, int grid, cudaStream_t st) {
+               float* dq_idx, float* KL, float* dk_idx, long long max_padded, int grid, cudaStream_t st) {
   if (p.k <= 64)
-    bwd_merge_kernel<HG, 2><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQ, dq_idx, KL,
-                                                   p.B, p.T, p.Hq, p.G, p.k, max_padded);
+    bwd_merge_kernel<HG, 2><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, ba.dki_part,
+                                                   dQ, dq_idx, KL, dk_idx, p.B, p.T, p.Hq, p.G, p.k, max_padded);
   else
-    bwd_merge_kernel<HG, 4><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, dQ, dq_idx, KL,
-                                                   p.B, p.T, p.Hq, p.G, p.k, max_padded);
+    bwd_merge_kernel<HG, 4><<<grid, 256, 0, st>>>(block_idx, rev, ba.dq_part, ba.dqi_part, ba.kl_part, ba.dki_part,
+                                                   dQ, dq_idx, KL, dk_idx, p.B, p.T, p.Hq, p.G, p.k, max_padded);
 }
 
 }  // namespace
@@ -1308,23 +1301,21 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     default: bwd_kernel<8><<<sms, kBwdThreads, BwdLayout<8>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
   }
   timing_end(MSA_TIME_BWD, st);
-  count_launches(6);
+  count_launches(5);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     const int grid = (int)std::min<long long>((grows * 32 + 255) / 256, 16LL * sms);
     const int32_t* rev = reinterpret_cast<const int32_t*>(ws + L.rev);
     float* dQf = static_cast<float*>(dQ);
     float* dqif = static_cast<float*>(dq_idx);
+    float* dkif = static_cast<float*>(dk_idx);
     switch (p.hg) {
-      case 1: bwd_merge<1>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
-      case 2: bwd_merge<2>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
-      case 4: bwd_merge<4>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
-      default: bwd_merge<8>(p, block_idx, rev, ba, dQf, dqif, KL, L.max_padded, grid, st); break;
+      case 1: bwd_merge<1>(p, block_idx, rev, ba, dQf, dqif, KL, dkif, L.max_padded, grid, st); break;
+      case 2: bwd_merge<2>(p, block_idx, rev, ba, dQf, dqif, KL, dkif, L.max_padded, grid, st); break;
+      case 4: bwd_merge<4>(p, block_idx, rev, ba, dQf, dqif, KL, dkif, L.max_padded, grid, st); break;
+      default: bwd_merge<8>(p, block_idx, rev, ba, dQf, dqif, KL, dkif, L.max_padded, grid, st); break;
     }
   }
-  const long long n2 = (long long)p.B * p.T * 32;
-  dki_merge_kernel<<<(int)std::min<long long>((n2 + 255) / 256, 16LL * sms), 256, 0, st>>>(
-      ba.dki_part, static_cast<float*>(dk_idx), p.B, p.T, p.G);
   return cudaGetLastError();
 }
 

@@ -199,12 +199,16 @@ MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K,
  * static device array of MSA_NOALLOC_SCRATCH_BYTES bytes inside the library,
  * which every GPU that loads the library holds until the process exits.
  *
- * - The first call on a device looks up that array's device address (once
- *   per device, with the device current); make that first call before any
- *   stream capture.
+ * - Each GPU has its own copy of the array. The first call on a device looks
+ *   up the address of that device's copy (once per device, with the device
+ *   current) and the library keeps it; make that first call before any stream
+ *   capture. The address belongs to the device's primary context: after
+ *   cudaDeviceReset() on that device, reload the library before calling
+ *   this function again.
  * - Every call clears the scratch it relies on (asynchronously, on `stream`)
- *   and then reuses it: calls that overlap on the GPU (different streams or
- *   devices' contexts sharing the array) race on it. Serialise them.
+ *   and then reuses it: calls that overlap on the same GPU (for example on
+ *   two streams of one device) race on it. Serialise them; calls on
+ *   different GPUs use different copies and do not race.
  * - A shape whose scratch would exceed MSA_NOALLOC_SCRATCH_BYTES is rejected
  *   with MSA_ERR_UNSUPPORTED.
  * - check != 0 synchronises `stream` and returns MSA_ERR_DEVICE if the kernel

@@ -33,12 +33,28 @@ def test_selected_pairs_equal_a_direct_count():
     assert direct == bench.n_selected(w)
 
 
-def test_forward_algorithmic_bytes_closed_form():
+def test_algorithmic_bytes_are_the_entry_points_tensor_sizes():
+    """Each stage's algorithmic bytes = its inputs read once + its outputs
+    written once, counted here from arrays of the C ABI's shapes and dtypes."""
+    import numpy as np
+
     import bench
 
-    for w in (synth.CONFIGS[1], synth.CONFIGS[3], synth.CONFIGS[0].with_(T=640, k=8)):
-        n, k, hg = w.n_blocks, w.k, w.Hq // w.G
-        # queries of block c keep min(k, c + 1) blocks: k(k+1)/2 + (n - k) k pairs per query row of a block when n >= k
-        per = k * (k + 1) // 2 + (n - k) * k if n >= k else n * (n + 1) // 2
-        pairs = w.Bk * per * w.B * w.G
-        assert bench.fwd_algorithmic_bytes(w) == pairs * hg * (2 * w.d * 2 + 4)
+    for w in (synth.CONFIGS[0], synth.CONFIGS[1].with_(B=2, T=1024)):
+        B, T, Hq, G, d, E, k = w.B, w.T, w.Hq, w.G, w.d, w.d_idx, w.k
+        bf, f32, i32 = np.uint16, np.float32, np.int32
+        t = dict(Q=((B, T, Hq, d), bf), K=((B, T, G, d), bf), V=((B, T, G, d), bf), O=((B, T, Hq, d), bf),
+                 dO=((B, T, Hq, d), bf), q_idx=((B, T, G, E), bf), k_idx=((B, T, E), bf),
+                 block_idx=((B, G, T, k), i32), LSE=((B, T, Hq), f32), dQ=((B, T, Hq, d), f32),
+                 dK=((B, T, G, d), f32), dV=((B, T, G, d), f32), dq_idx=((B, T, G, E), f32),
+                 dk_idx=((B, T, E), f32), KL=((B, G, T), f32))
+        nb = {n: np.zeros(sh, dt).nbytes for n, (sh, dt) in t.items()}
+        want = dict(
+            index=nb["q_idx"] + nb["k_idx"] + nb["block_idx"],
+            fwd=nb["Q"] + nb["K"] + nb["V"] + nb["block_idx"] + nb["O"] + nb["LSE"],
+            bwd=sum(nb[n] for n in ("Q", "K", "V", "O", "dO", "LSE", "q_idx", "k_idx", "block_idx", "dQ", "dK",
+                                    "dV", "dq_idx", "dk_idx", "KL")))
+        got = bench.algorithmic_bytes(w)
+        for n in want:
+            assert got[n] == want[n], n
+        assert got["total"] == sum(want.values())

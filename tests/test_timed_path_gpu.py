@@ -1,0 +1,110 @@
+"""Parity of the exact pipeline the benchmark times, at its workload.
+
+B=1, T=131072, Hq=32, G=8, k=16 with the seeded inputs of that workload:
+msa_index_topk -> msa_block_map -> msa_sparse_fwd_mapped -> msa_bwd_mapped, in
+one workspace, as one benchmark step runs them. The selection is the real one
+(index scores of the per-block-offset index keys), not a random stand-in.
+
+Checked against the fp64 oracle, which is given the GPU's block_idx
+(itinai.ru "How to solve the memory problem with MiniMax Sparse Attention",
+"Two-stage process"; dothoosh.com "how Flash-MSA cuts million-token training
+cost", "Kernel design and execution"):
+- sampled block_idx rows: bit-exact outside near-ties (oracle k-th/(k+1)-th
+  gap < 1e-4), the near-tie count printed;
+- sampled query rows: O and LSE of every head of the row's group, dQ, dq_idx
+  and KL;
+- dK, dV and dk_idx of the KV block with the longest selection list (most
+  (query, group) selections, i.e. the most tiles accumulated in TMEM) and of
+  an early block (c = 2).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_close, compare_block_idx, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def msa():
+    import __graft_entry__
+
+    __graft_entry__.build_library()
+    import block_sparse_attention_scores_gb300 as m
+
+    return m
+
+
+def test_timed_path_t131072(msa):
+    import torch
+
+    w = synth.CONFIGS[3]
+    inp = synth.make_inputs(w)
+    s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
+    ws = msa.alloc_workspace(s, msa.MSA_WS_BWD)
+    d = {n: to_dev(inp[n]) for n in ("Q", "K", "V", "dO", "q_idx", "k_idx")}
+    bi = torch.empty((w.B, w.G, w.T, w.k), dtype=torch.int32, device="cuda")
+    O = torch.empty_like(d["Q"])
+    LSE = torch.empty((w.B, w.T, w.Hq), dtype=torch.float32, device="cuda")
+    f32 = dict(dtype=torch.float32, device="cuda")
+    g = dict(dQ=torch.empty(d["Q"].shape, **f32), dK=torch.empty(d["K"].shape, **f32),
+             dV=torch.empty(d["V"].shape, **f32), dq_idx=torch.empty(d["q_idx"].shape, **f32),
+             dk_idx=torch.empty(d["k_idx"].shape, **f32), KL=torch.empty((w.B, w.G, w.T), **f32))
+    st = torch.cuda.current_stream()
+    for _ in range(2):  # twice, as consecutive benchmark steps reuse the workspace
+        msa.msa_index_topk(s, d["q_idx"], d["k_idx"], bi, ws, st)
+        msa.msa_block_map(s, bi, ws, st)
+        msa.msa_sparse_fwd_mapped(s, d["Q"], d["K"], d["V"], bi, O, LSE, ws, st)
+        msa.msa_bwd_mapped(s, d["Q"], d["K"], d["V"], O, d["dO"], LSE, d["q_idx"], d["k_idx"], bi, 1.0, g["dQ"],
+                           g["dK"], g["dV"], g["dq_idx"], g["dk_idx"], g["KL"], ws, st)
+    msa.msa_check_device_status(ws, st)
+    torch.cuda.synchronize()
+    bi_h = bi.cpu().numpy()
+    os_ = oracle.shape_of(w)
+    rng = np.random.default_rng(31)
+
+    # ---- block_idx on sampled rows: first blocks (fewer than k visible), block edges, the end, random
+    t_s = np.concatenate([np.arange(0, 2048, 97), np.arange(127, w.T, 8191), np.arange(w.T - 16, w.T),
+                          rng.integers(0, w.T, 160)])
+    g_s = rng.integers(0, w.G, t_s.size)
+    rows = g_s * w.T + t_s
+    want, gap, _ = oracle.index_topk(os_, inp["q_idx"], inp["k_idx"], rows=rows)
+    n, ties, bad, bad_tie = compare_block_idx(bi_h.reshape(-1, w.k)[rows], want, gap)
+    print(f"block_idx: {n} sampled rows, {ties} near-ties (gap < 1e-4), {bad} mismatches outside near-ties, "
+          f"{bad_tie} inside")
+    assert bad == 0
+
+    # ---- forward and per-query backward on sampled query rows, given the GPU's selection
+    n_rows = 256
+    t_q = np.concatenate([np.arange(4), np.arange(w.T - 4, w.T), rng.integers(0, w.T, n_rows - 8)])
+    g_q = rng.integers(0, w.G, n_rows)
+    hg = w.Hq // w.G
+    hrows = (t_q[:, None] * w.Hq + g_q[:, None] * hg + np.arange(hg)[None, :]).ravel()
+    O_ref, L_ref = oracle.sparse_fwd(os_, inp["Q"], inp["K"], inp["V"], bi_h, rows=hrows)
+    O_g = to_f64(O).reshape(-1, w.d)[hrows]
+    L_g = to_f64(LSE).reshape(-1)[hrows]
+    res = [("O",) + assert_close("O", O_g, O_ref), ("LSE",) + assert_close("LSE", L_g, L_ref)]
+    qrows = g_q * w.T + t_q
+    ins = [inp[x] for x in ("Q", "K", "V", "dO", "q_idx", "k_idx")]
+    dQ, dqi, KL = oracle.bwd_rows(os_, *ins, bi_h, rows=qrows)
+    gdQ = to_f64(g["dQ"])[0, t_q].reshape(n_rows, w.G, hg, w.d)[np.arange(n_rows), g_q]
+    res.append(("dQ",) + assert_close("dQ", gdQ, dQ))
+    res.append(("dq_idx",) + assert_close("dq_idx", to_f64(g["dq_idx"])[0, t_q, g_q], dqi))
+    res.append(("KL",) + assert_close("KL", to_f64(g["KL"])[0, g_q, t_q], KL))
+
+    # ---- per-block backward: the longest list (selections summed over groups) and an early block
+    counts = np.bincount(bi_h[bi_h >= 0].ravel(), minlength=w.n_blocks)
+    longest = int(np.argmax(counts))
+    blocks = [longest, 2] if longest != 2 else [2, 3]
+    dK, dV, dki = oracle.bwd_blocks(os_, *ins, bi_h, blocks=np.array(blocks))
+    gK, gV, gki = to_f64(g["dK"]), to_f64(g["dV"]), to_f64(g["dk_idx"])
+    for i, c in enumerate(blocks):
+        sl = slice(c * w.Bk, (c + 1) * w.Bk)
+        res.append((f"dK[c={c}]",) + assert_close("dK", gK[0, sl].transpose(1, 0, 2), dK[i]))
+        res.append((f"dV[c={c}]",) + assert_close("dV", gV[0, sl].transpose(1, 0, 2), dV[i]))
+        res.append((f"dk_idx[c={c}]",) + assert_close("dk_idx", gki[0, sl], dki[i]))
+    print(f"longest list: block {longest} with {int(counts[longest])} selections over {w.G} groups "
+          f"(mean {counts.mean():.0f}); block 2 has {int(counts[2])}")
+    print("timed path T=131072: " + "  ".join(f"{x} err={e:.1e} cos={c:.6f}" for x, e, c in res))
