@@ -563,8 +563,11 @@ def run_gpu(args, w):
         # dominant kernel of the step, timed alone (events recorded by the library around its launches)
         stage_flops = {"index_topk": fl["index"], "sparse_fwd": fl["fwd"], "bwd": fl["bwd"]}
         stage_bytes = {"index_topk": ab["index"], "sparse_fwd": ab["fwd"], "bwd": ab["bwd"]}
-        kname = {"index_topk": "index_topk_kernel", "sparse_fwd": "sparse_fwd_kernel", "bwd": "bwd_kernel"}
-        kfile = {"index_topk": "index_topk.cu", "sparse_fwd": "sparse_fwd.cu", "bwd": "sparse_bwd.cu"}
+        wide = w.Hq // w.G >= 4  # 4 or 8 heads per group: the 128-row-tile backward
+        kname = {"index_topk": "index_topk_kernel", "sparse_fwd": "sparse_fwd_kernel",
+                 "bwd": "bwd_wide_kernel" if wide else "bwd_kernel"}
+        kfile = {"index_topk": "index_topk.cu", "sparse_fwd": "sparse_fwd.cu",
+                 "bwd": "sparse_bwd_wide.cu" if wide else "sparse_bwd.cu"}
         dom = max(kernel_ms, key=kernel_ms.get)
         achieved = stage_flops[dom] / (kernel_ms[dom] * 1e-3) / 1e12
         kernels_line = {}

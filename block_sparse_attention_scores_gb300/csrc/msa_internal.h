@@ -99,7 +99,7 @@ cudaError_t build_block_map2(const Prob& p, const int32_t* block_idx, uint8_t* w
 
 // Queries per forward tile / per backward tile, and the forward's tiles per item.
 inline int fwd_tile_queries(const Prob& p) { return 128 / p.hg; }
-inline int bwd_tile_queries(const Prob& p) { return 64 / p.hg; }
+inline int bwd_tile_queries(const Prob& p) { return (p.hg >= 4 ? 128 : 64) / p.hg; }
 constexpr int kFwdTilesPerItem = 32;
 
 // mapped: use the map (and the forward's items) that build_block_map2 left

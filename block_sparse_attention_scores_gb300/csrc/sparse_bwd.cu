@@ -31,32 +31,17 @@
 //                       dq_idx^T = KI_c^T gs^T (per tile, to slot partials)
 //   bwd_merge_kernel  dQ, dq_idx, KL = sums of the slot partials; dk_idx = sum
 //                     over groups of the per-group dk_idx rows
-#include "msa_internal.h"
-#include "sm100.cuh"
+#include "bwd_common.cuh"
 
 namespace msa {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-
-__device__ __forceinline__ float fast_exp2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-
-__device__ __forceinline__ void decode_list(int l, int n, int G, int& b, int& g, int& c) {
-  const int bg = l / n;
-  c = l - bg * n;
-  b = bg / G;
-  g = bg - b * G;
-}
+using bwdc::decode_list;
+using bwdc::fast_exp2;
+using bwdc::lanes_sum_add;
+using bwdc::pack_bf16;
+constexpr float kLog2e = kBwdLog2e;
+constexpr float kLn2 = kBwdLn2;
 
 // ============================================================================ D
 __global__ void drow_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
@@ -349,61 +334,6 @@ struct __align__(16) RowMeta {
   float lpx2[kRows];  // lse_px * log2 e
   int ent[kRows];     // entry bits t << 8 | slot, -1 for padding
   int diag[8];        // per producer: some row sees only part of the block (causal mask needed)
-};
-
-// Sum over the 32 lanes of NV per-lane values, with a butterfly that halves
-// the values a lane keeps at each step (NV - 1 shuffles instead of 5 NV), then
-// add each sum into acc[] (one shared atomic per value, distinct addresses).
-template <int NV>
-__device__ __forceinline__ void lanes_sum_add(float (&v)[NV], int lane, float* acc) {
-  int base = 0;
-#pragma unroll
-  for (int s = 0; s < 5; ++s) {
-    const int off = 16 >> s;
-    constexpr int kNV = NV;
-    const int n = kNV >> s;
-    if (n >= 2) {
-      const int half = n >> 1;
-      const bool up = (lane & off) != 0;
-#pragma unroll
-      for (int i = 0; i < (kNV >> (s + 1)); ++i) {
-        const float send = up ? v[i] : v[i + half];
-        const float keep = up ? v[i + half] : v[i];
-        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-      }
-      if (up) base += half;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-    }
-  }
-  constexpr int kKeep = NV >= 32 ? NV / 32 : 1;
-  constexpr int kDup = NV >= 32 ? 1 : 32 / NV;  // lanes holding the same sums
-  if ((lane & (kDup - 1)) == 0) {
-#pragma unroll
-    for (int i = 0; i < kKeep; ++i) atomicAdd(&acc[base + i], v[i]);
-  }
-}
-
-struct BwdArgs {
-  const __nv_bfloat16* Q;
-  const __nv_bfloat16* dO;
-  const __nv_bfloat16* q_idx;
-  const float* LSE;
-  const float* drow;
-  const float* lse_px;
-  const int32_t* entries;
-  const int4* items;
-  const int* n_items;
-  int* counter;
-  int* err;
-  float* dK;
-  float* dV;
-  __nv_bfloat16* dq_part;  // [padded entries, hg, d], tile order
-  __nv_bfloat16* dqi_part; // [padded entries, E], tile order
-  float* kl_part;          // [B,T,G,k]
-  float* dki_part;         // [B,G,T,E]
-  int B, T, Hq, G, hg, n, k;
-  float scale_log2, scale, scale_idx_log2, scale_idx, kl_weight;
 };
 
 struct BwdShared {
@@ -1214,16 +1144,20 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if (!encode_tmap(&mqi, const_cast<void*>(q_idx), 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_128B))
       return cudaErrorInvalidValue;
   }
+  // 64-row tiles (1 or 2 heads per group) store 32 rows per epilogue warp,
+  // 128-row tiles (4 or 8) 64 rows
+  const bool wide = p.hg >= 4;
+  const uint32_t rows_per_warp = wide ? 64 : 32;
   CUtensorMap mdq, mdqi;
   {
     const uint64_t dims[2] = {128, (uint64_t)L.max_padded * p.hg};
     const uint64_t strides[1] = {256};
-    const uint32_t box[2] = {32, 32};  // 32 d x 32 rows per epilogue warp
+    const uint32_t box[2] = {32, rows_per_warp};  // 32 d x the warp's rows
     if (!encode_tmap(&mdq, ws + L.dq_part, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
     const uint64_t dims2[2] = {64, (uint64_t)L.max_padded};
     const uint64_t strides2[1] = {128};
-    const uint32_t box2[2] = {32, (uint32_t)(32 / p.hg)};  // 32 e x the queries of 32 rows
+    const uint32_t box2[2] = {32, rows_per_warp / (uint32_t)p.hg};  // 32 e x the queries of those rows
     if (!encode_tmap(&mdqi, ws + L.dqi_part, 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_NONE))
       return cudaErrorInvalidValue;
   }
@@ -1236,11 +1170,7 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
     if ((e = cudaFuncSetAttribute(bwd_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   BwdLayout<1>::kSmem)) != cudaSuccess ||
         (e = cudaFuncSetAttribute(bwd_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  BwdLayout<2>::kSmem)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  BwdLayout<4>::kSmem)) != cudaSuccess ||
-        (e = cudaFuncSetAttribute(bwd_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  BwdLayout<8>::kSmem)) != cudaSuccess)
+                                  BwdLayout<2>::kSmem)) != cudaSuccess)
       return e;
     attr[dslot] = true;
   }
@@ -1294,11 +1224,12 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.scale_idx = p.scale_idx;
   ba.kl_weight = kl_weight;
   timing_begin(MSA_TIME_BWD, st);
-  switch (p.hg) {
-    case 1: bwd_kernel<1><<<sms, kBwdThreads, BwdLayout<1>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
-    case 2: bwd_kernel<2><<<sms, kBwdThreads, BwdLayout<2>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
-    case 4: bwd_kernel<4><<<sms, kBwdThreads, BwdLayout<4>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
-    default: bwd_kernel<8><<<sms, kBwdThreads, BwdLayout<8>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi); break;
+  if (wide) {
+    if ((e = launch_bwd_wide(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi, st)) != cudaSuccess) return e;
+  } else if (p.hg == 1) {
+    bwd_kernel<1><<<sms, kBwdThreads, BwdLayout<1>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+  } else {
+    bwd_kernel<2><<<sms, kBwdThreads, BwdLayout<2>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
   }
   timing_end(MSA_TIME_BWD, st);
   count_launches(5);

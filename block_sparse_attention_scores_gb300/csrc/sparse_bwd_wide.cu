@@ -1,0 +1,668 @@
+// Fused backward of MiniMax Sparse Attention on 128-row tiles, for 4 or 8
+// query heads per GQA group: main-branch dQ/dK/dV and the KL-alignment
+// gradient of the index branch in one pass over the selected blocks.
+//
+// dothoosh.com "how Flash-MSA cuts million-token training cost", "Kernel
+// design and execution": one fused backward over proxy and main branch,
+// scheduled through the inverted block -> query map so that each KV block is
+// staged once for all query chunks that chose it; "Fixing the KL-divergence
+// bottleneck": d KL / d s_px = p_px - p_main. itinai.ru "How to solve the
+// memory problem with MiniMax Sparse Attention", "Training sparse attention":
+// the teacher is the head-averaged main softmax, detached. dothoosh.com "how
+// FlashAttention cuts GPU memory traffic", "Training and the backward pass":
+// P is rebuilt from the saved LSE; dV += P^T dO, dP = dO V^T.
+//
+// Per KV block c of (b, g) (one work item = one inverted list), keys on TMEM
+// lanes, tiles of 128 (query, head) rows = 128 / hg queries x hg heads:
+//   S^T  = K_c Q^T     (N = 128)      X^T = KI_c QI^T   (N = queries)
+//   P    = exp(s - LSE), p_main = head mean, p_px = exp(x - lse_px)
+//   dP^T = V_c dO^T    (N = 128)      dS = P (dP - D)
+//   dV  += P^T dO      (P^T from TMEM) dK += dS^T Q      (TMEM, whole list)
+//   dQ^T = K_c^T dS^T  (N = 128)       -> bf16 slot partial, TMA store
+//   gs   = w (p_px - p_main)           dk_idx += gs^T QI (TMEM, whole list)
+//   dq_idx^T = KI_c^T gs^T             -> bf16 slot partial, TMA store
+// Every MMA of a tile has N = 128 except the index ones, so the tensor pipe
+// runs near its per-instruction rate instead of at the N = 64 floor of a
+// 64-row tile.
+//
+// TMEM (512 columns): R [0, 128) holds S^T, then dP^T (once the epilogue has
+// loaded S^T), then dQ^T; P [128, 192) holds X^T, then P^T as packed bf16
+// pairs (once every epilogue warp has loaded X^T), then dq_idx^T (once dV has
+// read P^T); dV [192, 320), dK [320, 448), dk_idx [448, 512) accumulate over
+// the list.
+//
+// Shared memory: K, V, k_idx of the block (80 KB) and two gather buffers of
+// 68 KB (Q, dO: 128 rows x 256 B each; q_idx: one 128-byte row per query).
+// Inside a tile's buffer, dS^T goes where dO was (once dV has read it), gs^T
+// where Q was (once dK has read it), and the dQ / dq_idx partials are staged
+// there for their TMA stores.
+//
+// Warp roles (512 threads, one CTA per SM, persistent; registers split 64 /
+// 192 between the first two warpgroups and the last two):
+//   warp 0       TMEM owner, UMMA issuer (one thread)
+//   warps 1-7    producers 0-6: producer p gathers the queries p, p + 7, ...
+//                of every tile (TMA boxes of their hg head rows of Q and dO,
+//                and their q_idx row) and writes their row metadata;
+//                producer 0 also fetches the work items and loads K, V, k_idx
+//   warps 8-15   epilogue: TMEM lane quarter = warp % 4, warpgroup hf owns
+//                the tile rows [64 hf, 64 hf + 64)
+#include "bwd_common.cuh"
+
+namespace msa {
+namespace {
+
+using bwdc::decode_list;
+using bwdc::fast_exp2;
+using bwdc::lanes_sum_add;
+using bwdc::pack_bf16;
+constexpr float kLog2e = kBwdLog2e;
+constexpr float kLn2 = kBwdLn2;
+
+constexpr int kThreads = 512;
+constexpr int kProd = 7;                  // producer warps 1..7
+constexpr int kRows = 128;                // (query, head) rows per tile
+constexpr int kKV = 32768;                // 128 keys x 128 d bf16
+constexpr int kChunk = 16384;             // 128 rows x 64 bf16 (one SW128 column chunk)
+constexpr int kKIb = 16384;               // 128 keys x 64 bf16
+// smem map: K, V, k_idx, then two gather buffers, then the shared state
+constexpr int oK = 0, oV = kKV, oKI = 2 * kKV, oG = 2 * kKV + kKIb;
+constexpr int oQ = 0, oDO = 2 * kChunk, oQI = 4 * kChunk;  // inside a gather buffer
+constexpr int kQIb = 4096;                                  // up to 32 q_idx rows
+constexpr int kGather = oQI + kQIb;
+constexpr int oSh = oG + 2 * kGather;
+// TMEM columns
+constexpr uint32_t cR = 0, cP = 128, cDV = 192, cDK = 320, cKI = 448;
+
+struct __align__(16) RowMeta {
+  float lse2[kRows];  // LSE * log2 e (+inf for padding rows: P = 0 there)
+  float dsc[kRows];   // D * scale
+  float lpx2[kRows];  // lse_px * log2 e (+inf for padding rows)
+  int ent[kRows];     // entry bits t << 8 | slot, -1 for padding
+  int diag[8];        // per producer: some row sees only part of the block (causal mask needed)
+};
+
+struct Shared {
+  uint64_t it_full[2], it_empty[2];
+  uint64_t kv_full, kv_empty;
+  uint64_t g_full[2], g_empty[2];
+  uint64_t s_full, s_read, dp_full, p_ready, pv_done, ds_ready, dk_done, gs_ready, dq_full, ph2_full;
+  uint64_t r_free, x_free, acc_free, kl_ready, kl_free;
+  RowMeta meta[2];
+  float kl_acc[32];
+  int4 item[2];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr int kSmem = oSh + (int)sizeof(Shared);
+static_assert(kGather % 1024 == 0, "gather buffers keep the 1024-byte swizzle alignment");
+static_assert(kSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
+
+__device__ __forceinline__ void regs_dealloc64() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory"); }
+__device__ __forceinline__ void regs_alloc192() { asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory"); }
+
+// Stores 32 fp32 values as 32 consecutive columns of the thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+      " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+
+template <int HG>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_wide_kernel(BwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                    const __grid_constant__ CUtensorMap map_ki, const __grid_constant__ CUtensorMap map_dq,
+                    const __grid_constant__ CUtensorMap map_dqi, const __grid_constant__ CUtensorMap map_q,
+                    const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_qi) {
+  static_assert(HG == 4 || HG == 8, "128-row tiles for 4 or 8 heads per group");
+  constexpr int hg = HG;
+  constexpr int npos = kRows / HG;  // queries per tile (32 or 16)
+  constexpr int kHQ = npos / 2;     // queries of one epilogue half
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {  // uniform for the block: nothing started yet
+    if (threadIdx.x == 0) dev_fail(a.err, kDevSmemAlign, 600);
+    return;
+  }
+  Shared& sh = *reinterpret_cast<Shared*>(smem + oSh);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < npos; ++i) sh.kl_acc[i] = 0.f;
+    for (int i = 0; i < 8; ++i) sh.meta[0].diag[i] = sh.meta[1].diag[i] = 0;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.it_full[i], 1);
+      mbar_init(&sh.it_empty[i], kProd - 1 + 1 + 8);  // other producers, UMMA, epilogue warps
+      mbar_init(&sh.g_full[i], kProd);                // every producer warp (with its TMA bytes)
+      mbar_init(&sh.g_empty[i], 8);                   // epilogue warps, once their stores have read the buffer
+    }
+    mbar_init(&sh.kv_full, 1);
+    mbar_init(&sh.kv_empty, 1);
+    mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.s_read, 8);
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.p_ready, 8);
+    mbar_init(&sh.pv_done, 1);
+    mbar_init(&sh.ds_ready, 8);
+    mbar_init(&sh.dk_done, 1);
+    mbar_init(&sh.gs_ready, 8);
+    mbar_init(&sh.dq_full, 1);
+    mbar_init(&sh.ph2_full, 1);
+    mbar_init(&sh.r_free, 8);
+    mbar_init(&sh.x_free, 8);
+    mbar_init(&sh.acc_free, 8);
+    mbar_init(&sh.kl_ready, 8);
+    mbar_init(&sh.kl_free, 1);
+    sh.abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+  volatile int* abort_flag = &sh.abort;
+  const int n_items = *a.n_items;
+
+  // The register split is set where it dominates each role's code, so that
+  // the compiler gives the epilogue its 192 registers.
+  if (warp < 8) {
+  regs_dealloc64();
+  if (warp >= 1) {
+    // ------------------------------------------------------------ producers
+    const int p = warp - 1;
+    const int nq = (npos - p + kProd - 1) / kProd;  // queries of this producer in a tile
+    const int qmine = p + kProd * (lane / hg), hmine = lane % hg;
+    const bool mine = lane < nq * hg;  // lane's (query, head) row
+    auto load_entry = [&](const int4& item, int j) -> int {
+      const int idx = j * npos + qmine;
+      return (mine && idx < item.z) ? a.entries[item.y + idx] : -1;
+    };
+    auto load_rec = [&](int b, int g, int e) -> float4 {
+      if (e < 0) return make_float4(INFINITY, 0.f, INFINITY, __int_as_float(e));
+      const int t = e >> 8;
+      const size_t hr = ((size_t)b * a.T + t) * a.Hq + g * hg + hmine;
+      const float l = a.LSE[hr], d = a.drow[hr];
+      const float x = a.lse_px[((size_t)b * a.T + t) * a.G + g];
+      return make_float4(l * kLog2e, d * a.scale, x * kLog2e, __int_as_float(e));
+    };
+    if (lane == 0) {
+      tma_prefetch_desc(&map_q);
+      tma_prefetch_desc(&map_do);
+      tma_prefetch_desc(&map_qi);
+      if (p == 0) {
+        tma_prefetch_desc(&map_k);
+        tma_prefetch_desc(&map_v);
+        tma_prefetch_desc(&map_ki);
+      }
+    }
+    uint32_t tj = 0;
+    bool ok = true;
+    for (int it = 0; ok; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      int4 item = make_int4(-1, 0, 0, 0);
+      if (p == 0) {
+        if (lane == 0) {
+          if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 601)) *abort_flag = 1;
+          const int id = atomicAdd(a.counter, 1);
+          if (id < n_items && !*abort_flag) item = a.items[id];
+          sh.item[s] = item;
+          mbar_arrive(&sh.it_full[s]);
+        }
+        item.x = __shfl_sync(0xffffffffu, item.x, 0);
+        item.y = __shfl_sync(0xffffffffu, item.y, 0);
+        item.z = __shfl_sync(0xffffffffu, item.z, 0);
+        item.w = __shfl_sync(0xffffffffu, item.w, 0);
+      } else {
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 602)) { ok = false; break; }
+        item = sh.item[s];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      }
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      if (p == 0) {
+        if (lane == 0) {
+          if (mbar_wait(&sh.kv_empty, (it & 1) ^ 1, a.err, 603)) {
+            mbar_arrive_expect_tx(&sh.kv_full, 2 * kKV + kKIb);
+            const int row0 = b * a.T + c * 128;
+            tma_load_3d(smem + oK, &map_k, &sh.kv_full, 0, g, row0);
+            tma_load_3d(smem + oK + kChunk, &map_k, &sh.kv_full, 64, g, row0);
+            tma_load_3d(smem + oV, &map_v, &sh.kv_full, 0, g, row0);
+            tma_load_3d(smem + oV + kChunk, &map_v, &sh.kv_full, 64, g, row0);
+            tma_load_2d(smem + oKI, &map_ki, &sh.kv_full, 0, row0);
+          } else {
+            *abort_flag = 1;
+          }
+        }
+        __syncwarp();
+        if (*abort_flag) break;
+      }
+      const int ntiles = (item.z + npos - 1) / npos;
+      const int key_last = c * 128 + 127;
+      const int BT = a.B * a.T;
+      int e_next = load_entry(item, 0);
+      float4 rec = load_rec(b, g, e_next);
+      e_next = ntiles > 1 ? load_entry(item, 1) : -1;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int gb = tj & 1;
+        if (!mbar_wait(&sh.g_empty[gb], ((tj >> 1) & 1) ^ 1, a.err, 604 + p)) { ok = false; break; }
+        uint8_t* buf = smem + oG + gb * kGather;
+        RowMeta& m = sh.meta[gb];
+        const int e_own = __float_as_int(rec.w);
+        if (mine) {
+          const int r = qmine * hg + hmine;
+          m.lse2[r] = rec.x;
+          m.dsc[r] = rec.y;
+          m.lpx2[r] = rec.z;
+          m.ent[r] = e_own;
+        }
+        const unsigned dg = __ballot_sync(0xffffffffu, mine && e_own >= 0 && (e_own >> 8) < key_last);
+        if (lane == 0) {
+          m.diag[p] = dg != 0u;
+          mbar_arrive_expect_tx(&sh.g_full[gb], nq * (2 * hg * 256 + 128));
+        }
+        __syncwarp();
+        // per query: Q and dO boxes of its hg head rows (one per 64-column
+        // chunk) at row q * hg, then its q_idx row at row q; padding queries
+        // load an out-of-range box (zero fill, bytes still counted)
+#pragma unroll 1
+        for (int o = lane; o < nq * 5; o += 32) {
+          const int i = o / 5, op = o - i * 5;
+          const int q = p + kProd * i;
+          const int e = m.ent[q * hg];
+          const int bt = e >= 0 ? b * a.T + (e >> 8) : BT;
+          if (op < 4) {
+            const int which = op >> 1, chunk = op & 1;
+            tma_load_3d(buf + (which ? oDO : oQ) + chunk * kChunk + q * hg * 128, which ? &map_do : &map_q,
+                        &sh.g_full[gb], chunk * 64, g * hg, bt);
+          } else {
+            tma_load_2d(buf + oQI + q * 128, &map_qi, &sh.g_full[gb], 0, bt * a.G + g);
+          }
+        }
+        __syncwarp();
+        if (j + 1 < ntiles) {
+          rec = load_rec(b, g, e_next);
+          e_next = j + 2 < ntiles ? load_entry(item, j + 2) : -1;
+        }
+      }
+    }
+    if (!ok) *abort_flag = 1;
+  } else {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = make_idesc_bf16(128, 128, false, false);   // K-major x K-major, N = 128
+      constexpr uint32_t id_acc = make_idesc_bf16(128, 128, false, true);  // K-major A, MN-major B
+      constexpr uint32_t id_dq = make_idesc_bf16(128, 128, true, true);    // MN-major A and B
+      constexpr uint32_t id_x = make_idesc_bf16(128, npos, false, false);
+      constexpr uint32_t id_ki = make_idesc_bf16(128, 64, false, true);
+      constexpr uint32_t id_dqi = make_idesc_bf16(128, npos, true, true);
+      // descriptors built once; a k-step or the other gather buffer moves only the start address
+      const uint64_t dK = make_sdesc(smem_u32(smem + oK), 16, 1024, kSw128);       // K, K-major
+      const uint64_t dKt = make_sdesc(smem_u32(smem + oK), kChunk, 1024, kSw128);  // K as MN-major A (M = d)
+      const uint64_t dV = make_sdesc(smem_u32(smem + oV), 16, 1024, kSw128);
+      const uint64_t dKI = make_sdesc(smem_u32(smem + oKI), 16, 1024, kSw128);
+      const uint64_t dKIt = make_sdesc(smem_u32(smem + oKI), kChunk, 1024, kSw128);
+      const uint64_t dG = make_sdesc(smem_u32(smem + oG), 16, 1024, kSw128);        // K-major operands
+      const uint64_t dGt = make_sdesc(smem_u32(smem + oG), kChunk, 1024, kSw128);   // MN-major operands
+      auto at = [](uint64_t d, uint32_t off) -> uint64_t { return d + (uint64_t)(off >> 4); };
+      uint32_t tj = 0;
+      bool ok = true;
+      for (int it = 0; ok; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&sh.it_full[s], ph, a.err, 611)) { ok = false; break; }
+        const int4 item = sh.item[s];
+        mbar_arrive(&sh.it_empty[s]);
+        if (item.x < 0) break;
+        const int ntiles = (item.z + npos - 1) / npos;
+        if (!mbar_wait(&sh.kv_full, it & 1, a.err, 612)) { ok = false; break; }
+        for (int j = 0; j < ntiles; ++j, ++tj) {
+          const uint32_t go = (tj & 1) * kGather;
+          const uint32_t par = tj & 1;
+          // S^T = K Q^T into R, once the tile is gathered and the last dQ^T has been read out
+          if (!mbar_wait(&sh.g_full[tj & 1], (tj >> 1) & 1, a.err, 613)) { ok = false; break; }
+          if (!mbar_wait(&sh.r_free, par ^ 1, a.err, 614)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
+            umma_bf16_ss(tmem + cR, at(dK, o), at(dG, go + oQ + o), id_s, ks > 0);
+          }
+          // X^T = KI QI^T into P, once the last dq_idx^T has been read out
+          if (!mbar_wait(&sh.x_free, par ^ 1, a.err, 615)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks) umma_bf16_ss(tmem + cP, at(dKI, ks * 32), at(dG, go + oQI + ks * 32), id_x, ks > 0);
+          umma_commit(&sh.s_full);
+          // dP^T = V dO^T into R, once every epilogue warp has loaded S^T and X^T
+          if (!mbar_wait(&sh.s_read, par, a.err, 616)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
+            umma_bf16_ss(tmem + cR, at(dV, o), at(dG, go + oDO + o), id_s, ks > 0);
+          }
+          umma_commit(&sh.dp_full);
+          // dV += P^T dO with P^T from TMEM (K = 128 rows, 16 per step)
+          if (!mbar_wait(&sh.p_ready, par, a.err, 617)) { ok = false; break; }
+          if (j == 0 && !mbar_wait(&sh.acc_free, (it & 1) ^ 1, a.err, 618)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t acc = j > 0 ? 1u : 0u;
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ts(tmem + cDV, tmem + cP + ks * 8, at(dGt, go + oDO + ks * 2048), id_acc, acc | (ks > 0));
+          umma_commit(&sh.pv_done);
+          // dK += dS^T Q (dS^T where dO was), then dQ^T = K^T dS^T into R
+          if (!mbar_wait(&sh.ds_ready, par, a.err, 619)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
+            umma_bf16_ss(tmem + cDK, at(dG, go + oDO + o), at(dGt, go + oQ + ks * 2048), id_acc, acc | (ks > 0));
+          }
+          umma_commit(&sh.dk_done);
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ss(tmem + cR, at(dKt, ks * 2048), at(dGt, go + oDO + ks * 2048), id_dq, ks > 0);
+          umma_commit(&sh.dq_full);
+          // index branch: dk_idx += gs^T QI, dq_idx^T = KI^T gs^T into P (gs^T where Q was)
+          if (!mbar_wait(&sh.gs_ready, par, a.err, 620)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int ks = 0; ks < npos / 16; ++ks)
+            umma_bf16_ss(tmem + cKI, at(dG, go + oQ + ks * 32), at(dGt, go + oQI + ks * 2048), id_ki, acc | (ks > 0));
+#pragma unroll 1
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ss(tmem + cP, at(dKIt, ks * 2048), at(dGt, go + oQ + ks * 2048), id_dqi, ks > 0);
+          umma_commit(&sh.ph2_full);
+        }
+        umma_commit(&sh.kv_empty);
+      }
+      if (!ok) *abort_flag = 1;
+    }
+  }
+  } else {
+    regs_alloc192();
+    // ------------------------------------------------------------ epilogue (thread = TMEM lane)
+    const int quarter = warp & 3;
+    const int hf = (warp >> 2) & 1;
+    const int col0 = 64 * hf;                // this half's tile rows
+    const int kk = quarter * 32 + lane;      // TMEM lane: key (S, dP, P, X), d (dQ^T), e (dq_idx^T)
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const bool kl_writer = warp == 8;
+    uint32_t tj = 0;
+    bool ok = true;
+    int rel_gb = -1;  // gather buffer whose partial stores must finish reading before it is handed back
+    for (int it = 0; ok; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (!mbar_wait(&sh.it_full[s], ph, a.err, 621)) { ok = false; break; }
+      const int4 item = sh.item[s];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.it_empty[s]);
+      if (item.x < 0) break;
+      int b, g, c;
+      decode_list(item.x, a.n, a.G, b, g, c);
+      const int key = c * 128 + kk;
+      const int ntiles = (item.z + npos - 1) / npos;
+      for (int j = 0; j < ntiles; ++j, ++tj) {
+        const int gb = tj & 1;
+        const uint32_t par = tj & 1;
+        uint8_t* buf = smem + oG + gb * kGather;
+        const RowMeta& m = sh.meta[gb];
+        if (!mbar_wait(&sh.g_full[gb], (tj >> 1) & 1, a.err, 622)) { ok = false; break; }
+        if (!mbar_wait(&sh.s_full, par, a.err, 623)) { ok = false; break; }
+        tc_fence_after();
+        const int4 dg0 = *reinterpret_cast<const int4*>(m.diag);
+        const int4 dg1 = *reinterpret_cast<const int4*>(m.diag + 4);
+        const bool masked = (dg0.x | dg0.y | dg0.z | dg0.w | dg1.x | dg1.y | dg1.z | dg1.w) != 0;
+        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; P^T into TMEM
+        float pv[64];
+        float xv[kHQ];
+        tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float sv[32];
+          tmem_ld32(tmem + lane_off + cR + col0 + 32 * h2, sv);
+          tmem_wait_ld();
+          const float4* l4 = reinterpret_cast<const float4*>(m.lse2 + col0 + 32 * h2);
+          if (!masked) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 l = l4[i];
+              pv[32 * h2 + 4 * i + 0] = fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x));
+              pv[32 * h2 + 4 * i + 1] = fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y));
+              pv[32 * h2 + 4 * i + 2] = fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z));
+              pv[32 * h2 + 4 * i + 3] = fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w));
+            }
+          } else {
+            const int4* e4 = reinterpret_cast<const int4*>(m.ent + col0 + 32 * h2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 l = l4[i];
+              const int4 e = e4[i];
+              pv[32 * h2 + 4 * i + 0] = key <= (e.x >> 8) ? fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x)) : 0.f;
+              pv[32 * h2 + 4 * i + 1] = key <= (e.y >> 8) ? fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y)) : 0.f;
+              pv[32 * h2 + 4 * i + 2] = key <= (e.z >> 8) ? fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z)) : 0.f;
+              pv[32 * h2 + 4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_read);  // R may take dP^T; P may take P^T once all warps are here
+        if (!mbar_wait(&sh.s_read, par, a.err, 624)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t pk[32];  // this key's P^T row over the half's 64 rows, bf16 pairs (low half = even row)
+#pragma unroll
+          for (int z = 0; z < 32; ++z) pk[z] = pack_bf16(pv[2 * z], pv[2 * z + 1]);
+          tmem_st32(tmem + lane_off + cP + 32 * hf, pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.p_ready);
+        // the previous tile's partial stores have had a whole stage to read their staging:
+        // hand that gather buffer back to the producers
+        if (rel_gb >= 0) {
+          if (lane == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sh.g_empty[rel_gb]);
+          }
+          __syncwarp();
+          rel_gb = -1;
+        }
+        // ---- stage B: dS = P (dP - D) * scale, bf16, into the dO area once dV has read it
+        {
+          uint32_t dsk[32];
+          if (!mbar_wait(&sh.dp_full, par, a.err, 625)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float dp[32];
+            tmem_ld32(tmem + lane_off + cR + col0 + 32 * h2, dp);
+            tmem_wait_ld();
+            const float4* d4 = reinterpret_cast<const float4*>(m.dsc + col0 + 32 * h2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 dv = d4[i];
+              const int r = 32 * h2 + 4 * i;
+              dsk[16 * h2 + 2 * i] = pack_bf16(pv[r] * fmaf(dp[4 * i], a.scale, -dv.x),
+                                               pv[r + 1] * fmaf(dp[4 * i + 1], a.scale, -dv.y));
+              dsk[16 * h2 + 2 * i + 1] = pack_bf16(pv[r + 2] * fmaf(dp[4 * i + 2], a.scale, -dv.z),
+                                                   pv[r + 3] * fmaf(dp[4 * i + 3], a.scale, -dv.w));
+            }
+          }
+          if (!mbar_wait(&sh.pv_done, par, a.err, 626)) { ok = false; break; }
+          uint8_t* dst = buf + oDO + hf * kChunk;  // dS^T rows [64 hf, 64 hf + 64) of key kk
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc)
+            *reinterpret_cast<uint4*>(dst + sw128_off(kk, cc)) =
+                make_uint4(dsk[4 * cc], dsk[4 * cc + 1], dsk[4 * cc + 2], dsk[4 * cc + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.ds_ready);
+        }
+        // ---- stage C: index branch; X^T and gs^T have one column per query
+        {
+          float term[kHQ];
+          uint32_t gp[kHQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs
+#pragma unroll
+          for (int qq = 0; qq < kHQ; ++qq) {
+            const int r = qq * hg;  // the query's first head row in this half
+            float pm = 0.f;
+#pragma unroll
+            for (int h = 0; h < hg; ++h) pm += pv[r + h];
+            pm *= 1.f / (float)hg;
+            const float lpx2 = fmaf(xv[qq], a.scale_idx_log2, -m.lpx2[col0 + r]);  // log2 p_px
+            float ppx = fast_exp2(lpx2);
+            if (masked && key > (m.ent[col0 + r] >> 8)) ppx = 0.f;
+            const float gsv = a.kl_weight * (ppx - pm) * a.scale_idx;
+            const uint32_t bits = pack_bf16(gsv, 0.f) & 0xffffu;
+            if (qq & 1) gp[qq >> 1] |= bits << 16;
+            else gp[qq >> 1] = bits;
+            term[qq] = pm > 0.f ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
+          }
+          if (!mbar_wait(&sh.dk_done, par, a.err, 627)) { ok = false; break; }
+#pragma unroll
+          for (int cc = 0; cc < kHQ / 8; ++cc)
+            *reinterpret_cast<uint4*>(buf + oQ + sw128_off(kk, hf * (kHQ / 8) + cc)) =
+                make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.gs_ready);
+          // KL terms summed over the 128 keys: lanes by a butterfly, the four
+          // key quarters by shared atomics into the tile's cleared sums
+          if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
+          lanes_sum_add<kHQ>(term, lane, sh.kl_acc + hf * kHQ);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.kl_ready);
+        }
+        // ---- stage D: read out dQ^T (lane = d) and dq_idx^T (lane = e < 64) as bf16 slot partials
+        {
+          const int pos0 = item.w + j * npos;  // padded entry of the tile's first query
+          if (!mbar_wait(&sh.dq_full, par, a.err, 629)) { ok = false; break; }
+          tc_fence_after();
+          __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(buf + oDO + (hf * 4 + quarter) * 4096);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float dq[32];
+            tmem_ld32(tmem + lane_off + cR + col0 + 32 * h2, dq);
+            tmem_wait_ld();
+            if (h2 == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sh.r_free);  // R may take the next tile's S^T
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stg[(32 * h2 + i) * 32 + lane] = __float2bfloat16_rn(dq[i]);
+          }
+          if (!mbar_wait(&sh.ph2_full, par, a.err, 630)) { ok = false; break; }
+          tc_fence_after();
+          __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(buf + oQ + 16384 + (hf * 2 + (quarter & 1)) * (kHQ * 64));
+          if (quarter < 2) {
+            float dqi[kHQ];
+            tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, dqi);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < kHQ; ++i) stq[i * 32 + lane] = __float2bfloat16_rn(dqi[i]);
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(&sh.x_free);  // P may take the next tile's X^T
+            tma_store_2d(&map_dq, stg, quarter * 32, pos0 * hg + col0);
+            if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kHQ);
+            bulk_commit();
+          }
+          rel_gb = gb;
+          if (kl_writer) {  // every epilogue warp has added its KL terms: write the per-query sums
+            if (!mbar_wait(&sh.kl_ready, par, a.err, 631)) { ok = false; break; }
+            for (int q = lane; q < npos; q += 32) {
+              const int e = m.ent[q * hg];
+              if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
+              sh.kl_acc[q] = 0.f;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.kl_free);
+          }
+        }
+      }
+      if (!ok) break;
+      // ---- list end: dV, dK (columns [64 hf, 64 hf + 64)) and dk_idx ([32 hf, 32 hf + 32)), lane = key
+      {
+        const size_t orow = ((size_t)b * a.T + key) * a.G + g;
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int d0 = 64 * hf + 32 * q;
+          tmem_ld32(tmem + lane_off + cDV + d0, v);
+          tmem_wait_ld();
+          float4* dst = reinterpret_cast<float4*>(a.dV + orow * 128 + d0);
+#pragma unroll
+          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+          tmem_ld32(tmem + lane_off + cDK + d0, v);
+          tmem_wait_ld();
+          dst = reinterpret_cast<float4*>(a.dK + orow * 128 + d0);
+#pragma unroll
+          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+        }
+        float* dki = a.dki_part + (((size_t)b * a.G + g) * a.T + key) * 64 + 32 * hf;
+        tmem_ld32(tmem + lane_off + cKI + 32 * hf, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int z = 0; z < 8; ++z)
+          reinterpret_cast<float4*>(dki)[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.acc_free);
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+    if (!ok) *abort_flag = 1;
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mki,
+                            const CUtensorMap& mdq, const CUtensorMap& mdqi, const CUtensorMap& mq,
+                            const CUtensorMap& mdo, const CUtensorMap& mqi, cudaStream_t st) {
+  static bool attr[kMaxDevices] = {};  // kernel attributes are per device context
+  const int dslot = device_slot();
+  cudaError_t e;
+  if (!attr[dslot]) {
+    for (auto f : {bwd_wide_kernel<4>, bwd_wide_kernel<8>}) {
+      if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess) return e;
+      // the 64 / 192 register split redistributes exactly the 128 x 512 registers the block is launched
+      // with; any other launch count would leave the epilogue's increase waiting for registers
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, f)) != cudaSuccess) return e;
+      if (fa.numRegs != 128) return cudaErrorInvalidConfiguration;
+    }
+    attr[dslot] = true;
+  }
+  if (a.hg == 4)
+    bwd_wide_kernel<4><<<num_sms(), kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+  else
+    bwd_wide_kernel<8><<<num_sms(), kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+  return cudaGetLastError();
+}
+
+}  // namespace msa
