@@ -37,8 +37,8 @@
 // where Q was (once dK has read it), and the dQ / dq_idx partials are staged
 // there for their TMA stores.
 //
-// Warp roles (512 threads, one CTA per SM, persistent; registers split 64 /
-// 192 between the first two warpgroups and the last two):
+// Warp roles (512 threads, one CTA per SM, persistent; registers split 72 /
+// 184 between the first two warpgroups and the last two):
 //   warp 0       TMEM owner, UMMA issuer (one thread)
 //   warps 1-7    producers 0-6: producer p gathers the queries p, p + 7, ...
 //                of every tile (TMA boxes of their hg head rows of Q and dO,
@@ -85,7 +85,8 @@ struct Shared {
   uint64_t it_full[2], it_empty[2];
   uint64_t kv_full, kv_empty;
   uint64_t g_full[2], g_empty[2];
-  uint64_t s_full, s_read, dp_full, p_ready, pv_done, ds_ready, dk_done, gs_ready, dq_full, ph2_full;
+  uint64_t s_full, x_full, s_read, x_read, dp_full, dp_read, p_ready, pv_done, ds_tmem, ds_smem, dk_done;
+  uint64_t gs_ready, dq_full, ph2_full;
   uint64_t r_free, x_free, acc_free, kl_ready, kl_free;
   RowMeta meta[2];
   float kl_acc[32];
@@ -97,8 +98,8 @@ constexpr int kSmem = oSh + (int)sizeof(Shared);
 static_assert(kGather % 1024 == 0, "gather buffers keep the 1024-byte swizzle alignment");
 static_assert(kSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
 
-__device__ __forceinline__ void regs_dealloc64() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory"); }
-__device__ __forceinline__ void regs_alloc192() { asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory"); }
+__device__ __forceinline__ void regs_dealloc72() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory"); }
+__device__ __forceinline__ void regs_alloc184() { asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory"); }
 
 // Stores 32 fp32 values as 32 consecutive columns of the thread's TMEM lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -142,11 +143,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.kv_full, 1);
     mbar_init(&sh.kv_empty, 1);
     mbar_init(&sh.s_full, 1);
+    mbar_init(&sh.x_full, 1);
     mbar_init(&sh.s_read, 8);
+    mbar_init(&sh.x_read, 8);
     mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.dp_read, 8);
     mbar_init(&sh.p_ready, 8);
     mbar_init(&sh.pv_done, 1);
-    mbar_init(&sh.ds_ready, 8);
+    mbar_init(&sh.ds_tmem, 8);
+    mbar_init(&sh.ds_smem, 8);
     mbar_init(&sh.dk_done, 1);
     mbar_init(&sh.gs_ready, 8);
     mbar_init(&sh.dq_full, 1);
@@ -171,9 +176,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_items = *a.n_items;
 
   // The register split is set where it dominates each role's code, so that
-  // the compiler gives the epilogue its 192 registers.
+  // the compiler gives the epilogue its 184 registers.
   if (warp < 8) {
-  regs_dealloc64();
+  regs_dealloc72();
   if (warp >= 1) {
     // ------------------------------------------------------------ producers
     const int p = warp - 1;
@@ -337,13 +342,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
             umma_bf16_ss(tmem + cR, at(dK, o), at(dG, go + oQ + o), id_s, ks > 0);
           }
+          umma_commit(&sh.s_full);
           // X^T = KI QI^T into P, once the last dq_idx^T has been read out
           if (!mbar_wait(&sh.x_free, par ^ 1, a.err, 615)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
           for (int ks = 0; ks < 4; ++ks) umma_bf16_ss(tmem + cP, at(dKI, ks * 32), at(dG, go + oQI + ks * 32), id_x, ks > 0);
-          umma_commit(&sh.s_full);
-          // dP^T = V dO^T into R, once every epilogue warp has loaded S^T and X^T
+          umma_commit(&sh.x_full);
+          // dP^T = V dO^T into R, once every epilogue warp has loaded S^T
           if (!mbar_wait(&sh.s_read, par, a.err, 616)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
@@ -361,15 +367,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ts(tmem + cDV, tmem + cP + ks * 8, at(dGt, go + oDO + ks * 2048), id_acc, acc | (ks > 0));
           umma_commit(&sh.pv_done);
-          // dK += dS^T Q (dS^T where dO was), then dQ^T = K^T dS^T into R
-          if (!mbar_wait(&sh.ds_ready, par, a.err, 619)) { ok = false; break; }
+          // dK += dS^T Q with dS^T from TMEM (packed bf16 in R's first 64 columns, K = 128 rows)
+          if (!mbar_wait(&sh.ds_tmem, par, a.err, 619)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
-            umma_bf16_ss(tmem + cDK, at(dG, go + oDO + o), at(dGt, go + oQ + ks * 2048), id_acc, acc | (ks > 0));
-          }
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ts(tmem + cDK, tmem + cR + ks * 8, at(dGt, go + oQ + ks * 2048), id_acc, acc | (ks > 0));
           umma_commit(&sh.dk_done);
+          // dQ^T = K^T dS^T into R, with dS^T's shared-memory copy (where dO was): it is the B operand
+          if (!mbar_wait(&sh.ds_smem, par, a.err, 632)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll 1
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ss(tmem + cR, at(dKt, ks * 2048), at(dGt, go + oDO + ks * 2048), id_dq, ks > 0);
@@ -391,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    regs_alloc192();
+    regs_alloc184();
     // ------------------------------------------------------------ epilogue (thread = TMEM lane)
     const int quarter = warp & 3;
     const int hf = (warp >> 2) & 1;
@@ -401,7 +408,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool kl_writer = warp == 8;
     uint32_t tj = 0;
     bool ok = true;
-    int rel_gb = -1;  // gather buffer whose partial stores must finish reading before it is handed back
     for (int it = 0; ok; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -425,24 +431,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 dg0 = *reinterpret_cast<const int4*>(m.diag);
         const int4 dg1 = *reinterpret_cast<const int4*>(m.diag + 4);
         const bool masked = (dg0.x | dg0.y | dg0.z | dg0.w | dg1.x | dg1.y | dg1.z | dg1.w) != 0;
-        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; P^T into TMEM
+        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; P^T into TMEM.
+        // S^T is released to the tensor core (for dP^T) as soon as it is in registers.
         float pv[64];
         float xv[kHQ];
-        tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
+        tmem_ld32(tmem + lane_off + cR + col0, *reinterpret_cast<float(*)[32]>(pv));
+        tmem_ld32(tmem + lane_off + cR + col0 + 32, *reinterpret_cast<float(*)[32]>(pv + 32));
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.s_read);  // R may take dP^T
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
-          float sv[32];
-          tmem_ld32(tmem + lane_off + cR + col0 + 32 * h2, sv);
-          tmem_wait_ld();
           const float4* l4 = reinterpret_cast<const float4*>(m.lse2 + col0 + 32 * h2);
+          float* sv = pv + 32 * h2;
           if (!masked) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 l = l4[i];
-              pv[32 * h2 + 4 * i + 0] = fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x));
-              pv[32 * h2 + 4 * i + 1] = fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y));
-              pv[32 * h2 + 4 * i + 2] = fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z));
-              pv[32 * h2 + 4 * i + 3] = fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w));
+              sv[4 * i + 0] = fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x));
+              sv[4 * i + 1] = fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y));
+              sv[4 * i + 2] = fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z));
+              sv[4 * i + 3] = fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w));
             }
           } else {
             const int4* e4 = reinterpret_cast<const int4*>(m.ent + col0 + 32 * h2);
@@ -450,17 +460,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 8; ++i) {
               const float4 l = l4[i];
               const int4 e = e4[i];
-              pv[32 * h2 + 4 * i + 0] = key <= (e.x >> 8) ? fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x)) : 0.f;
-              pv[32 * h2 + 4 * i + 1] = key <= (e.y >> 8) ? fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y)) : 0.f;
-              pv[32 * h2 + 4 * i + 2] = key <= (e.z >> 8) ? fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z)) : 0.f;
-              pv[32 * h2 + 4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
+              sv[4 * i + 0] = key <= (e.x >> 8) ? fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x)) : 0.f;
+              sv[4 * i + 1] = key <= (e.y >> 8) ? fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y)) : 0.f;
+              sv[4 * i + 2] = key <= (e.z >> 8) ? fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z)) : 0.f;
+              sv[4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
             }
           }
         }
+        // X^T leaves the P columns once every epilogue warp has it in registers
+        if (!mbar_wait(&sh.x_full, par, a.err, 633)) { ok = false; break; }
+        tc_fence_after();
+        tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
+        tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.s_read);  // R may take dP^T; P may take P^T once all warps are here
-        if (!mbar_wait(&sh.s_read, par, a.err, 624)) { ok = false; break; }
+        if (lane == 0) mbar_arrive(&sh.x_read);
+        if (!mbar_wait(&sh.x_read, par, a.err, 624)) { ok = false; break; }
         tc_fence_after();
         {
           uint32_t pk[32];  // this key's P^T row over the half's 64 rows, bf16 pairs (low half = even row)
@@ -472,17 +487,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.p_ready);
-        // the previous tile's partial stores have had a whole stage to read their staging:
-        // hand that gather buffer back to the producers
-        if (rel_gb >= 0) {
-          if (lane == 0) {
-            bulk_wait_read_all();
-            mbar_arrive(&sh.g_empty[rel_gb]);
-          }
-          __syncwarp();
-          rel_gb = -1;
-        }
-        // ---- stage B: dS = P (dP - D) * scale, bf16, into the dO area once dV has read it
+        // ---- stage B: dS = P (dP - D) * scale, bf16. Packed into R's first 64 columns (the
+        // TMEM A operand of dK) once every warp has loaded dP^T, and copied into the dO area
+        // (the B operand of dQ^T) once dV has read dO
         {
           uint32_t dsk[32];
           if (!mbar_wait(&sh.dp_full, par, a.err, 625)) { ok = false; break; }
@@ -503,6 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                    pv[r + 3] * fmaf(dp[4 * i + 3], a.scale, -dv.w));
             }
           }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.dp_read);
+          if (!mbar_wait(&sh.dp_read, par, a.err, 634)) { ok = false; break; }
+          tc_fence_after();
+          tmem_st32(tmem + lane_off + cR + 32 * hf, dsk);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.ds_tmem);
           if (!mbar_wait(&sh.pv_done, par, a.err, 626)) { ok = false; break; }
           uint8_t* dst = buf + oDO + hf * kChunk;  // dS^T rows [64 hf, 64 hf + 64) of key kk
 #pragma unroll
@@ -511,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(dsk[4 * cc], dsk[4 * cc + 1], dsk[4 * cc + 2], dsk[4 * cc + 3]);
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.ds_ready);
+          if (lane == 0) mbar_arrive(&sh.ds_smem);
         }
         // ---- stage C: index branch; X^T and gs^T have one column per query
         {
@@ -586,7 +603,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kHQ);
             bulk_commit();
           }
-          rel_gb = gb;
           if (kl_writer) {  // every epilogue warp has added its KL terms: write the per-query sums
             if (!mbar_wait(&sh.kl_ready, par, a.err, 631)) { ok = false; break; }
             for (int q = lane; q < npos; q += 32) {
@@ -597,6 +613,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.kl_free);
           }
+          // the buffer goes back to the producers once this warp's partial stores have read it
+          if (lane == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sh.g_empty[gb]);
+          }
+          __syncwarp();
         }
       }
       if (!ok) break;
@@ -650,7 +672,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUten
   if (!attr[dslot]) {
     for (auto f : {bwd_wide_kernel<4>, bwd_wide_kernel<8>}) {
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess) return e;
-      // the 64 / 192 register split redistributes exactly the 128 x 512 registers the block is launched
+      // the 72 / 184 register split redistributes exactly the 128 x 512 registers the block is launched
       // with; any other launch count would leave the epilogue's increase waiting for registers
       cudaFuncAttributes fa;
       if ((e = cudaFuncGetAttributes(&fa, f)) != cudaSuccess) return e;
