@@ -316,6 +316,57 @@ __host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same descriptor as two 32-bit words, for MMA issue loops that must stay
+// a few instructions long (one thread issues every MMA, sharing its scheduler
+// with busy epilogue warps). All operands with SBO = 1024 and 128-byte swizzle
+// share the high word; the low word holds the start address (16-byte units)
+// and the leading byte offset, so adding (byte offset >> 4) to it moves the
+// start address with a single 32-bit add (no carry out of the 14-bit field
+// while addresses stay below 256 KB, the shared-memory window).
+__host__ __device__ constexpr uint32_t sdesc_hi_sw128_sbo1024() {
+  return (1024u >> 4) | (1u << 14) | ((uint32_t)kSw128 << 29);
+}
+// High word for a given stride byte offset and swizzle mode.
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo_bytes, uint32_t swz) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | ((swz & 7u) << 29);
+}
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+
+// umma_bf16_ss / umma_bf16_ts with the shared-memory descriptors given as (low word, high word).
+__device__ __forceinline__ void umma_bf16_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %3};\n\tmov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The same with separate high words for A and B (operands of different swizzle or stride).
+__device__ __forceinline__ void umma_bf16_ss_w2(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                                uint32_t b_hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+      "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+      "mov.b64 db, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Byte offset of element (row r, 16-byte chunk c) inside a K-major tile with
 // 128-byte swizzle: rows of 128 B, 8-row atoms of 1024 B (the TMA SWIZZLE_128B image).
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c16) {

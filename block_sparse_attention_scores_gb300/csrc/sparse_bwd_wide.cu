@@ -37,8 +37,8 @@
 // where Q was (once dK has read it), and the dQ / dq_idx partials are staged
 // there for their TMA stores.
 //
-// Warp roles (512 threads, one CTA per SM, persistent; registers split 72 /
-// 184 between the first two warpgroups and the last two):
+// Warp roles (512 threads, one CTA per SM, persistent; registers split 64 /
+// 192 between the first two warpgroups and the last two):
 //   warp 0       TMEM owner, UMMA issuer (one thread)
 //   warps 1-7    producers 0-6: producer p gathers the queries p, p + 7, ...
 //                of every tile (TMA boxes of their hg head rows of Q and dO,
@@ -69,15 +69,19 @@ constexpr int oK = 0, oV = kKV, oKI = 2 * kKV, oG = 2 * kKV + kKIb;
 constexpr int oQ = 0, oDO = 2 * kChunk, oQI = 4 * kChunk;  // inside a gather buffer
 constexpr int kQIb = 4096;                                  // up to 32 q_idx rows
 constexpr int kGather = oQI + kQIb;
-constexpr int oSh = oG + 2 * kGather;
+// gs^T of the current tile: 128 keys x (queries per tile) bf16, 64-byte rows with 64-byte swizzle
+// (4 heads per group, 32 queries) or 32-byte rows with 32-byte swizzle (8 heads, 16 queries)
+constexpr int oGS = oG + 2 * kGather;
+constexpr int kGSb = 8192;
+constexpr int oSh = oGS + kGSb;
 // TMEM columns
 constexpr uint32_t cR = 0, cP = 128, cDV = 192, cDK = 320, cKI = 448;
 
 struct __align__(16) RowMeta {
-  float lse2[kRows];  // LSE * log2 e (+inf for padding rows: P = 0 there)
-  float dsc[kRows];   // D * scale
-  float lpx2[kRows];  // lse_px * log2 e (+inf for padding rows)
-  int ent[kRows];     // entry bits t << 8 | slot, -1 for padding
+  float lse2[kRows];  // per (query, head) row: LSE * log2 e (+inf for padding rows: P = 0 there)
+  float dsc[kRows];   // per row: D * scale
+  float lpx2[32];     // per query: lse_px * log2 e (+inf for padding queries)
+  int ent[32];        // per query: entry bits t << 8 | slot, -1 for padding
   int diag[8];        // per producer: some row sees only part of the block (causal mask needed)
 };
 
@@ -98,8 +102,14 @@ constexpr int kSmem = oSh + (int)sizeof(Shared);
 static_assert(kGather % 1024 == 0, "gather buffers keep the 1024-byte swizzle alignment");
 static_assert(kSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
 
-__device__ __forceinline__ void regs_dealloc72() { asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n" ::: "memory"); }
-__device__ __forceinline__ void regs_alloc184() { asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory"); }
+// The value unchanged, through an instruction the compiler cannot see through.
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
+  asm volatile("mov.b32 %0, %0;" : "+r"(x));
+  return x;
+}
+
+__device__ __forceinline__ void regs_dealloc64() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory"); }
+__device__ __forceinline__ void regs_alloc192() { asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory"); }
 
 // Stores 32 fp32 values as 32 consecutive columns of the thread's TMEM lane.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -124,6 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int hg = HG;
   constexpr int npos = kRows / HG;  // queries per tile (32 or 16)
   constexpr int kHQ = npos / 2;     // queries of one epilogue half
+  constexpr uint32_t kGsRow = npos * 2;       // bytes of one key's gs^T row
+  constexpr uint32_t kGsAtom = 8 * kGsRow;    // 8-row swizzle atom
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {  // uniform for the block: nothing started yet
     if (threadIdx.x == 0) dev_fail(a.err, kDevSmemAlign, 600);
@@ -157,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.dq_full, 1);
     mbar_init(&sh.ph2_full, 1);
     mbar_init(&sh.r_free, 8);
-    mbar_init(&sh.x_free, 8);
+    mbar_init(&sh.x_free, 4);  // the warps of TMEM lanes 0..63, which hold dq_idx^T
     mbar_init(&sh.acc_free, 8);
     mbar_init(&sh.kl_ready, 8);
     mbar_init(&sh.kl_free, 1);
@@ -176,9 +188,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_items = *a.n_items;
 
   // The register split is set where it dominates each role's code, so that
-  // the compiler gives the epilogue its 184 registers.
+  // the compiler gives the epilogue its 192 registers.
   if (warp < 8) {
-  regs_dealloc72();
+  regs_dealloc64();
   if (warp >= 1) {
     // ------------------------------------------------------------ producers
     const int p = warp - 1;
@@ -267,8 +279,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = qmine * hg + hmine;
           m.lse2[r] = rec.x;
           m.dsc[r] = rec.y;
-          m.lpx2[r] = rec.z;
-          m.ent[r] = e_own;
+          if (hmine == 0) {
+            m.lpx2[qmine] = rec.z;
+            m.ent[qmine] = e_own;
+          }
         }
         const unsigned dg = __ballot_sync(0xffffffffu, mine && e_own >= 0 && (e_own >> 8) < key_last);
         if (lane == 0) {
@@ -283,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int o = lane; o < nq * 5; o += 32) {
           const int i = o / 5, op = o - i * 5;
           const int q = p + kProd * i;
-          const int e = m.ent[q * hg];
+          const int e = m.ent[q];
           const int bt = e >= 0 ? b * a.T + (e >> 8) : BT;
           if (op < 4) {
             const int which = op >> 1, chunk = op & 1;
@@ -310,15 +324,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_x = make_idesc_bf16(128, npos, false, false);
       constexpr uint32_t id_ki = make_idesc_bf16(128, 64, false, true);
       constexpr uint32_t id_dqi = make_idesc_bf16(128, npos, true, true);
-      // descriptors built once; a k-step or the other gather buffer moves only the start address
-      const uint64_t dK = make_sdesc(smem_u32(smem + oK), 16, 1024, kSw128);       // K, K-major
-      const uint64_t dKt = make_sdesc(smem_u32(smem + oK), kChunk, 1024, kSw128);  // K as MN-major A (M = d)
-      const uint64_t dV = make_sdesc(smem_u32(smem + oV), 16, 1024, kSw128);
-      const uint64_t dKI = make_sdesc(smem_u32(smem + oKI), 16, 1024, kSw128);
-      const uint64_t dKIt = make_sdesc(smem_u32(smem + oKI), kChunk, 1024, kSw128);
-      const uint64_t dG = make_sdesc(smem_u32(smem + oG), 16, 1024, kSw128);        // K-major operands
-      const uint64_t dGt = make_sdesc(smem_u32(smem + oG), kChunk, 1024, kSw128);   // MN-major operands
-      auto at = [](uint64_t d, uint32_t off) -> uint64_t { return d + (uint64_t)(off >> 4); };
+      // Descriptors as 32-bit low words sharing one high word (SBO 1024, 128-byte swizzle): every
+      // MMA below is one or two immediate adds and the issue, so that this thread, which shares its
+      // scheduler with two epilogue warps, keeps the tensor pipe fed at its N = 128 rate.
+      constexpr uint32_t hi = sdesc_hi_sw128_sbo1024();
+      const uint32_t kA0 = sdesc_lo(smem_u32(smem + oK), 16);        // K, K-major
+      const uint32_t kT0 = sdesc_lo(smem_u32(smem + oK), kChunk);    // K as MN-major A (M = d)
+      const uint32_t vA0 = sdesc_lo(smem_u32(smem + oV), 16);
+      const uint32_t iA0 = sdesc_lo(smem_u32(smem + oKI), 16);
+      const uint32_t iT0 = sdesc_lo(smem_u32(smem + oKI), kChunk);
+      const uint32_t gA0 = sdesc_lo(smem_u32(smem + oG), 16);       // gather-buffer operands, K-major
+      const uint32_t gT0 = sdesc_lo(smem_u32(smem + oG), kChunk);   // and MN-major
+      // gs^T: rows of npos bf16 (64 or 32 bytes), atoms of 8 rows; K-major A of dk_idx and MN-major B
+      // of dq_idx^T (one atom wide) from the same image
+      constexpr uint32_t hiGS = sdesc_hi(kGsAtom, npos == 32 ? kSw64 : kSw32);
+      const uint32_t gsA = sdesc_lo(smem_u32(smem + oGS), 16);
+      const uint32_t gsB = sdesc_lo(smem_u32(smem + oGS), kGSb);
       uint32_t tj = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
@@ -331,65 +352,70 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ntiles = (item.z + npos - 1) / npos;
         if (!mbar_wait(&sh.kv_full, it & 1, a.err, 612)) { ok = false; break; }
         for (int j = 0; j < ntiles; ++j, ++tj) {
-          const uint32_t go = (tj & 1) * kGather;
           const uint32_t par = tj & 1;
+          const uint32_t gA = gA0 + ((tj & 1) * kGather >> 4), gT = gT0 + ((tj & 1) * kGather >> 4);
+          // per-tile copies the compiler cannot hoist: otherwise it keeps every base + k-step sum of
+          // the tile loop live in registers across it
+          const uint32_t kA = opaque_u32(kA0), kT = opaque_u32(kT0), vA = opaque_u32(vA0);
+          const uint32_t iA = opaque_u32(iA0), iT = opaque_u32(iT0);
+          // a K-major k-step inside a tile of two 64-column chunks, in descriptor units
+#define KSTEP(ks) ((uint32_t)((((ks) >> 2) * kChunk + ((ks) & 3) * 32) >> 4))
           // S^T = K Q^T into R, once the tile is gathered and the last dQ^T has been read out
           if (!mbar_wait(&sh.g_full[tj & 1], (tj >> 1) & 1, a.err, 613)) { ok = false; break; }
           if (!mbar_wait(&sh.r_free, par ^ 1, a.err, 614)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
-            umma_bf16_ss(tmem + cR, at(dK, o), at(dG, go + oQ + o), id_s, ks > 0);
-          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ss_w(tmem + cR, kA + KSTEP(ks), gA + (oQ >> 4) + KSTEP(ks), hi, id_s, ks > 0);
           umma_commit(&sh.s_full);
           // X^T = KI QI^T into P, once the last dq_idx^T has been read out
           if (!mbar_wait(&sh.x_free, par ^ 1, a.err, 615)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll 1
-          for (int ks = 0; ks < 4; ++ks) umma_bf16_ss(tmem + cP, at(dKI, ks * 32), at(dG, go + oQI + ks * 32), id_x, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16_ss_w(tmem + cP, iA + 2 * ks, gA + (oQI >> 4) + 2 * ks, hi, id_x, ks > 0);
           umma_commit(&sh.x_full);
           // dP^T = V dO^T into R, once every epilogue warp has loaded S^T
           if (!mbar_wait(&sh.s_read, par, a.err, 616)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll 1
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t o = (ks >> 2) * kChunk + (ks & 3) * 32;
-            umma_bf16_ss(tmem + cR, at(dV, o), at(dG, go + oDO + o), id_s, ks > 0);
-          }
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ss_w(tmem + cR, vA + KSTEP(ks), gA + (oDO >> 4) + KSTEP(ks), hi, id_s, ks > 0);
           umma_commit(&sh.dp_full);
-          // dV += P^T dO with P^T from TMEM (K = 128 rows, 16 per step)
+          // dV += P^T dO with P^T from TMEM (K = 128 rows, 16 per step; an MN-major step is 2048 bytes)
           if (!mbar_wait(&sh.p_ready, par, a.err, 617)) { ok = false; break; }
           if (j == 0 && !mbar_wait(&sh.acc_free, (it & 1) ^ 1, a.err, 618)) { ok = false; break; }
           tc_fence_after();
           const uint32_t acc = j > 0 ? 1u : 0u;
-#pragma unroll 1
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ts(tmem + cDV, tmem + cP + ks * 8, at(dGt, go + oDO + ks * 2048), id_acc, acc | (ks > 0));
+            umma_bf16_ts_w(tmem + cDV, tmem + cP + ks * 8, gT + (oDO >> 4) + 128 * ks, hi, id_acc, acc | (ks > 0));
           umma_commit(&sh.pv_done);
           // dK += dS^T Q with dS^T from TMEM (packed bf16 in R's first 64 columns, K = 128 rows)
           if (!mbar_wait(&sh.ds_tmem, par, a.err, 619)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll 1
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ts(tmem + cDK, tmem + cR + ks * 8, at(dGt, go + oQ + ks * 2048), id_acc, acc | (ks > 0));
+            umma_bf16_ts_w(tmem + cDK, tmem + cR + ks * 8, gT + (oQ >> 4) + 128 * ks, hi, id_acc, acc | (ks > 0));
           umma_commit(&sh.dk_done);
           // dQ^T = K^T dS^T into R, with dS^T's shared-memory copy (where dO was): it is the B operand
           if (!mbar_wait(&sh.ds_smem, par, a.err, 632)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll 1
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ss(tmem + cR, at(dKt, ks * 2048), at(dGt, go + oDO + ks * 2048), id_dq, ks > 0);
+            umma_bf16_ss_w(tmem + cR, kT + 128 * ks, gT + (oDO >> 4) + 128 * ks, hi, id_dq, ks > 0);
           umma_commit(&sh.dq_full);
-          // index branch: dk_idx += gs^T QI, dq_idx^T = KI^T gs^T into P (gs^T where Q was)
+          // index branch (gs^T written long before, in stage A): dk_idx += gs^T QI, dq_idx^T = KI^T gs^T
+          // into P, after dV has read P^T (same issuing thread: in order)
           if (!mbar_wait(&sh.gs_ready, par, a.err, 620)) { ok = false; break; }
           tc_fence_after();
-#pragma unroll 1
+#pragma unroll
           for (int ks = 0; ks < npos / 16; ++ks)
-            umma_bf16_ss(tmem + cKI, at(dG, go + oQ + ks * 32), at(dGt, go + oQI + ks * 2048), id_ki, acc | (ks > 0));
-#pragma unroll 1
+            umma_bf16_ss_w2(tmem + cKI, gsA + 2 * ks, hiGS, gT + (oQI >> 4) + 128 * ks, hi, id_ki, acc | (ks > 0));
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ss(tmem + cP, at(dKIt, ks * 2048), at(dGt, go + oQ + ks * 2048), id_dqi, ks > 0);
+            umma_bf16_ss_w2(tmem + cP, iT + 128 * ks, hi, gsB + ks * (2 * kGsAtom >> 4), hiGS, id_dqi, ks > 0);
+#undef KSTEP
           umma_commit(&sh.ph2_full);
         }
         umma_commit(&sh.kv_empty);
@@ -398,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    regs_alloc184();
+    regs_alloc192();
     // ------------------------------------------------------------ epilogue (thread = TMEM lane)
     const int quarter = warp & 3;
     const int hf = (warp >> 2) & 1;
@@ -408,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool kl_writer = warp == 8;
     uint32_t tj = 0;
     bool ok = true;
+    int rel_gb = -1;  // gather buffer whose partial stores must finish reading before it is handed back
     for (int it = 0; ok; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
@@ -431,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 dg0 = *reinterpret_cast<const int4*>(m.diag);
         const int4 dg1 = *reinterpret_cast<const int4*>(m.diag + 4);
         const bool masked = (dg0.x | dg0.y | dg0.z | dg0.w | dg1.x | dg1.y | dg1.z | dg1.w) != 0;
-        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; P^T into TMEM.
-        // S^T is released to the tensor core (for dP^T) as soon as it is in registers.
+        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; the index branch
+        // (p_main, p_px, gs, KL terms); P^T into TMEM. S^T goes back to the tensor core (for dP^T)
+        // as soon as it is in registers.
         float pv[64];
-        float xv[kHQ];
         tmem_ld32(tmem + lane_off + cR + col0, *reinterpret_cast<float(*)[32]>(pv));
         tmem_ld32(tmem + lane_off + cR + col0 + 32, *reinterpret_cast<float(*)[32]>(pv + 32));
         tmem_wait_ld();
@@ -455,26 +482,68 @@ __global__ void __launch_bounds__(kThreads, 1)
               sv[4 * i + 3] = fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w));
             }
           } else {
-            const int4* e4 = reinterpret_cast<const int4*>(m.ent + col0 + 32 * h2);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 l = l4[i];
-              const int4 e = e4[i];
-              sv[4 * i + 0] = key <= (e.x >> 8) ? fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x)) : 0.f;
-              sv[4 * i + 1] = key <= (e.y >> 8) ? fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y)) : 0.f;
-              sv[4 * i + 2] = key <= (e.z >> 8) ? fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z)) : 0.f;
-              sv[4 * i + 3] = key <= (e.w >> 8) ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
+              const bool vis = key <= (m.ent[(col0 + 32 * h2 + 4 * i) / hg] >> 8);  // 4 rows: one query
+              sv[4 * i + 0] = vis ? fast_exp2(fmaf(sv[4 * i + 0], a.scale_log2, -l.x)) : 0.f;
+              sv[4 * i + 1] = vis ? fast_exp2(fmaf(sv[4 * i + 1], a.scale_log2, -l.y)) : 0.f;
+              sv[4 * i + 2] = vis ? fast_exp2(fmaf(sv[4 * i + 2], a.scale_log2, -l.z)) : 0.f;
+              sv[4 * i + 3] = vis ? fast_exp2(fmaf(sv[4 * i + 3], a.scale_log2, -l.w)) : 0.f;
             }
           }
         }
-        // X^T leaves the P columns once every epilogue warp has it in registers
+        // X^T is complete (and, since it was issued after them, every MMA of the previous tile,
+        // the readers of the previous gs^T included)
         if (!mbar_wait(&sh.x_full, par, a.err, 633)) { ok = false; break; }
         tc_fence_after();
-        tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.x_read);
+        {
+          float xv[kHQ];
+          tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
+          tmem_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.x_read);  // X^T leaves the P columns once every warp has it
+          // index branch: X^T and gs^T have one column per query
+          float term[kHQ];
+          uint32_t gp[kHQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs
+#pragma unroll
+          for (int qq = 0; qq < kHQ; ++qq) {
+            const int r = qq * hg;          // the query's first head row in this half
+            const int q = col0 / hg + qq;   // the query in the tile
+            float pm = 0.f;
+#pragma unroll
+            for (int h = 0; h < hg; ++h) pm += pv[r + h];
+            pm *= 1.f / (float)hg;
+            const float lpx2 = fmaf(xv[qq], a.scale_idx_log2, -m.lpx2[q]);  // log2 p_px
+            float ppx = fast_exp2(lpx2);
+            if (masked && key > (m.ent[q] >> 8)) ppx = 0.f;
+            const float gsv = a.kl_weight * (ppx - pm) * a.scale_idx;
+            const uint32_t bits = pack_bf16(gsv, 0.f) & 0xffffu;
+            if (qq & 1) gp[qq >> 1] |= bits << 16;
+            else gp[qq >> 1] = bits;
+            term[qq] = pm > 0.f ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
+          }
+          // gs^T row kk: 16-byte chunks of 8 queries, swizzled like the TMA image of the same width
+          if constexpr (npos == 32) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+              *reinterpret_cast<uint4*>(smem + oGS + kk * 64 + (((2 * hf + cc) ^ ((kk >> 1) & 3)) << 4)) =
+                  make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
+          } else {
+            *reinterpret_cast<uint4*>(smem + oGS + kk * 32 + ((hf ^ ((kk >> 2) & 1)) << 4)) =
+                make_uint4(gp[0], gp[1], gp[2], gp[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.gs_ready);
+          // KL terms summed over the 128 keys: lanes by a butterfly, the four
+          // key quarters by shared atomics into the tile's cleared sums
+          if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
+          lanes_sum_add<kHQ>(term, lane, sh.kl_acc + hf * kHQ);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.kl_ready);
+        }
         if (!mbar_wait(&sh.x_read, par, a.err, 624)) { ok = false; break; }
         tc_fence_after();
         {
@@ -487,6 +556,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.p_ready);
+        // the previous tile's gather buffer: every MMA on it is done (X^T of this tile was issued after
+        // them) and its partial stores have had a stage to read their staging
+        if (rel_gb >= 0) {
+          if (lane == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sh.g_empty[rel_gb]);
+          }
+          __syncwarp();
+          rel_gb = -1;
+        }
         // ---- stage B: dS = P (dP - D) * scale, bf16. Packed into R's first 64 columns (the
         // TMEM A operand of dK) once every warp has loaded dP^T, and copied into the dO area
         // (the B operand of dQ^T) once dV has read dO
@@ -530,42 +609,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.ds_smem);
         }
-        // ---- stage C: index branch; X^T and gs^T have one column per query
-        {
-          float term[kHQ];
-          uint32_t gp[kHQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs
-#pragma unroll
-          for (int qq = 0; qq < kHQ; ++qq) {
-            const int r = qq * hg;  // the query's first head row in this half
-            float pm = 0.f;
-#pragma unroll
-            for (int h = 0; h < hg; ++h) pm += pv[r + h];
-            pm *= 1.f / (float)hg;
-            const float lpx2 = fmaf(xv[qq], a.scale_idx_log2, -m.lpx2[col0 + r]);  // log2 p_px
-            float ppx = fast_exp2(lpx2);
-            if (masked && key > (m.ent[col0 + r] >> 8)) ppx = 0.f;
-            const float gsv = a.kl_weight * (ppx - pm) * a.scale_idx;
-            const uint32_t bits = pack_bf16(gsv, 0.f) & 0xffffu;
-            if (qq & 1) gp[qq >> 1] |= bits << 16;
-            else gp[qq >> 1] = bits;
-            term[qq] = pm > 0.f ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
-          }
-          if (!mbar_wait(&sh.dk_done, par, a.err, 627)) { ok = false; break; }
-#pragma unroll
-          for (int cc = 0; cc < kHQ / 8; ++cc)
-            *reinterpret_cast<uint4*>(buf + oQ + sw128_off(kk, hf * (kHQ / 8) + cc)) =
-                make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.gs_ready);
-          // KL terms summed over the 128 keys: lanes by a butterfly, the four
-          // key quarters by shared atomics into the tile's cleared sums
-          if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
-          lanes_sum_add<kHQ>(term, lane, sh.kl_acc + hf * kHQ);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.kl_ready);
-        }
-        // ---- stage D: read out dQ^T (lane = d) and dq_idx^T (lane = e < 64) as bf16 slot partials
+        // ---- stage D: read out dQ^T (lane = d) and dq_idx^T (lane = e < 64) as bf16 slot partials,
+        // staged where dS^T and Q were (dQ^T and the index MMAs are the last readers)
         {
           const int pos0 = item.w + j * npos;  // padded entry of the tile's first query
           if (!mbar_wait(&sh.dq_full, par, a.err, 629)) { ok = false; break; }
@@ -584,41 +629,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) stg[(32 * h2 + i) * 32 + lane] = __float2bfloat16_rn(dq[i]);
           }
-          if (!mbar_wait(&sh.ph2_full, par, a.err, 630)) { ok = false; break; }
-          tc_fence_after();
-          __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(buf + oQ + 16384 + (hf * 2 + (quarter & 1)) * (kHQ * 64));
-          if (quarter < 2) {
+          __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(buf + oQ + (hf * 2 + (quarter & 1)) * (kHQ * 64));
+          if (quarter < 2) {  // dq_idx^T lives on TMEM lanes 0..63
+            if (!mbar_wait(&sh.ph2_full, par, a.err, 630)) { ok = false; break; }
+            tc_fence_after();
             float dqi[kHQ];
             tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, dqi);
             tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.x_free);  // P may take the next tile's X^T
 #pragma unroll
             for (int i = 0; i < kHQ; ++i) stq[i * 32 + lane] = __float2bfloat16_rn(dqi[i]);
           }
-          tc_fence_before();
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            mbar_arrive(&sh.x_free);  // P may take the next tile's X^T
             tma_store_2d(&map_dq, stg, quarter * 32, pos0 * hg + col0);
             if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kHQ);
             bulk_commit();
           }
-          if (kl_writer) {  // every epilogue warp has added its KL terms: write the per-query sums
+          rel_gb = gb;
+          if (kl_writer) {  // every epilogue warp has added its KL terms (in stage A): write the per-query sums
             if (!mbar_wait(&sh.kl_ready, par, a.err, 631)) { ok = false; break; }
             for (int q = lane; q < npos; q += 32) {
-              const int e = m.ent[q * hg];
+              const int e = m.ent[q];
               if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
               sh.kl_acc[q] = 0.f;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.kl_free);
           }
-          // the buffer goes back to the producers once this warp's partial stores have read it
-          if (lane == 0) {
-            bulk_wait_read_all();
-            mbar_arrive(&sh.g_empty[gb]);
-          }
-          __syncwarp();
         }
       }
       if (!ok) break;
@@ -672,7 +713,7 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUten
   if (!attr[dslot]) {
     for (auto f : {bwd_wide_kernel<4>, bwd_wide_kernel<8>}) {
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess) return e;
-      // the 72 / 184 register split redistributes exactly the 128 x 512 registers the block is launched
+      // the 64 / 192 register split redistributes exactly the 128 x 512 registers the block is launched
       // with; any other launch count would leave the epilogue's increase waiting for registers
       cudaFuncAttributes fa;
       if ((e = cudaFuncGetAttributes(&fa, f)) != cudaSuccess) return e;
