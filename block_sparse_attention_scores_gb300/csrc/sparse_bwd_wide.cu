@@ -102,6 +102,12 @@ constexpr int kSmem = oSh + (int)sizeof(Shared);
 static_assert(kGather % 1024 == 0, "gather buffers keep the 1024-byte swizzle alignment");
 static_assert(kSmem <= 232448, "backward kernel exceeds 227 KB of shared memory");
 
+__device__ __forceinline__ float fast_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // The value unchanged, through an instruction the compiler cannot see through.
 __device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
   asm volatile("mov.b32 %0, %0;" : "+r"(x));
@@ -351,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (item.x < 0) break;
         const int ntiles = (item.z + npos - 1) / npos;
         if (!mbar_wait(&sh.kv_full, it & 1, a.err, 612)) { ok = false; break; }
+        bool s_issued = false;  // this tile's S^T went out during the previous tile
         for (int j = 0; j < ntiles; ++j, ++tj) {
           const uint32_t par = tj & 1;
           const uint32_t gA = gA0 + ((tj & 1) * kGather >> 4), gT = gT0 + ((tj & 1) * kGather >> 4);
@@ -360,14 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t iA = opaque_u32(iA0), iT = opaque_u32(iT0);
           // a K-major k-step inside a tile of two 64-column chunks, in descriptor units
 #define KSTEP(ks) ((uint32_t)((((ks) >> 2) * kChunk + ((ks) & 3) * 32) >> 4))
-          // S^T = K Q^T into R, once the tile is gathered and the last dQ^T has been read out
-          if (!mbar_wait(&sh.g_full[tj & 1], (tj >> 1) & 1, a.err, 613)) { ok = false; break; }
-          if (!mbar_wait(&sh.r_free, par ^ 1, a.err, 614)) { ok = false; break; }
-          tc_fence_after();
+          // S^T = K Q^T into R, once the tile is gathered and the last dQ^T has been read out (issued
+          // during the previous tile, right after its dQ^T, unless this is the list's first tile)
+          auto issue_s = [&](uint32_t u) -> bool {
+            if (!mbar_wait(&sh.g_full[u & 1], (u >> 1) & 1, a.err, 613)) return false;
+            if (!mbar_wait(&sh.r_free, (u & 1) ^ 1, a.err, 614)) return false;
+            tc_fence_after();
+            const uint32_t gAu = gA0 + ((u & 1) * kGather >> 4);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ss_w(tmem + cR, kA + KSTEP(ks), gA + (oQ >> 4) + KSTEP(ks), hi, id_s, ks > 0);
-          umma_commit(&sh.s_full);
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16_ss_w(tmem + cR, kA + KSTEP(ks), gAu + (oQ >> 4) + KSTEP(ks), hi, id_s, ks > 0);
+            umma_commit(&sh.s_full);
+            return true;
+          };
+          if (!s_issued && !issue_s(tj)) { ok = false; break; }
+          s_issued = false;
           // X^T = KI QI^T into P, once the last dq_idx^T has been read out
           if (!mbar_wait(&sh.x_free, par ^ 1, a.err, 615)) { ok = false; break; }
           tc_fence_after();
@@ -405,6 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ss_w(tmem + cR, kT + 128 * ks, gT + (oDO >> 4) + 128 * ks, hi, id_dq, ks > 0);
           umma_commit(&sh.dq_full);
+          if (j + 1 < ntiles) {  // the next tile's S^T, as soon as this dQ^T has left R
+            if (!issue_s(tj + 1)) { ok = false; break; }
+            s_issued = true;
+          }
           // index branch (gs^T written long before, in stage A): dk_idx += gs^T QI, dq_idx^T = KI^T gs^T
           // into P, after dV has read P^T (same issuing thread: in order)
           if (!mbar_wait(&sh.gs_ready, par, a.err, 620)) { ok = false; break; }
@@ -458,9 +476,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int4 dg0 = *reinterpret_cast<const int4*>(m.diag);
         const int4 dg1 = *reinterpret_cast<const int4*>(m.diag + 4);
         const bool masked = (dg0.x | dg0.y | dg0.z | dg0.w | dg1.x | dg1.y | dg1.z | dg1.w) != 0;
-        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; the index branch
-        // (p_main, p_px, gs, KL terms); P^T into TMEM. S^T goes back to the tensor core (for dP^T)
-        // as soon as it is in registers.
+        // ---- stage A: P = exp(s - LSE), zero on masked keys and padding rows; P^T into TMEM.
+        // S^T goes back to the tensor core (for dP^T) as soon as it is in registers.
         float pv[64];
         tmem_ld32(tmem + lane_off + cR + col0, *reinterpret_cast<float(*)[32]>(pv));
         tmem_ld32(tmem + lane_off + cR + col0 + 32, *reinterpret_cast<float(*)[32]>(pv + 32));
@@ -497,53 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the readers of the previous gs^T included)
         if (!mbar_wait(&sh.x_full, par, a.err, 633)) { ok = false; break; }
         tc_fence_after();
-        {
-          float xv[kHQ];
-          tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
-          tmem_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.x_read);  // X^T leaves the P columns once every warp has it
-          // index branch: X^T and gs^T have one column per query
-          float term[kHQ];
-          uint32_t gp[kHQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs
-#pragma unroll
-          for (int qq = 0; qq < kHQ; ++qq) {
-            const int r = qq * hg;          // the query's first head row in this half
-            const int q = col0 / hg + qq;   // the query in the tile
-            float pm = 0.f;
-#pragma unroll
-            for (int h = 0; h < hg; ++h) pm += pv[r + h];
-            pm *= 1.f / (float)hg;
-            const float lpx2 = fmaf(xv[qq], a.scale_idx_log2, -m.lpx2[q]);  // log2 p_px
-            float ppx = fast_exp2(lpx2);
-            if (masked && key > (m.ent[q] >> 8)) ppx = 0.f;
-            const float gsv = a.kl_weight * (ppx - pm) * a.scale_idx;
-            const uint32_t bits = pack_bf16(gsv, 0.f) & 0xffffu;
-            if (qq & 1) gp[qq >> 1] |= bits << 16;
-            else gp[qq >> 1] = bits;
-            term[qq] = pm > 0.f ? pm * (__log2f(pm) - lpx2) * kLn2 : 0.f;
-          }
-          // gs^T row kk: 16-byte chunks of 8 queries, swizzled like the TMA image of the same width
-          if constexpr (npos == 32) {
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
-              *reinterpret_cast<uint4*>(smem + oGS + kk * 64 + (((2 * hf + cc) ^ ((kk >> 1) & 3)) << 4)) =
-                  make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
-          } else {
-            *reinterpret_cast<uint4*>(smem + oGS + kk * 32 + ((hf ^ ((kk >> 2) & 1)) << 4)) =
-                make_uint4(gp[0], gp[1], gp[2], gp[3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.gs_ready);
-          // KL terms summed over the 128 keys: lanes by a butterfly, the four
-          // key quarters by shared atomics into the tile's cleared sums
-          if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
-          lanes_sum_add<kHQ>(term, lane, sh.kl_acc + hf * kHQ);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.kl_ready);
-        }
+        float xv[kHQ];
+        tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.x_read);  // X^T leaves the P columns once every warp has it
         if (!mbar_wait(&sh.x_read, par, a.err, 624)) { ok = false; break; }
         tc_fence_after();
         {
@@ -609,10 +585,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.ds_smem);
         }
-        // ---- stage D: read out dQ^T (lane = d) and dq_idx^T (lane = e < 64) as bf16 slot partials,
-        // staged where dS^T and Q were (dQ^T and the index MMAs are the last readers)
+        // ---- stage C1: index branch in registers (p_main, p_px, gs, KL terms), while dQ^T is computed
+        float term[kHQ];
+        uint32_t gp[kHQ / 2];  // this key's gs^T entries for the half's queries, bf16 pairs (low half = even query)
         {
-          const int pos0 = item.w + j * npos;  // padded entry of the tile's first query
+          const float ws = a.kl_weight * a.scale_idx;
+#pragma unroll
+          for (int q2 = 0; q2 < kHQ / 2; ++q2) {
+            float gsv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int qq = 2 * q2 + u;
+              const int r = qq * hg;          // the query's first head row in this half
+              const int q = col0 / hg + qq;   // the query in the tile
+              float pm = 0.f;
+#pragma unroll
+              for (int h = 0; h < hg; ++h) pm += pv[r + h];
+              pm *= 1.f / (float)hg;
+              const float lpx2 = fmaf(xv[qq], a.scale_idx_log2, -m.lpx2[q]);  // log2 p_px
+              float ppx = fast_exp2(lpx2);
+              if (masked && key > (m.ent[q] >> 8)) ppx = 0.f;
+              gsv[u] = ws * (ppx - pm);
+              // p_main ln(p_main / p_px); p_main below the smallest normal float adds nothing visible
+              term[qq] = pm >= 1.17549435e-38f ? pm * (fast_log2(pm) - lpx2) * kLn2 : 0.f;
+            }
+            gp[q2] = pack_bf16(gsv[0], gsv[1]);
+          }
+        }
+        // ---- stage D1: read out dQ^T (lane = d) as bf16 slot partials, staged where dS^T was
+        // (dQ^T is its last reader); R goes back to the tensor core for the next tile's S^T
+        const int pos0 = item.w + j * npos;  // padded entry of the tile's first query
+        {
           if (!mbar_wait(&sh.dq_full, par, a.err, 629)) { ok = false; break; }
           tc_fence_after();
           __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(buf + oDO + (hf * 4 + quarter) * 4096);
@@ -629,8 +632,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) stg[(32 * h2 + i) * 32 + lane] = __float2bfloat16_rn(dq[i]);
           }
-          __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(buf + oQ + (hf * 2 + (quarter & 1)) * (kHQ * 64));
-          if (quarter < 2) {  // dq_idx^T lives on TMEM lanes 0..63
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_dq, stg, quarter * 32, pos0 * hg + col0);
+            bulk_commit();
+          }
+        }
+        // ---- stage C2: gs^T for the index MMAs (the previous tile's were done before this tile's
+        // X^T), and the KL sums
+        {
+          // gs^T row kk: 16-byte chunks of 8 queries, swizzled like the TMA image of the same width
+          if constexpr (npos == 32) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+              *reinterpret_cast<uint4*>(smem + oGS + kk * 64 + (((2 * hf + cc) ^ ((kk >> 1) & 3)) << 4)) =
+                  make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
+          } else {
+            *reinterpret_cast<uint4*>(smem + oGS + kk * 32 + ((hf ^ ((kk >> 2) & 1)) << 4)) =
+                make_uint4(gp[0], gp[1], gp[2], gp[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.gs_ready);
+          // KL terms summed over the 128 keys: lanes by a butterfly, the four
+          // key quarters by shared atomics into the tile's cleared sums
+          if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
+          lanes_sum_add<kHQ>(term, lane, sh.kl_acc + hf * kHQ);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.kl_ready);
+        }
+        // ---- stage D2: dq_idx^T (TMEM lanes 0..63) as bf16 slot partials, staged where Q was (dK,
+        // its last reader, is done); the per-query KL sums
+        {
+          if (quarter < 2) {
             if (!mbar_wait(&sh.ph2_full, par, a.err, 630)) { ok = false; break; }
             tc_fence_after();
             float dqi[kHQ];
@@ -639,18 +674,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.x_free);  // P may take the next tile's X^T
+            __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(buf + oQ + (hf * 2 + quarter) * (kHQ * 64));
 #pragma unroll
             for (int i = 0; i < kHQ; ++i) stq[i * 32 + lane] = __float2bfloat16_rn(dqi[i]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&map_dq, stg, quarter * 32, pos0 * hg + col0);
-            if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kHQ);
-            bulk_commit();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kHQ);
+              bulk_commit();
+            }
           }
           rel_gb = gb;
-          if (kl_writer) {  // every epilogue warp has added its KL terms (in stage A): write the per-query sums
+          if (kl_writer) {  // every epilogue warp has added its KL terms: write the per-query sums
             if (!mbar_wait(&sh.kl_ready, par, a.err, 631)) { ok = false; break; }
             for (int q = lane; q < npos; q += 32) {
               const int e = m.ent[q];
@@ -663,7 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      // ---- list end: dV, dK (columns [64 hf, 64 hf + 64)) and dk_idx ([32 hf, 32 hf + 32)), lane = key
+      // ---- list end: dV, dK (columns [64 hf, 64 hf + 64)) and dk_idx ([32 hf, 32 hf + 32)), lane = key.
+      // dV and dK were final when this warp saw pv_done and dq_full of the last tile; dk_idx is final once
+      // that tile's index MMAs are (only the warps of lanes 0..63 waited for them, for dq_idx^T)
+      if (!mbar_wait(&sh.ph2_full, (tj - 1) & 1, a.err, 635)) { ok = false; break; }
+      tc_fence_after();
       {
         const size_t orow = ((size_t)b * a.T + key) * a.G + g;
         float v[32];
