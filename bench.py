@@ -135,8 +135,8 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def traffic_record(kernel_file: str):
-    """Per-launch DRAM bytes from a committed ncu summary, if it still matches the source."""
+def traffic_record(kernel_file: str, workload: str):
+    """Per-launch DRAM bytes from a committed ncu summary, if it still matches the source and the workload."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -145,7 +145,7 @@ def traffic_record(kernel_file: str):
     src = os.path.join(ROOT, "block_sparse_attention_scores_gb300", "csrc", kernel_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     r = rec.get(kernel_file)
-    if not r or r.get("source_sha") != sha:
+    if not r or r.get("source_sha") != sha or r.get("workload") != workload:
         return None
     return r
 
@@ -573,7 +573,7 @@ def run_gpu(args, w):
         kernels_line = {}
         for n in kernel_ms:
             sec = kernel_ms[n] * 1e-3
-            tr_n = traffic_record(kfile[n])
+            tr_n = traffic_record(kfile[n], w.name)
             kernels_line[kname[n]] = {
                 "ms": kernel_ms[n], "tflops": stage_flops[n] / sec / 1e12,
                 "frac_bf16_peak": stage_flops[n] / sec / 1e12 / peak,
@@ -582,7 +582,7 @@ def run_gpu(args, w):
                 "dram_gb_measured": tr_n["bytes_per_launch"] / 1e9 if tr_n else None,
                 "dram_gbs_measured": tr_n["bytes_per_launch"] / sec / 1e9 if tr_n else None,
                 "frac_hbm_measured": tr_n["bytes_per_launch"] / sec / 1e9 / hbm if tr_n else None}
-        tr = traffic_record(kfile[dom])
+        tr = traffic_record(kfile[dom], w.name)
         line = {
             "metric": METRIC, "value": aggregate_tokens_per_s(w, world, ms_step), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
