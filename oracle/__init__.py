@@ -169,15 +169,26 @@ def index_topk_fp8(s: OShape, q_idx, k_idx, rows=None, want_pool=False):
     return index_topk(s, q_deq, k_deq, rows=rows, want_pool=want_pool)
 
 
+def _selection(block_idx):
+    """block_idx as int32 and its pointer; None (a NULL pointer) selects every
+    causally visible token (full attention, as in the indexer warmup)."""
+    if block_idx is None:
+        return None, None
+    bi = np.ascontiguousarray(block_idx, dtype=np.int32)
+    return bi, bi.ctypes.data
+
+
 def sparse_fwd(s: OShape, Q, K, V, block_idx, rows=None):
-    """Steps 4-5. rows: ids (b*T + t)*Hq + h, default all. Returns (O [n,d], LSE [n])."""
+    """Steps 4-5. rows: ids (b*T + t)*Hq + h, default all. Returns (O [n,d], LSE [n]).
+
+    block_idx None: every visible token (full causal attention)."""
     lib = _load()
     (qp, kp, vp), dt, keep = _inputs(Q, K, V)
-    bi = np.ascontiguousarray(block_idx, dtype=np.int32)
+    bi, bip = _selection(block_idx)
     rp, n, rk = _rows(rows, s.B * s.T * s.Hq)
     O = np.empty((n, s.d), dtype=np.float64)
     LSE = np.empty(n, dtype=np.float64)
-    lib.oracle_sparse_fwd(ctypes.byref(s), qp, kp, vp, dt, bi.ctypes.data, rp, n, O.ctypes.data,
+    lib.oracle_sparse_fwd(ctypes.byref(s), qp, kp, vp, dt, bip, rp, n, O.ctypes.data,
                           LSE.ctypes.data)
     return O, LSE
 
@@ -189,13 +200,13 @@ def bwd_rows(s: OShape, Q, K, V, dO, q_idx, k_idx, block_idx, rows=None):
     """
     lib = _load()
     ptrs, dt, keep = _inputs(Q, K, V, dO, q_idx, k_idx)
-    bi = np.ascontiguousarray(block_idx, dtype=np.int32)
+    bi, bip = _selection(block_idx)
     rp, n, rk = _rows(rows, s.B * s.G * s.T)
     hg = s.Hq // s.G
     dQ = np.empty((n, hg, s.d), dtype=np.float64)
     dqi = np.empty((n, s.d_idx), dtype=np.float64)
     KL = np.empty(n, dtype=np.float64)
-    lib.oracle_bwd_rows(ctypes.byref(s), *ptrs, dt, bi.ctypes.data, rp, n, dQ.ctypes.data, dqi.ctypes.data,
+    lib.oracle_bwd_rows(ctypes.byref(s), *ptrs, dt, bip, rp, n, dQ.ctypes.data, dqi.ctypes.data,
                         KL.ctypes.data)
     return dQ, dqi, KL
 
@@ -207,13 +218,13 @@ def bwd_blocks(s: OShape, Q, K, V, dO, q_idx, k_idx, block_idx, blocks=None):
     """
     lib = _load()
     ptrs, dt, keep = _inputs(Q, K, V, dO, q_idx, k_idx)
-    bi = np.ascontiguousarray(block_idx, dtype=np.int32)
+    bi, bip = _selection(block_idx)
     nb = (s.T + s.Bk - 1) // s.Bk
     rp, n, rk = _rows(blocks, s.B * nb)
     dK = np.empty((n, s.G, s.Bk, s.d), dtype=np.float64)
     dV = np.empty((n, s.G, s.Bk, s.d), dtype=np.float64)
     dki = np.empty((n, s.Bk, s.d_idx), dtype=np.float64)
-    lib.oracle_bwd_blocks(ctypes.byref(s), *ptrs, dt, bi.ctypes.data, rp, n, dK.ctypes.data, dV.ctypes.data,
+    lib.oracle_bwd_blocks(ctypes.byref(s), *ptrs, dt, bip, rp, n, dK.ctypes.data, dV.ctypes.data,
                           dki.ctypes.data)
     return dK, dV, dki
 

@@ -18,7 +18,10 @@
  *      under (pool descending, block index ascending); stored ascending and
  *      padded with -1  (itinai.ru, "Two-stage process" and "How the indexer
  *      works": k blocks per query, the query's own block always included)
- *   4. selected tokens S(g,t) = { j <= t : block(j) listed in block_idx }
+ *   4. selected tokens S(g,t) = { j <= t : block(j) listed in block_idx };
+ *      without a block_idx (NULL), every visible token j <= t: the full
+ *      causal attention of the indexer warmup (itinai.ru, "Training sparse
+ *      attention": the first iterations attend to everything)
  *   5. main branch: exact softmax attention over S, two-pass, with the LSE
  *      (itinai.ru "Two-stage process"; dothoosh.com "how FlashAttention cuts
  *      GPU memory traffic", "Exactness vs approximation")
@@ -237,9 +240,14 @@ int oracle_quantize_fp8(const oshape *s, const void *q_idx, const void *k_idx, d
 
 /* ---------------------------------------------------------------- step 4 */
 /* Selected, causally visible tokens of (b,g,t), ascending; duplicates in the
- * block list count once. Returns |S|. tok must hold k*Bk entries. */
+ * block list count once. block_idx NULL selects every visible token. Returns
+ * |S|. tok must hold k*Bk entries (T without a block_idx). */
 static int selected_tokens(const oshape *s, const int32_t *block_idx, int b, int g, int t,
                            int32_t *tok) {
+    if (!block_idx) {
+        for (int j = 0; j <= t; j++) tok[j] = j;
+        return t + 1;
+    }
     const int32_t *bl = block_idx + (((size_t)b * s->G + g) * s->T + t) * s->k;
     int cs[256];
     int m = 0;
@@ -262,6 +270,7 @@ static int selected_tokens(const oshape *s, const int32_t *block_idx, int b, int
 
 /* ---------------------------------------------------------------- steps 5-7 */
 typedef struct {
+    size_t cap;    /* capacity: largest |S|       */
     int n;         /* |S|                         */
     int32_t *tok;  /* [k*Bk]                      */
     double *P;     /* [hg][k*Bk] main softmax     */
@@ -275,8 +284,14 @@ typedef struct {
     double KL;
 } rowst;
 
-static void rowst_alloc(const oshape *s, rowst *r) {
-    const size_t L = (size_t)s->k * s->Bk, hg = (size_t)(s->Hq / s->G);
+/* Largest |S| of a row: k blocks, or every token without a block_idx. */
+static size_t row_capacity(const oshape *s, const int32_t *block_idx) {
+    return block_idx ? (size_t)s->k * s->Bk : (size_t)s->T;
+}
+
+static void rowst_alloc(const oshape *s, rowst *r, size_t L) {
+    const size_t hg = (size_t)(s->Hq / s->G);
+    r->cap = L;
     r->tok = (int32_t *)malloc(sizeof(int32_t) * L);
     r->P = (double *)malloc(sizeof(double) * hg * L);
     r->dS = (double *)malloc(sizeof(double) * hg * L);
@@ -324,7 +339,7 @@ static void row_state(const oshape *s, const oinputs *in, int b, int g, int t, i
                       rowst *r) {
     const int T = s->T, Hq = s->Hq, G = s->G, d = s->d, E = s->d_idx;
     const int hg = Hq / G;
-    const size_t L = (size_t)s->k * s->Bk;
+    const size_t L = r->cap;
     const int n = selected_tokens(s, in->block_idx, b, g, t, r->tok);
     r->n = n;
     for (int h = 0; h < hg; h++) {
@@ -384,7 +399,7 @@ static void row_state(const oshape *s, const oinputs *in, int b, int g, int t, i
 
 /*
  * Forward for rows id = (b*T + t)*Hq + h (NULL: all B*T*Hq rows).
- * O: [nrows, d], LSE: [nrows].
+ * O: [nrows, d], LSE: [nrows]. block_idx NULL: every visible token (step 4).
  */
 int oracle_sparse_fwd(const oshape *s, const void *Q, const void *K, const void *V, int dt,
                       const int32_t *block_idx, const int64_t *rows, int64_t nrows, double *O,
@@ -394,7 +409,7 @@ int oracle_sparse_fwd(const oshape *s, const void *Q, const void *K, const void 
 #pragma omp parallel
     {
         rowst r;
-        rowst_alloc(s, &r);
+        rowst_alloc(s, &r, row_capacity(s, block_idx));
 #pragma omp for schedule(dynamic, 8)
         for (int64_t q = 0; q < nrows; q++) {
             const int64_t id = rows ? rows[q] : q;
@@ -414,17 +429,18 @@ int oracle_sparse_fwd(const oshape *s, const void *Q, const void *K, const void 
 /*
  * Per-query backward outputs for rows id = (b*G + g)*T + t (NULL: all).
  * dQ: [nrows, hg, d]; dq_idx: [nrows, d_idx]; KL: [nrows]. Any may be NULL.
+ * block_idx NULL: every visible token (step 4).
  */
 int oracle_bwd_rows(const oshape *s, const void *Q, const void *K, const void *V, const void *dO,
                     const void *q_idx, const void *k_idx, int dt, const int32_t *block_idx,
                     const int64_t *rows, int64_t nrows, double *dQ, double *dq_idx, double *KL) {
     const int T = s->T, G = s->G, d = s->d, E = s->d_idx, hg = s->Hq / s->G;
-    const size_t L = (size_t)s->k * s->Bk;
+    const size_t L = row_capacity(s, block_idx);
     oinputs in = {Q, K, V, dO, q_idx, k_idx, dt, block_idx};
 #pragma omp parallel
     {
         rowst r;
-        rowst_alloc(s, &r);
+        rowst_alloc(s, &r, row_capacity(s, block_idx));
 #pragma omp for schedule(dynamic, 4)
         for (int64_t q = 0; q < nrows; q++) {
             const int64_t id = rows ? rows[q] : q;
@@ -461,7 +477,8 @@ int oracle_bwd_rows(const oshape *s, const void *Q, const void *K, const void *V
 
 /*
  * Per-key-block backward outputs for blocks id = b*n_blocks + c (NULL: all).
- * Gathers every query of every group that selected block c.
+ * Gathers every query of every group that selected block c (block_idx NULL:
+ * every query t >= c*Bk, step 4).
  * dK, dV: [nblocks, G, Bk, d]; dk_idx: [nblocks, Bk, d_idx]. Any may be NULL.
  */
 int oracle_bwd_blocks(const oshape *s, const void *Q, const void *K, const void *V, const void *dO,
@@ -470,12 +487,12 @@ int oracle_bwd_blocks(const oshape *s, const void *Q, const void *K, const void 
                       double *dk_idx) {
     const int T = s->T, Hq = s->Hq, G = s->G, d = s->d, E = s->d_idx, Bk = s->Bk, k = s->k;
     const int hg = Hq / G, nb = (T + Bk - 1) / Bk;
-    const size_t L = (size_t)k * Bk;
+    const size_t L = row_capacity(s, block_idx);
     oinputs in = {Q, K, V, dO, q_idx, k_idx, dt, block_idx};
 #pragma omp parallel
     {
         rowst r;
-        rowst_alloc(s, &r);
+        rowst_alloc(s, &r, row_capacity(s, block_idx));
 #pragma omp for schedule(dynamic, 1)
         for (int64_t q = 0; q < nblocks; q++) {
             const int64_t id = blocks ? blocks[q] : q;
@@ -487,9 +504,12 @@ int oracle_bwd_blocks(const oshape *s, const void *Q, const void *K, const void 
             if (dk_idx) memset(dk_idx + q * (size_t)Bk * E, 0, sizeof(double) * (size_t)Bk * E);
             for (int g = 0; g < G; g++) {
                 for (int t = j0; t < T; t++) {
-                    const int32_t *bl = block_idx + (((size_t)b * G + g) * T + t) * k;
-                    int hit = 0;
-                    for (int i = 0; i < k; i++) hit |= (bl[i] == c);
+                    /* without a block_idx every query t >= j0 sees block c */
+                    int hit = !block_idx;
+                    if (block_idx) {
+                        const int32_t *bl = block_idx + (((size_t)b * G + g) * T + t) * k;
+                        for (int i = 0; i < k; i++) hit |= (bl[i] == c);
+                    }
                     if (!hit) continue;
                     row_state(s, &in, b, g, t, 1, &r);
                     const size_t qio = (((size_t)b * T + t) * G + g) * E;

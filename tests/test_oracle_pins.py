@@ -151,20 +151,25 @@ def test_topk_exact_tie_levels_match_tie_rule(k):
     assert (gap[..., 3 * w.Bk:] == 0).mean() > 0.1  # many rows have a tie at the k-boundary
 
 
-def test_warmup_selection_is_dense_causal_attention_with_dense_teacher_kl():
+@pytest.mark.parametrize("selection", ["all_blocks", "none"])
+def test_warmup_selection_is_dense_causal_attention_with_dense_teacher_kl(selection):
     """Indexer warmup (full attention while the indexer learns): with every
-    visible block selected, the oracle's forward, backward and KL equal torch
-    autograd (fp64) of the dense formulation -- causal softmax attention, and
-    the KL of the index softmax against the detached head mean of the attention
-    weights, both over all visible tokens."""
+    visible block selected -- listed in block_idx, or with no block_idx at all
+    (the oracle's full-attention form) -- the oracle's forward, backward and KL
+    equal torch autograd (fp64) of the dense formulation: causal softmax
+    attention, and the KL of the index softmax against the detached head mean
+    of the attention weights, both over all visible tokens. T = 60 leaves the
+    last block partial."""
     torch = pytest.importorskip("torch")
-    w = _small(T=64, Bk=8, Hq=4, G=2, d=8, d_idx=4, k=8, B=2)  # k = T / Bk
+    w = _small(T=60, Bk=8, Hq=4, G=2, d=8, d_idx=4, k=8, B=2)  # k = ceil(T / Bk)
     inp = synth.make_inputs(w)
     s = oracle.shape_of(w, kl_weight=0.7)
     bi, _, _ = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])
     t = np.arange(w.T)
     want_sel = np.where(np.arange(w.k)[None, :] <= (t // w.Bk)[:, None], np.arange(w.k)[None, :], -1)
     assert np.array_equal(bi.reshape(w.B, w.G, w.T, w.k), np.broadcast_to(want_sel, (w.B, w.G, w.T, w.k)))
+    if selection == "none":
+        bi = None
     names = ("Q", "K", "V", "dO", "q_idx", "k_idx")
     O_ref, LSE_ref = oracle.sparse_fwd(s, inp["Q"], inp["K"], inp["V"], bi)
     ref = oracle.full_bwd(s, *[inp[n] for n in names], bi)
