@@ -62,7 +62,7 @@ def _load():
         lib.oracle_bwd_rows.argtypes = [ctypes.POINTER(OShape), P, P, P, P, P, P, ctypes.c_int, P, P, I64,
                                         P, P, P]
         lib.oracle_bwd_blocks.argtypes = [ctypes.POINTER(OShape), P, P, P, P, P, P, ctypes.c_int, P, P, I64,
-                                          P, P, P]
+                                          ctypes.c_int, P, P, P]
         for f in (lib.oracle_index_topk, lib.oracle_sparse_fwd, lib.oracle_bwd_rows, lib.oracle_bwd_blocks):
             f.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
@@ -211,8 +211,10 @@ def bwd_rows(s: OShape, Q, K, V, dO, q_idx, k_idx, block_idx, rows=None):
     return dQ, dqi, KL
 
 
-def bwd_blocks(s: OShape, Q, K, V, dO, q_idx, k_idx, block_idx, blocks=None):
+def bwd_blocks(s: OShape, Q, K, V, dO, q_idx, k_idx, block_idx, blocks=None, group=None):
     """Steps 6-7, per key block. blocks: ids b*n_blocks + c, default all.
+    group: only that group's queries (dK, dV of the other groups zero, dk_idx
+    that group's share); default every group.
 
     Returns (dK [n, G, Bk, d], dV [n, G, Bk, d], dk_idx [n, Bk, d_idx]).
     """
@@ -224,8 +226,8 @@ def bwd_blocks(s: OShape, Q, K, V, dO, q_idx, k_idx, block_idx, blocks=None):
     dK = np.empty((n, s.G, s.Bk, s.d), dtype=np.float64)
     dV = np.empty((n, s.G, s.Bk, s.d), dtype=np.float64)
     dki = np.empty((n, s.Bk, s.d_idx), dtype=np.float64)
-    lib.oracle_bwd_blocks(ctypes.byref(s), *ptrs, dt, bip, rp, n, dK.ctypes.data, dV.ctypes.data,
-                          dki.ctypes.data)
+    lib.oracle_bwd_blocks(ctypes.byref(s), *ptrs, dt, bip, rp, n, -1 if group is None else int(group),
+                          dK.ctypes.data, dV.ctypes.data, dki.ctypes.data)
     return dK, dV, dki
 
 

@@ -478,12 +478,14 @@ int oracle_bwd_rows(const oshape *s, const void *Q, const void *K, const void *V
 /*
  * Per-key-block backward outputs for blocks id = b*n_blocks + c (NULL: all).
  * Gathers every query of every group that selected block c (block_idx NULL:
- * every query t >= c*Bk, step 4).
+ * every query t >= c*Bk, step 4). group >= 0 restricts the sums to that
+ * group's queries (the other groups' dK, dV rows stay zero and dk_idx holds
+ * only that group's share); group < 0 takes every group.
  * dK, dV: [nblocks, G, Bk, d]; dk_idx: [nblocks, Bk, d_idx]. Any may be NULL.
  */
 int oracle_bwd_blocks(const oshape *s, const void *Q, const void *K, const void *V, const void *dO,
                       const void *q_idx, const void *k_idx, int dt, const int32_t *block_idx,
-                      const int64_t *blocks, int64_t nblocks, double *dK, double *dV,
+                      const int64_t *blocks, int64_t nblocks, int group, double *dK, double *dV,
                       double *dk_idx) {
     const int T = s->T, Hq = s->Hq, G = s->G, d = s->d, E = s->d_idx, Bk = s->Bk, k = s->k;
     const int hg = Hq / G, nb = (T + Bk - 1) / Bk;
@@ -503,6 +505,7 @@ int oracle_bwd_blocks(const oshape *s, const void *Q, const void *K, const void 
             if (dV) memset(dV + q * (size_t)G * Bk * d, 0, sizeof(double) * (size_t)G * Bk * d);
             if (dk_idx) memset(dk_idx + q * (size_t)Bk * E, 0, sizeof(double) * (size_t)Bk * E);
             for (int g = 0; g < G; g++) {
+                if (group >= 0 && g != group) continue;
                 for (int t = j0; t < T; t++) {
                     /* without a block_idx every query t >= j0 sees block c */
                     int hit = !block_idx;

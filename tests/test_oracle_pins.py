@@ -420,6 +420,29 @@ def test_row_and_block_views_agree_with_partial_last_block():
     assert np.all(dK[0, :, 4:] == 0)
 
 
+def test_block_view_group_filter_splits_the_sums():
+    """Restricting the per-block backward to one group keeps that group's dK, dV
+    rows, zeroes the others, and splits dk_idx into shares summing to the whole
+    (with a block list and in the full-attention form)."""
+    w = _small(T=64, Bk=8, Hq=6, G=3, k=3)
+    inp = synth.make_inputs(w)
+    s = oracle.shape_of(w)
+    names = ("Q", "K", "V", "dO", "q_idx", "k_idx")
+    bi, _, _ = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])
+    blocks = np.array([0 * w.n_blocks + 1, 1 * w.n_blocks + 5])
+    for sel in (bi, None):
+        dK, dV, dki = oracle.bwd_blocks(s, *[inp[n] for n in names], sel, blocks=blocks)
+        share = np.zeros_like(dki)
+        for g in range(w.G):
+            gK, gV, gki = oracle.bwd_blocks(s, *[inp[n] for n in names], sel, blocks=blocks, group=g)
+            np.testing.assert_array_equal(gK[:, g], dK[:, g])
+            np.testing.assert_array_equal(gV[:, g], dV[:, g])
+            assert not np.any(np.delete(gK, g, axis=1)) and not np.any(np.delete(gV, g, axis=1))
+            share += gki
+        np.testing.assert_allclose(share, dki, rtol=1e-12, atol=1e-15)
+        assert np.abs(dki).max() > 1e-6
+
+
 def test_oracle_is_independent_of_cuda_path():
     here = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     for fn in os.listdir(os.path.join(here, "oracle")):
