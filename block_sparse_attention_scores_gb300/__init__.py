@@ -28,13 +28,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmsa_gb300.so")
 
 MSA_OK, MSA_ERR_INVALID_ARG, MSA_ERR_UNSUPPORTED, MSA_ERR_WORKSPACE, MSA_ERR_CUDA, MSA_ERR_DEVICE = range(6)
-MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD, MSA_WS_TOPK_FP8 = 0, 1, 2, 3
-MSA_TIME_INDEX_TOPK, MSA_TIME_SPARSE_FWD, MSA_TIME_BWD = 0, 1, 2
+MSA_WS_TOPK, MSA_WS_FWD, MSA_WS_BWD, MSA_WS_TOPK_FP8, MSA_WS_DENSE = 0, 1, 2, 3, 4
+MSA_TIME_INDEX_TOPK, MSA_TIME_SPARSE_FWD, MSA_TIME_BWD, MSA_TIME_DENSE_FWD, MSA_TIME_DENSE_BWD = 0, 1, 2, 3, 4
 
 EXPORTED = ("msa_workspace_size", "msa_index_topk", "msa_sparse_fwd", "msa_bwd", "msa_last_error",
             "msa_check_device_status", "msa_selftest_wait_timeout", "msa_kernel_launches", "msa_version",
             "msa_index_topk_noalloc", "msa_index_topk_fp8", "msa_block_map", "msa_sparse_fwd_mapped", "msa_bwd_mapped",
-            "msa_warmup_block_idx", "msa_set_timing_events")
+            "msa_warmup_block_idx", "msa_set_timing_events", "msa_dense_fwd", "msa_dense_bwd")
 
 
 class MsaError(RuntimeError):
@@ -102,6 +102,10 @@ def load_library():
     lib.msa_kernel_launches.restype = ctypes.c_int64
     lib.msa_index_topk_noalloc.argtypes = [S, P, P, P, ctypes.c_int32, P]
     lib.msa_index_topk_noalloc.restype = ctypes.c_int
+    lib.msa_dense_fwd.argtypes = [S, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.msa_dense_fwd.restype = ctypes.c_int
+    lib.msa_dense_bwd.argtypes = [S, P, P, P, P, P, P, P, P, ctypes.c_float, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.msa_dense_bwd.restype = ctypes.c_int
     lib.msa_selftest_wait_timeout.argtypes = [P, ctypes.c_int32, P]
     lib.msa_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
@@ -229,6 +233,21 @@ def msa_bwd_mapped(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weigh
                                          _ptr(workspace), wb, _stream(stream)))
 
 
+def msa_dense_fwd(shape, Q, K, V, O, LSE, workspace, stream=None, workspace_bytes=None) -> None:
+    wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
+    _check(load_library().msa_dense_fwd(ctypes.byref(_shape(shape)), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE),
+                                        _ptr(workspace), wb, _stream(stream)))
+
+
+def msa_dense_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, kl_weight, dQ, dK, dV, dq_idx, dk_idx, KL, workspace,
+                  stream=None, workspace_bytes=None) -> None:
+    wb = workspace_bytes if workspace_bytes is not None else _nbytes(workspace)
+    _check(load_library().msa_dense_bwd(ctypes.byref(_shape(shape)), _ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO),
+                                        _ptr(LSE), _ptr(q_idx), _ptr(k_idx), float(kl_weight), _ptr(dQ), _ptr(dK),
+                                        _ptr(dV), _ptr(dq_idx), _ptr(dk_idx), _ptr(KL), _ptr(workspace), wb,
+                                        _stream(stream)))
+
+
 def msa_selftest_wait_timeout(workspace, limit_us: int, stream=None) -> None:
     _check(load_library().msa_selftest_wait_timeout(_ptr(workspace), int(limit_us), _stream(stream)))
 
@@ -288,4 +307,29 @@ def bwd(shape: Shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight=1.
                KL=torch.empty((shape.B, shape.G, shape.T), **f32))
     msa_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, block_idx, kl_weight, out["dQ"], out["dK"], out["dV"],
             out["dq_idx"], out["dk_idx"], out["KL"], ws, stream)
+    return out
+
+
+def dense_fwd(shape: Shape, Q, K, V, workspace=None, stream=None):
+    """Allocate O and LSE and run msa_dense_fwd (full causal attention)."""
+    import torch
+
+    ws = workspace if workspace is not None else alloc_workspace(shape, MSA_WS_DENSE, Q.device)
+    O = torch.empty_like(Q)
+    LSE = torch.empty((shape.B, shape.T, shape.Hq), dtype=torch.float32, device=Q.device)
+    msa_dense_fwd(shape, Q, K, V, O, LSE, ws, stream)
+    return O, LSE
+
+
+def dense_bwd(shape: Shape, Q, K, V, O, dO, LSE, q_idx, k_idx, kl_weight=1.0, workspace=None, stream=None):
+    """Allocate the fp32 gradients and KL and run msa_dense_bwd. Returns a dict."""
+    import torch
+
+    ws = workspace if workspace is not None else alloc_workspace(shape, MSA_WS_DENSE, Q.device)
+    f32 = dict(dtype=torch.float32, device=Q.device)
+    out = dict(dQ=torch.empty(Q.shape, **f32), dK=torch.empty(K.shape, **f32), dV=torch.empty(V.shape, **f32),
+               dq_idx=torch.empty(q_idx.shape, **f32), dk_idx=torch.empty(k_idx.shape, **f32),
+               KL=torch.empty((shape.B, shape.G, shape.T), **f32))
+    msa_dense_bwd(shape, Q, K, V, O, dO, LSE, q_idx, k_idx, kl_weight, out["dQ"], out["dK"], out["dV"],
+                  out["dq_idx"], out["dk_idx"], out["KL"], ws, stream)
     return out

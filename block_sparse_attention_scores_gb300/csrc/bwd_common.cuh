@@ -29,6 +29,15 @@ struct BwdArgs {
   __nv_bfloat16* dqi_part; // [padded entries, E], tile order
   float* kl_part;          // [B,T,G,k]
   float* dki_part;         // [B,G,T,E]
+  // Full attention (every query t >= 128 c sees block c): the lists are not
+  // stored but cut into segments of dense_seg queries; the outputs are the
+  // caller's, zeroed, and receive fp32 sums (dQ through the dq tensor map).
+  float* dq_idx;           // [B,T,G,E]
+  float* dk_idx;           // [B,T,E]
+  float* KL;               // [B,G,T]
+  int dense_seg;           // queries per segment, a multiple of 128
+  int dense_per_b;         // work items per batch entry
+  int dense_items;         // all work items
   int B, T, Hq, G, hg, n, k;
   float scale_log2, scale, scale_idx_log2, scale_idx, kl_weight;
 };
@@ -39,6 +48,12 @@ struct BwdArgs {
 cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mki,
                             const CUtensorMap& mdq, const CUtensorMap& mdqi, const CUtensorMap& mq,
                             const CUtensorMap& mdo, const CUtensorMap& mqi, cudaStream_t st);
+
+// The same kernel under full attention: mdq is an fp32 map of the caller's dQ
+// ([B*T, Hq, d], box 32 x hg x queries per half tile) that the kernel adds into.
+cudaError_t launch_bwd_wide_dense(const BwdArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                                  const CUtensorMap& mki, const CUtensorMap& mdq, const CUtensorMap& mq,
+                                  const CUtensorMap& mdo, const CUtensorMap& mqi, cudaStream_t st);
 
 namespace bwdc {
 

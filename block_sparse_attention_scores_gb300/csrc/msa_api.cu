@@ -82,6 +82,21 @@ int max_work_items(const Prob& p, int tiles_per_item, int rows_per_tile) {
   return (int)(tiles / tiles_per_item + lists + 1);
 }
 
+bool dense_schedule(const Prob& p, DenseSchedule* ds) {
+  // segments of 4096 queries: the dQ rows the CTAs add into at the same time (a segment of every group:
+  // 4096 x Hq x d fp32, 64 MB at Hq = 32) stay in L2
+  const long long seg = std::min<long long>(4096, p.T);
+  const long long nseg = (p.T + seg - 1) / seg;
+  long long per_b = 0;
+  for (long long s = 0; s < nseg; ++s) per_b += (long long)p.G * std::min<long long>((s + 1) * seg / 128, p.n);
+  const long long items = per_b * p.B;
+  if (items > 0x7fffffffLL) return false;
+  ds->seg = (int)seg;
+  ds->per_b = (int)per_b;
+  ds->items = (int)items;
+  return true;
+}
+
 WsLayout ws_layout(const Prob& p, int which) {
   WsLayout L;
   size_t off = 256;  // header: error word + counters
@@ -92,6 +107,12 @@ WsLayout ws_layout(const Prob& p, int which) {
   };
   const size_t lists = (size_t)p.B * p.G * p.n;
   const size_t rows = (size_t)p.B * p.T;
+  if (which == MSA_WS_DENSE) {
+    L.drow = take(rows * p.Hq * 4);
+    L.lse_px = take(rows * p.G * 4);
+    L.total = off;
+    return L;
+  }
   if (which == MSA_WS_TOPK_FP8) {
     L.q8 = take(rows * p.G * p.E);
     L.k8 = take(rows * p.E);
@@ -168,6 +189,22 @@ static msa_status validate(const msa_shape* s, Prob* p) {
   return MSA_OK;
 }
 
+// The full-attention calls take no block list (shape->k is not used) and run
+// the 128-row-tile kernels: 4 or 8 heads per group.
+static msa_status validate_dense(const msa_shape* s, Prob* p) {
+  if (!s) return fail(MSA_ERR_INVALID_ARG, "shape is NULL");
+  msa_shape c = *s;
+  c.k = 1;
+  msa_status st;
+  if ((st = validate(&c, p)) != MSA_OK) return st;
+  if (p->hg != 4 && p->hg != 8)
+    return fail(MSA_ERR_UNSUPPORTED,
+                "Hq/G=%d: full attention needs 4 or 8 heads per group (with 1 or 2, use msa_warmup_block_idx "
+                "with the sparse calls up to T = 128 * Bk)",
+                p->hg);
+  return MSA_OK;
+}
+
 // The index top-k keeps its list in registers: at most 64 blocks per row.
 static msa_status check_topk_k(const Prob& p) {
   if (p.k > 64) return fail(MSA_ERR_UNSUPPORTED, "index top-k keeps at most 64 blocks (k=%d)", p.k);
@@ -205,7 +242,7 @@ static msa_status cuda_status(cudaError_t e, const char* what) {
   return fail(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-cudaEvent_t g_timing[3][2] = {};  // caller's events per timed kernel (msa_set_timing_events)
+cudaEvent_t g_timing[5][2] = {};  // caller's events per timed kernel (msa_set_timing_events)
 
 void timing_begin(int which, cudaStream_t st) {
   if (g_timing[which][0]) cudaEventRecord(g_timing[which][0], st);
@@ -220,7 +257,7 @@ using namespace msa;
 
 extern "C" {
 
-int32_t msa_version(void) { return (1 << 16) | 3; }
+int32_t msa_version(void) { return (1 << 16) | 4; }
 
 int64_t msa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
@@ -228,7 +265,11 @@ const char* msa_last_error(void) { return g_err; }
 
 size_t msa_workspace_size(const msa_shape* shape, int which) {
   Prob p{};
-  if (which < MSA_WS_TOPK || which > MSA_WS_TOPK_FP8) return 0;
+  if (which < MSA_WS_TOPK || which > MSA_WS_DENSE) return 0;
+  if (which == MSA_WS_DENSE) {
+    if (validate_dense(shape, &p) != MSA_OK) return 0;
+    return ws_layout(p, which).total;
+  }
   if (validate(shape, &p) != MSA_OK) return 0;
   if ((which == MSA_WS_TOPK || which == MSA_WS_TOPK_FP8) && p.k > 64) return 0;
   return ws_layout(p, which).total;
@@ -377,8 +418,54 @@ msa_status msa_warmup_block_idx(const msa_shape* shape, int32_t* block_idx, msa_
                      "warmup block_idx launch");
 }
 
+msa_status msa_dense_fwd(const msa_shape* shape, const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         void* workspace, size_t workspace_bytes, msa_stream_t stream) {
+  Prob p{};
+  WsLayout L;
+  msa_status s;
+  if ((s = validate_dense(shape, &p)) != MSA_OK) return s;
+  if ((s = check_ptr(Q, "Q", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(K, "K", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(V, "V", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(O, "O", 16)) != MSA_OK) return s;
+  if ((s = check_ptr(LSE, "LSE", 4)) != MSA_OK) return s;
+  if ((s = check_ws(p, MSA_WS_DENSE, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_dense_fwd(p, Q, K, V, O, LSE, w, L, st), "dense forward launch");
+}
+
+msa_status msa_dense_bwd(const msa_shape* shape, const void* Q, const void* K, const void* V, const void* O,
+                         const void* dO, const float* LSE, const void* q_idx, const void* k_idx, float kl_weight,
+                         float* dQ, float* dK, float* dV, float* dq_idx, float* dk_idx, float* KL, void* workspace,
+                         size_t workspace_bytes, msa_stream_t stream) {
+  Prob p{};
+  WsLayout L;
+  msa_status s;
+  if ((s = validate_dense(shape, &p)) != MSA_OK) return s;
+  const void* in16[] = {Q, K, V, O, dO, q_idx, k_idx, dQ, dK, dV, dq_idx, dk_idx};
+  const char* names16[] = {"Q", "K", "V", "O", "dO", "q_idx", "k_idx", "dQ", "dK", "dV", "dq_idx", "dk_idx"};
+  for (int i = 0; i < 12; ++i)
+    if ((s = check_ptr(in16[i], names16[i], 16)) != MSA_OK) return s;
+  if ((s = check_ptr(LSE, "LSE", 4)) != MSA_OK) return s;
+  if ((s = check_ptr(KL, "KL", 4)) != MSA_OK) return s;
+  if (!isfinite(kl_weight)) return fail(MSA_ERR_INVALID_ARG, "kl_weight must be finite");
+  DenseSchedule ds;
+  if (!dense_schedule(p, &ds)) return fail(MSA_ERR_UNSUPPORTED, "B*T too large for the full-attention schedule");
+  if ((s = check_ws(p, MSA_WS_DENSE, workspace, workspace_bytes, &L)) != MSA_OK) return s;
+  if ((s = check_device()) != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  if ((s = cuda_status(cudaMemsetAsync(w, 0, 256, st), "clearing workspace header")) != MSA_OK) return s;
+  return cuda_status(launch_bwd_dense(p, Q, K, V, O, dO, LSE, q_idx, k_idx, kl_weight, dQ, dK, dV, dq_idx, dk_idx,
+                                      KL, w, L, ds, st),
+                     "dense backward launch");
+}
+
 msa_status msa_set_timing_events(int32_t which, void* start_event, void* stop_event) {
-  if (which < MSA_TIME_INDEX_TOPK || which > MSA_TIME_BWD)
+  if (which < MSA_TIME_INDEX_TOPK || which > MSA_TIME_DENSE_BWD)
     return fail(MSA_ERR_INVALID_ARG, "which=%d is not a timed kernel", which);
   if ((start_event == nullptr) != (stop_event == nullptr))
     return fail(MSA_ERR_INVALID_ARG, "give both events or neither");

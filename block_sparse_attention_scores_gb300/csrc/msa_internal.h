@@ -73,7 +73,7 @@ int device_slot();
 void count_launches(int n);
 
 // Caller-owned events recorded around a main kernel (msa_set_timing_events):
-// which = MSA_TIME_INDEX_TOPK, MSA_TIME_SPARSE_FWD or MSA_TIME_BWD.
+// which = one of the MSA_TIME_* kernels.
 void timing_begin(int which, cudaStream_t st);
 void timing_end(int which, cudaStream_t st);
 
@@ -113,6 +113,24 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
                        const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
                        float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
                        uint8_t* ws, const WsLayout& L, cudaStream_t st, bool mapped = false);
+
+// Full attention (indexer warmup at any T; heads per group 4 or 8).
+// The backward's work items: every (KV block c, query t >= 128 c) pair, cut
+// into segments of `seg` queries (dense_schedule; items <= INT_MAX checked).
+struct DenseSchedule {
+  int seg;     // queries per segment (multiple of 128)
+  int per_b;   // work items per batch entry
+  int items;   // all work items
+};
+bool dense_schedule(const Prob& p, DenseSchedule* ds);
+cudaError_t launch_dense_fwd(const Prob& p, const void* Q, const void* K, const void* V, void* O, float* LSE,
+                             uint8_t* ws, const WsLayout& L, cudaStream_t st);
+cudaError_t launch_dense_px(const Prob& p, const void* q_idx, const void* k_idx, float* lse_px, uint8_t* ws,
+                            const WsLayout& L, cudaStream_t st);
+cudaError_t launch_bwd_dense(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, const void* q_idx, const void* k_idx, float kl_weight,
+                             float* dQ, float* dK, float* dV, float* dq_idx, float* dk_idx, float* KL, uint8_t* ws,
+                             const WsLayout& L, const DenseSchedule& ds, cudaStream_t st);
 
 cudaError_t launch_selftest_wait_timeout(int* err, long long limit_ns, cudaStream_t st);
 

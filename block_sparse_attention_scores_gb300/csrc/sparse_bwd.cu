@@ -1092,6 +1092,46 @@ void bwd_merge(const Prob& p, const int32_t* block_idx, const int32_t* rev, cons
 
 }  // namespace
 
+// Tensor maps of the backward's inputs: K, V (box 64 d x 1 x 128 keys), k_idx
+// (64 x 128), and the gathered rows of one query: Q, dO (64 d x hg heads x 1
+// token), q_idx (64 x 1).
+struct BwdMaps {
+  CUtensorMap mk, mv, mki, mq, mdo, mqi;
+};
+
+static bool make_bwd_maps(const Prob& p, const void* Q, const void* K, const void* V, const void* dO,
+                          const void* q_idx, const void* k_idx, BwdMaps* m) {
+  {
+    const uint64_t dims[2] = {64, (uint64_t)p.BT()};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {64, 128};
+    if (!encode_tmap(&m->mki, const_cast<void*>(k_idx), 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  }
+  {
+    const uint64_t dims[3] = {128, (uint64_t)p.G, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {256, (uint64_t)p.G * 256};
+    const uint32_t box[3] = {64, 1, 128};
+    if (!encode_tmap(&m->mk, const_cast<void*>(K), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&m->mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  }
+  {
+    const uint64_t dims[3] = {128, (uint64_t)p.Hq, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {256, (uint64_t)p.Hq * 256};
+    const uint32_t box[3] = {64, (uint32_t)p.hg, 1};
+    if (!encode_tmap(&m->mq, const_cast<void*>(Q), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&m->mdo, const_cast<void*>(dO), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+    const uint64_t dims2[2] = {64, (uint64_t)p.BT() * p.G};
+    const uint64_t strides2[1] = {128};
+    const uint32_t box2[2] = {64, 1};
+    if (!encode_tmap(&m->mqi, const_cast<void*>(q_idx), 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_128B))
+      return false;
+  }
+  return true;
+}
+
 cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* V, const void* O, const void* dO,
                        const float* LSE, const void* q_idx, const void* k_idx, const int32_t* block_idx,
                        float kl_weight, void* dQ, void* dK, void* dV, void* dq_idx, void* dk_idx, float* KL,
@@ -1111,39 +1151,8 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
       static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), drow, hrows);
   if ((e = cudaMemsetAsync(counters + 2, 0, 2 * sizeof(int), st)) != cudaSuccess) return e;
 
-  CUtensorMap mki, mk, mv;
-  {
-    const uint64_t dims[2] = {64, (uint64_t)p.BT()};
-    const uint64_t strides[1] = {128};
-    const uint32_t box[2] = {64, 128};
-    if (!encode_tmap(&mki, const_cast<void*>(k_idx), 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t dims[3] = {128, (uint64_t)p.G, (uint64_t)p.BT()};
-    const uint64_t strides[2] = {256, (uint64_t)p.G * 256};
-    const uint32_t box[3] = {64, 1, 128};
-    if (!encode_tmap(&mk, const_cast<void*>(K), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-    if (!encode_tmap(&mv, const_cast<void*>(V), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
-  CUtensorMap mq, mdo, mqi;
-  {
-    // one query's head rows of its group: box {64 d, hg heads, 1 token}
-    const uint64_t dims[3] = {128, (uint64_t)p.Hq, (uint64_t)p.BT()};
-    const uint64_t strides[2] = {256, (uint64_t)p.Hq * 256};
-    const uint32_t box[3] = {64, (uint32_t)p.hg, 1};
-    if (!encode_tmap(&mq, const_cast<void*>(Q), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-    if (!encode_tmap(&mdo, const_cast<void*>(dO), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-    const uint64_t dims2[2] = {64, (uint64_t)p.BT() * p.G};
-    const uint64_t strides2[1] = {128};
-    const uint32_t box2[2] = {64, 1};
-    if (!encode_tmap(&mqi, const_cast<void*>(q_idx), 2, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_128B))
-      return cudaErrorInvalidValue;
-  }
+  BwdMaps mp;
+  if (!make_bwd_maps(p, Q, K, V, dO, q_idx, k_idx, &mp)) return cudaErrorInvalidValue;
   // 64-row tiles (1 or 2 heads per group) store 32 rows per epilogue warp,
   // 128-row tiles (4 or 8) 64 rows
   const bool wide = p.hg >= 4;
@@ -1189,7 +1198,7 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   pa.n = p.n;
   pa.k = p.k;
   pa.scale_log2 = p.scale_idx * kLog2e;
-  px_stats_kernel<<<sms, kPxThreads, kPxSmem, st>>>(pa, mki);
+  px_stats_kernel<<<sms, kPxThreads, kPxSmem, st>>>(pa, mp.mki);
   px_merge_kernel<<<(int)std::min<long long>((grows + 255) / 256, 16LL * sms), 256, 0, st>>>(
       block_idx, px_part, lse_px, p.B, p.T, p.G, p.k);
 
@@ -1225,11 +1234,14 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
   ba.kl_weight = kl_weight;
   timing_begin(MSA_TIME_BWD, st);
   if (wide) {
-    if ((e = launch_bwd_wide(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi, st)) != cudaSuccess) return e;
+    if ((e = launch_bwd_wide(ba, mp.mk, mp.mv, mp.mki, mdq, mdqi, mp.mq, mp.mdo, mp.mqi, st)) != cudaSuccess)
+      return e;
   } else if (p.hg == 1) {
-    bwd_kernel<1><<<sms, kBwdThreads, BwdLayout<1>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+    bwd_kernel<1><<<sms, kBwdThreads, BwdLayout<1>::kSmem, st>>>(ba, mp.mk, mp.mv, mp.mki, mdq, mdqi, mp.mq, mp.mdo,
+                                                                 mp.mqi);
   } else {
-    bwd_kernel<2><<<sms, kBwdThreads, BwdLayout<2>::kSmem, st>>>(ba, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+    bwd_kernel<2><<<sms, kBwdThreads, BwdLayout<2>::kSmem, st>>>(ba, mp.mk, mp.mv, mp.mki, mdq, mdqi, mp.mq, mp.mdo,
+                                                                 mp.mqi);
   }
   timing_end(MSA_TIME_BWD, st);
   count_launches(5);
@@ -1247,6 +1259,81 @@ cudaError_t launch_bwd(const Prob& p, const void* Q, const void* K, const void* 
       default: bwd_merge<8>(p, block_idx, rev, ba, dQf, dqif, KL, dkif, L.max_padded, grid, st); break;
     }
   }
+  return cudaGetLastError();
+}
+
+// Full attention (the indexer warmup at any T): D, the index LSE over every
+// visible token, then the 128-row-tile backward over every (block, query >=
+// block) pair, adding into the zeroed outputs.
+cudaError_t launch_bwd_dense(const Prob& p, const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, const void* q_idx, const void* k_idx, float kl_weight,
+                             float* dQ, float* dK, float* dV, float* dq_idx, float* dk_idx, float* KL, uint8_t* ws,
+                             const WsLayout& L, const DenseSchedule& ds, cudaStream_t st) {
+  cudaError_t e;
+  const size_t rows = (size_t)p.BT();
+  const struct {
+    void* ptr;
+    size_t bytes;
+  } zero[] = {{dQ, rows * p.Hq * p.d * 4}, {dK, rows * p.G * p.d * 4}, {dV, rows * p.G * p.d * 4},
+              {dq_idx, rows * p.G * p.E * 4}, {dk_idx, rows * p.E * 4}, {KL, rows * p.G * 4}};
+  for (const auto& z : zero)
+    if ((e = cudaMemsetAsync(z.ptr, 0, z.bytes, st)) != cudaSuccess) return e;
+  int* err = reinterpret_cast<int*>(ws + L.err);
+  int* counters = reinterpret_cast<int*>(ws + L.counters);
+  float* drow = reinterpret_cast<float*>(ws + L.drow);
+  float* lse_px = reinterpret_cast<float*>(ws + L.lse_px);
+  const long long hrows = (long long)p.B * p.T * p.Hq;
+  const int sms = num_sms();
+  drow_kernel<<<(int)std::min<long long>((hrows * 32 + 255) / 256, 16LL * sms), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), drow, hrows);
+  count_launches(1);
+  if ((e = launch_dense_px(p, q_idx, k_idx, lse_px, ws, L, st)) != cudaSuccess) return e;
+  BwdMaps mp;
+  if (!make_bwd_maps(p, Q, K, V, dO, q_idx, k_idx, &mp)) return cudaErrorInvalidValue;
+  CUtensorMap mdq;
+  {
+    // the caller's fp32 dQ, added into per half tile: 32 d x hg heads x (64 / hg) queries
+    const uint64_t dims[3] = {128, (uint64_t)p.Hq, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {512, (uint64_t)p.Hq * 512};
+    const uint32_t box[3] = {32, (uint32_t)p.hg, (uint32_t)(64 / p.hg)};
+    if (!encode_tmap(&mdq, dQ, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+      return cudaErrorInvalidValue;
+  }
+  BwdArgs ba = {};
+  ba.Q = static_cast<const __nv_bfloat16*>(Q);
+  ba.dO = static_cast<const __nv_bfloat16*>(dO);
+  ba.q_idx = static_cast<const __nv_bfloat16*>(q_idx);
+  ba.LSE = LSE;
+  ba.drow = drow;
+  ba.lse_px = lse_px;
+  ba.counter = counters + 6;
+  ba.err = err;
+  ba.dK = dK;
+  ba.dV = dV;
+  ba.dq_idx = dq_idx;
+  ba.dk_idx = dk_idx;
+  ba.KL = KL;
+  ba.dense_seg = ds.seg;
+  ba.dense_per_b = ds.per_b;
+  ba.dense_items = ds.items;
+  ba.B = p.B;
+  ba.T = p.T;
+  ba.Hq = p.Hq;
+  ba.G = p.G;
+  ba.hg = p.hg;
+  ba.n = p.n;
+  ba.k = p.k;
+  ba.scale_log2 = p.scale * kLog2e;
+  ba.scale = p.scale;
+  ba.scale_idx_log2 = p.scale_idx * kLog2e;
+  ba.scale_idx = p.scale_idx;
+  ba.kl_weight = kl_weight;
+  if ((e = cudaMemsetAsync(ba.counter, 0, sizeof(int), st)) != cudaSuccess) return e;
+  timing_begin(MSA_TIME_DENSE_BWD, st);
+  e = launch_bwd_wide_dense(ba, mp.mk, mp.mv, mp.mki, mdq, mp.mq, mp.mdo, mp.mqi, st);
+  timing_end(MSA_TIME_DENSE_BWD, st);
+  count_launches(1);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

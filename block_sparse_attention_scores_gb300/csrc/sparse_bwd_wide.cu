@@ -117,20 +117,29 @@ __device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
 __device__ __forceinline__ void regs_dealloc64() { asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory"); }
 __device__ __forceinline__ void regs_alloc192() { asm volatile("setmaxnreg.inc.sync.aligned.u32 192;\n" ::: "memory"); }
 
-// Stores 32 fp32 values as 32 consecutive columns of the thread's TMEM lane.
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
-      " {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-      "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-      "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
+// Full attention: work item id -> {list (b, g, c), first query, number of queries, 0}. Items run over the
+// batch entries, then segments of dense_seg queries, then blocks c ascending (longest first) and groups,
+// so that the CTAs running at the same time add into the dQ rows of one segment, which stay in L2.
+__device__ __forceinline__ int4 dense_item(int id, const BwdArgs& a) {
+  const int b = id / a.dense_per_b;
+  int r = id - b * a.dense_per_b;
+  const int bps = a.dense_seg / 128;  // blocks per segment
+  const int nseg = (a.T + a.dense_seg - 1) / a.dense_seg;
+  int s = 0;
+  for (; s < nseg - 1; ++s) {
+    const int cnt = a.G * min((s + 1) * bps, a.n);
+    if (r < cnt) break;
+    r -= cnt;
+  }
+  const int c = r / a.G, g = r - c * a.G;
+  const int t0 = max(c * 128, s * a.dense_seg);
+  const int t1 = min((s + 1) * a.dense_seg, a.T);
+  return make_int4((b * a.G + g) * a.n + c, t0, t1 - t0, 0);
 }
 
-template <int HG>
+// DENSE: full attention. The lists are every query from the block on, cut into segments (dense_item);
+// dQ leaves by TMA reduce-add into the caller's fp32 dQ, dq_idx, KL, dK, dV and dk_idx by atomic adds.
+template <int HG, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_wide_kernel(BwdArgs a, const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                     const __grid_constant__ CUtensorMap map_ki, const __grid_constant__ CUtensorMap map_dq,
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
   volatile int* abort_flag = &sh.abort;
-  const int n_items = *a.n_items;
+  const int n_items = DENSE ? a.dense_items : *a.n_items;
 
   // The register split is set where it dominates each role's code, so that
   // the compiler gives the epilogue its 192 registers.
@@ -205,7 +214,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool mine = lane < nq * hg;  // lane's (query, head) row
     auto load_entry = [&](const int4& item, int j) -> int {
       const int idx = j * npos + qmine;
-      return (mine && idx < item.z) ? a.entries[item.y + idx] : -1;
+      if constexpr (DENSE) return (mine && idx < item.z) ? (item.y + idx) << 8 : -1;
+      else return (mine && idx < item.z) ? a.entries[item.y + idx] : -1;
     };
     auto load_rec = [&](int b, int g, int e) -> float4 {
       if (e < 0) return make_float4(INFINITY, 0.f, INFINITY, __int_as_float(e));
@@ -235,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
           if (!mbar_wait(&sh.it_empty[s], ph ^ 1, a.err, 601)) *abort_flag = 1;
           const int id = atomicAdd(a.counter, 1);
-          if (id < n_items && !*abort_flag) item = a.items[id];
+          if (id < n_items && !*abort_flag) {
+            if constexpr (DENSE) item = dense_item(id, a);
+            else item = a.items[id];
+          }
           sh.item[s] = item;
           mbar_arrive(&sh.it_full[s]);
         }
@@ -615,7 +628,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- stage D1: read out dQ^T (lane = d) as bf16 slot partials, staged where dS^T was
         // (dQ^T is its last reader); R goes back to the tensor core for the next tile's S^T
         const int pos0 = item.w + j * npos;  // padded entry of the tile's first query
-        {
+        const int tq0 = item.y + j * npos;   // DENSE: the tile's first query
+        if constexpr (DENSE) {
+          // dQ^T (lane = d) added into dQ: fp32 rows staged where Q and dO were (dK and dQ^T, their last
+          // readers, are done), one TMA reduce per warp (32 d x the half's 64 (query, head) rows)
+          if (!mbar_wait(&sh.dq_full, par, a.err, 629)) { ok = false; break; }
+          tc_fence_after();
+          float* stg = reinterpret_cast<float*>(buf + oQ + (hf * 4 + quarter) * 8192);
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            float dq[32];
+            tmem_ld32(tmem + lane_off + cR + col0 + 32 * h2, dq);
+            tmem_wait_ld();
+            if (h2 == 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&sh.r_free);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stg[(32 * h2 + i) * 32 + lane] = dq[i];
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_reduce_add_3d(&map_dq, stg, quarter * 32, g * hg, b * a.T + tq0 + hf * kHQ);
+            bulk_commit();
+          }
+        } else {
           if (!mbar_wait(&sh.dq_full, par, a.err, 629)) { ok = false; break; }
           tc_fence_after();
           __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(buf + oDO + (hf * 4 + quarter) * 4096);
@@ -674,6 +713,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.x_free);  // P may take the next tile's X^T
+            if constexpr (DENSE) {
+              float* dst = a.dq_idx + (((size_t)b * a.T + tq0 + hf * kHQ) * a.G + g) * 64 + kk;
+#pragma unroll
+              for (int i = 0; i < kHQ; ++i) atomicAdd(dst + (size_t)i * a.G * 64, dqi[i]);
+            } else {
             __nv_bfloat16* stq = reinterpret_cast<__nv_bfloat16*>(buf + oQ + (hf * 2 + quarter) * (kHQ * 64));
 #pragma unroll
             for (int i = 0; i < kHQ; ++i) stq[i * 32 + lane] = __float2bfloat16_rn(dqi[i]);
@@ -683,13 +727,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_store_2d(&map_dqi, stq, quarter * 32, pos0 + hf * kHQ);
               bulk_commit();
             }
+            }
           }
           rel_gb = gb;
           if (kl_writer) {  // every epilogue warp has added its KL terms: write the per-query sums
             if (!mbar_wait(&sh.kl_ready, par, a.err, 631)) { ok = false; break; }
             for (int q = lane; q < npos; q += 32) {
               const int e = m.ent[q];
-              if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
+              if constexpr (DENSE) {
+                if (e >= 0) atomicAdd(a.KL + ((size_t)b * a.G + g) * a.T + (e >> 8), sh.kl_acc[q]);
+              } else {
+                if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
+              }
               sh.kl_acc[q] = 0.f;
             }
             __syncwarp();
@@ -705,27 +754,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       {
         const size_t orow = ((size_t)b * a.T + key) * a.G + g;
+        // a dense item covers one segment of the block's queries: its sums are added
+        auto put4 = [&](float* p, const float (&v)[32]) {
+          float4* dst = reinterpret_cast<float4*>(p);
+#pragma unroll
+          for (int z = 0; z < 8; ++z) {
+            const float4 x = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+            if constexpr (DENSE) atomicAdd(dst + z, x);
+            else dst[z] = x;
+          }
+        };
         float v[32];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const int d0 = 64 * hf + 32 * q;
           tmem_ld32(tmem + lane_off + cDV + d0, v);
           tmem_wait_ld();
-          float4* dst = reinterpret_cast<float4*>(a.dV + orow * 128 + d0);
-#pragma unroll
-          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+          put4(a.dV + orow * 128 + d0, v);
           tmem_ld32(tmem + lane_off + cDK + d0, v);
           tmem_wait_ld();
-          dst = reinterpret_cast<float4*>(a.dK + orow * 128 + d0);
-#pragma unroll
-          for (int z = 0; z < 8; ++z) dst[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+          put4(a.dK + orow * 128 + d0, v);
         }
-        float* dki = a.dki_part + (((size_t)b * a.G + g) * a.T + key) * 64 + 32 * hf;
         tmem_ld32(tmem + lane_off + cKI + 32 * hf, v);
         tmem_wait_ld();
-#pragma unroll
-        for (int z = 0; z < 8; ++z)
-          reinterpret_cast<float4*>(dki)[z] = make_float4(v[4 * z], v[4 * z + 1], v[4 * z + 2], v[4 * z + 3]);
+        if constexpr (DENSE) put4(a.dk_idx + ((size_t)b * a.T + key) * 64 + 32 * hf, v);  // summed over groups too
+        else put4(a.dki_part + (((size_t)b * a.G + g) * a.T + key) * 64 + 32 * hf, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_free);
@@ -743,14 +796,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mki,
-                            const CUtensorMap& mdq, const CUtensorMap& mdqi, const CUtensorMap& mq,
-                            const CUtensorMap& mdo, const CUtensorMap& mqi, cudaStream_t st) {
+static cudaError_t set_wide_attributes() {
   static bool attr[kMaxDevices] = {};  // kernel attributes are per device context
   const int dslot = device_slot();
   cudaError_t e;
   if (!attr[dslot]) {
-    for (auto f : {bwd_wide_kernel<4>, bwd_wide_kernel<8>}) {
+    for (auto f : {bwd_wide_kernel<4, false>, bwd_wide_kernel<8, false>, bwd_wide_kernel<4, true>,
+                   bwd_wide_kernel<8, true>}) {
       if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem)) != cudaSuccess) return e;
       // the 64 / 192 register split redistributes exactly the 128 x 512 registers the block is launched
       // with; any other launch count would leave the epilogue's increase waiting for registers
@@ -760,10 +812,31 @@ cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUten
     }
     attr[dslot] = true;
   }
+  return cudaSuccess;
+}
+
+cudaError_t launch_bwd_wide(const BwdArgs& a, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mki,
+                            const CUtensorMap& mdq, const CUtensorMap& mdqi, const CUtensorMap& mq,
+                            const CUtensorMap& mdo, const CUtensorMap& mqi, cudaStream_t st) {
+  cudaError_t e;
+  if ((e = set_wide_attributes()) != cudaSuccess) return e;
   if (a.hg == 4)
-    bwd_wide_kernel<4><<<num_sms(), kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+    bwd_wide_kernel<4, false><<<num_sms(), kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
   else
-    bwd_wide_kernel<8><<<num_sms(), kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+    bwd_wide_kernel<8, false><<<num_sms(), kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdqi, mq, mdo, mqi);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_wide_dense(const BwdArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                                  const CUtensorMap& mki, const CUtensorMap& mdq, const CUtensorMap& mq,
+                                  const CUtensorMap& mdo, const CUtensorMap& mqi, cudaStream_t st) {
+  cudaError_t e;
+  if ((e = set_wide_attributes()) != cudaSuccess) return e;
+  const int grid = std::min(a.dense_items, num_sms());
+  if (a.hg == 4)
+    bwd_wide_kernel<4, true><<<grid, kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdq, mq, mdo, mqi);
+  else
+    bwd_wide_kernel<8, true><<<grid, kThreads, kSmem, st>>>(a, mk, mv, mki, mdq, mdq, mq, mdo, mqi);
   return cudaGetLastError();
 }
 

@@ -90,7 +90,7 @@ typedef struct msa_shape {
 } msa_shape;
 
 /* Which entry point a workspace is sized for. */
-enum { MSA_WS_TOPK = 0, MSA_WS_FWD = 1, MSA_WS_BWD = 2, MSA_WS_TOPK_FP8 = 3 };
+enum { MSA_WS_TOPK = 0, MSA_WS_FWD = 1, MSA_WS_BWD = 2, MSA_WS_TOPK_FP8 = 3, MSA_WS_DENSE = 4 };
 
 /* Bytes of device workspace the entry point `which` needs for `shape`
  * (0 if the shape is invalid or unsupported). A workspace sized for
@@ -257,6 +257,39 @@ MSA_API msa_status msa_bwd_mapped(const msa_shape *shape, const void *Q, const v
  * MSA_ERR_UNSUPPORTED unless k >= T / Bk (so at most T = 128 * Bk). */
 MSA_API msa_status msa_warmup_block_idx(const msa_shape *shape, int32_t *block_idx, msa_stream_t stream);
 
+/*
+ * Full attention at any T: the forward and backward that msa_sparse_fwd and
+ * msa_bwd compute for the selection msa_warmup_block_idx writes (every
+ * visible block), without a block list and without per-(query, block)
+ * scratch, so that the indexer warmup (itinai.ru "How to solve the memory
+ * problem with MiniMax Sparse Attention", "Training sparse attention": the
+ * first iterations run full attention) reaches the sequence lengths of the
+ * sparse path. For head h in group g and query t, over every j <= t:
+ *   O, LSE as msa_sparse_fwd with S(g,t) = { 0 .. t };
+ *   dQ, dK, dV, dq_idx, dk_idx, KL as msa_bwd over the same set (the KL of
+ *   the index softmax over every visible token against the head mean of the
+ *   full attention weights).
+ * Same tensors, layouts and scales as msa_sparse_fwd / msa_bwd; no block_idx.
+ * shape->k is not used (any value is accepted). Supported: Hq / G in {4, 8}
+ * (MSA_ERR_UNSUPPORTED otherwise: 1 or 2 heads per group take
+ * msa_warmup_block_idx with the sparse calls, T <= 128 * Bk), and the other
+ * limits of the common conventions. Workspace: MSA_WS_DENSE (msa_dense_fwd
+ * needs only its 256-byte header).
+ *
+ * msa_dense_fwd is query-outer (the running maximum, sum and O of each row
+ * stay on chip) and writes O and LSE once; deterministic.
+ * msa_dense_bwd overwrites its six outputs with sums accumulated by fp32
+ * atomic and TMA reduce-add operations from concurrent CTAs: the summation
+ * order, hence the last bits, varies from run to run. O and LSE must be
+ * msa_dense_fwd's outputs (or the sparse forward's under the full selection).
+ */
+MSA_API msa_status msa_dense_fwd(const msa_shape *shape, const void *Q, const void *K, const void *V, void *O,
+                                 float *LSE, void *workspace, size_t workspace_bytes, msa_stream_t stream);
+MSA_API msa_status msa_dense_bwd(const msa_shape *shape, const void *Q, const void *K, const void *V, const void *O,
+                                 const void *dO, const float *LSE, const void *q_idx, const void *k_idx,
+                                 float kl_weight, float *dQ, float *dK, float *dV, float *dq_idx, float *dk_idx,
+                                 float *KL, void *workspace, size_t workspace_bytes, msa_stream_t stream);
+
 /* Message describing the last non-OK status returned on this thread. */
 MSA_API const char *msa_last_error(void);
 
@@ -278,7 +311,9 @@ MSA_API msa_status msa_selftest_wait_timeout(void *workspace, int32_t limit_us, 
 enum {
   MSA_TIME_INDEX_TOPK = 0, /* index_topk_kernel (msa_index_topk, msa_index_topk_fp8, the no-workspace call) */
   MSA_TIME_SPARSE_FWD = 1, /* sparse_fwd_kernel (msa_sparse_fwd, msa_sparse_fwd_mapped), not the map or merge */
-  MSA_TIME_BWD = 2         /* bwd_kernel (msa_bwd, msa_bwd_mapped), not the pre-passes or merges */
+  MSA_TIME_BWD = 2,        /* bwd_kernel (msa_bwd, msa_bwd_mapped), not the pre-passes or merges */
+  MSA_TIME_DENSE_FWD = 3,  /* dense_fwd_kernel (msa_dense_fwd) */
+  MSA_TIME_DENSE_BWD = 4   /* the backward kernel of msa_dense_bwd, not D or the index LSE */
 };
 
 /* While set, every launch of kernel `which` is bracketed by

@@ -87,7 +87,7 @@ def test_warmup_selection_validates_before_device_work(lib):
 
 def test_timing_events_validate_without_device(lib):
     with pytest.raises(lib.MsaError) as e:
-        lib.msa_set_timing_events(3, None, None)
+        lib.msa_set_timing_events(5, None, None)
     assert e.value.status == lib.MSA_ERR_INVALID_ARG
     with pytest.raises(lib.MsaError) as e:
         lib.msa_set_timing_events(lib.MSA_TIME_BWD, 4096, None)
@@ -109,3 +109,31 @@ def test_selection_width_limits(lib):
     with pytest.raises(lib.MsaError) as e:
         lib.msa_index_topk_fp8(s, 4096, 4096, 4096, 4096, stream=0, workspace_bytes=1 << 30)
     assert e.value.status == lib.MSA_ERR_UNSUPPORTED
+
+
+def test_full_attention_shapes_and_validation(lib):
+    # the full-attention calls take no block list: any k, heads per group 4 or 8, T up to 2^20
+    for kw in (dict(k=1), dict(k=1024), dict(T=131072, k=16), dict(Hq=64, G=8)):
+        base = dict(B=1, T=1024, Hq=8, G=2)
+        base.update(kw)
+        s = lib.Shape(**base)
+        assert lib.msa_workspace_size(s, lib.MSA_WS_DENSE) >= 256 + s.B * s.T * (s.Hq + s.G) * 4
+    for kw in (dict(Hq=4, G=2), dict(Hq=8, G=8), dict(d=64), dict(T=1000)):
+        base = dict(B=1, T=1024, Hq=8, G=2, k=4)
+        base.update(kw)
+        assert lib.msa_workspace_size(lib.Shape(**base), lib.MSA_WS_DENSE) == 0
+    s = lib.Shape(B=1, T=1024, Hq=8, G=2, k=1024)
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_dense_fwd(s, 0, 4096, 4096, 4096, 4096, 4096, stream=0, workspace_bytes=1 << 20)
+    assert e.value.status == lib.MSA_ERR_INVALID_ARG and "Q" in str(e.value)
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_dense_fwd(lib.Shape(B=1, T=1024, Hq=4, G=2, k=1), 4096, 4096, 4096, 4096, 4096, 4096, stream=0,
+                          workspace_bytes=1 << 20)
+    assert e.value.status == lib.MSA_ERR_UNSUPPORTED and "heads per group" in str(e.value)
+    args = [4096] * 8 + [1.0] + [4096] * 6  # Q .. k_idx, kl_weight, dQ .. KL
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_dense_bwd(s, *args, 4096, stream=0, workspace_bytes=16)
+    assert e.value.status == lib.MSA_ERR_WORKSPACE
+    with pytest.raises(lib.MsaError) as e:
+        lib.msa_dense_bwd(s, *args[:8], float("nan"), *args[9:], 4096, stream=0, workspace_bytes=1 << 30)
+    assert e.value.status == lib.MSA_ERR_INVALID_ARG and "kl_weight" in str(e.value)
