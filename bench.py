@@ -512,41 +512,57 @@ def run_gpu(args, w):
     msa.msa_check_device_status(ws8, stream)
     del ws8, bi8
 
-    # ---- indexer warmup: full causal attention (every visible block selected)
-    # and the KL against the dense teacher, at B = 2, T = 8192 (all 64 blocks)
-    wu = synth.CONFIGS[1].with_(B=2, k=64, name="warmup_b2_t8192_hq32_g8_all_blocks")
-    su = msa.Shape(B=wu.B, T=wu.T, Hq=wu.Hq, G=wu.G, d=wu.d, d_idx=wu.d_idx, Bk=wu.Bk, k=wu.k)
-    hu = synth.make_inputs(rank_workload(wu, rank))
-    du = {n: torch.from_numpy(np.ascontiguousarray(hu[n]).view(np.int16)).view(torch.bfloat16).to(dev) for n in hu}
-    wsu = msa.alloc_workspace(su, msa.MSA_WS_BWD, dev)
-    biu = torch.empty((wu.B, wu.G, wu.T, wu.k), dtype=torch.int32, device=dev)
-    Ou = torch.empty_like(du["Q"])
-    LSEu = torch.empty((wu.B, wu.T, wu.Hq), dtype=torch.float32, device=dev)
-    outu = {n: torch.empty(du[src].shape, **f32) for n, src in (("dQ", "Q"), ("dK", "K"), ("dV", "V"),
-                                                                  ("dq_idx", "q_idx"), ("dk_idx", "k_idx"))}
-    outu["KL"] = torch.empty((wu.B, wu.G, wu.T), **f32)
+    # ---- indexer warmup: full causal attention and the KL against the dense teacher at this workload,
+    # through msa_dense_fwd + msa_dense_bwd (outputs in the step's buffers). A step is about a second at
+    # T = 131072: at most three timed steps.
+    warm = None
+    if w.Hq // w.G in (4, 8):
+        sd = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, d=w.d, d_idx=w.d_idx, Bk=w.Bk, k=1)
+        wsd = msa.alloc_workspace(sd, msa.MSA_WS_DENSE, dev)
+        dkev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for n in ("fwd", "bwd")}
+        for pair in dkev.values():
+            for x in pair:
+                x.record(stream)
 
-    def warmup_step():
-        msa.msa_warmup_block_idx(su, biu, stream)
-        msa.msa_sparse_fwd(su, du["Q"], du["K"], du["V"], biu, Ou, LSEu, wsu, stream)
-        msa.msa_bwd(su, du["Q"], du["K"], du["V"], Ou, du["dO"], LSEu, du["q_idx"], du["k_idx"], biu, 1.0,
-                    outu["dQ"], outu["dK"], outu["dV"], outu["dq_idx"], outu["dk_idx"], outu["KL"], wsu, stream)
+        def dense_step():
+            msa.msa_dense_fwd(sd, d_in["Q"], d_in["K"], d_in["V"], O, LSE, wsd, stream)
+            msa.msa_dense_bwd(sd, d_in["Q"], d_in["K"], d_in["V"], O, d_in["dO"], LSE, d_in["q_idx"], d_in["k_idx"],
+                              1.0, out["dQ"], out["dK"], out["dV"], out["dq_idx"], out["dk_idx"], out["KL"], wsd,
+                              stream)
 
-    for _ in range(args.warmup):
-        warmup_step()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    u0 = torch.cuda.Event(enable_timing=True)
-    u1 = torch.cuda.Event(enable_timing=True)
-    u0.record(stream)
-    for _ in range(args.steps):
-        warmup_step()
-    u1.record(stream)
-    torch.cuda.synchronize()
-    warm_ms = dist_max(u0.elapsed_time(u1) / args.steps, dev)
-    msa.msa_check_device_status(wsu, stream)
-    del wsu, du, Ou, LSEu, outu, biu
+        for _ in range(args.warmup):
+            dense_step()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        n_dense = min(args.steps, 3)
+        msa.msa_set_timing_events(msa.MSA_TIME_DENSE_FWD, *dkev["fwd"])
+        msa.msa_set_timing_events(msa.MSA_TIME_DENSE_BWD, *dkev["bwd"])
+        u0 = torch.cuda.Event(enable_timing=True)
+        u1 = torch.cuda.Event(enable_timing=True)
+        u0.record(stream)
+        for _ in range(n_dense):
+            dense_step()
+        u1.record(stream)
+        torch.cuda.synchronize()
+        msa.msa_set_timing_events(msa.MSA_TIME_DENSE_FWD, None, None)
+        msa.msa_set_timing_events(msa.MSA_TIME_DENSE_BWD, None, None)
+        msa.msa_check_device_status(wsd, stream)
+        warm_ms = dist_max(u0.elapsed_time(u1) / n_dense, dev)
+        wk = {n: dkev[n][0].elapsed_time(dkev[n][1]) for n in dkev}  # the last step's kernels
+        del wsd
+        ns = w.B * w.G * w.T * (w.T + 1) // 2  # causal (query, key) pairs
+        fwd_fl = 4 * w.d * (w.Hq // w.G) * ns
+        bwd_fl = 10 * w.d * (w.Hq // w.G) * ns + 6 * w.d_idx * ns
+        warm = {"workload": w.name.rsplit("_k", 1)[0] + "_full_attention", "steps": n_dense,
+                "ms_per_step": warm_ms, "tokens_per_s": aggregate_tokens_per_s(w, world, warm_ms),
+                "tflops": (fwd_fl + bwd_fl) / (warm_ms * 1e-3) / 1e12,
+                "dense_fwd_kernel": {"ms": wk["fwd"], "tflops": fwd_fl / (wk["fwd"] * 1e-3) / 1e12},
+                "bwd_wide_kernel_dense": {"ms": wk["bwd"], "tflops": bwd_fl / (wk["bwd"] * 1e-3) / 1e12},
+                "note": "indexer warmup at this workload: msa_dense_fwd + msa_dense_bwd (every visible token, "
+                        "KL against the dense teacher); counted FLOPs as for the sparse step over the T(T+1)/2 "
+                        "causal pairs; kernel times from CUDA events of the last timed step"}
 
     if rank == 0:
         fl = counted_flops(w)
@@ -621,11 +637,7 @@ def run_gpu(args, w):
             "index_topk_fp8": {"ms": fp8_ms, "tflops": fl["index"] / (fp8_ms * 1e-3) / 1e12,
                                "note": "msa_index_topk_fp8: E4M3 q_idx (per row) and k_idx (per block) with "
                                        "kind::f8f6f4 MMAs; same workload as index_topk"},
-            "indexer_warmup": {"workload": wu.name, "ms_per_step": warm_ms,
-                       "tokens_per_s": aggregate_tokens_per_s(wu, world, warm_ms),
-                       "tflops": (counted_flops(wu)["fwd"] + counted_flops(wu)["bwd"]) / (warm_ms * 1e-3) / 1e12,
-                       "note": "indexer warmup: msa_warmup_block_idx (every visible block) + msa_sparse_fwd + "
-                               "msa_bwd = dense causal attention and the dense-teacher KL"},
+            "indexer_warmup": warm,
         }
         if world == 1 and not args.no_cpu_baseline:
             line["selection_check"] = selection_check(w, host, sel_rows, sel_got)
