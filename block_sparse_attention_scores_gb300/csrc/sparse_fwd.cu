@@ -553,14 +553,48 @@ __global__ void __launch_bounds__(kMergeThreads)
     float acc[kPer];
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
-    for (int sidx = 0; sidx < k; ++sidx) {
-      const int r = s_row[wib][sidx];
-      if (r < 0) continue;
-      const float wgt = s_wgt[wib][sidx][my_head];
-      float v[kPer];
-      load_bf16_row<kPer>(o_part + (size_t)r * HG * 128 + lane * kPer, v);
+    // slots in ascending order, two rows' loads in flight before they are added
+    for (int s0 = 0; s0 < k; s0 += 2) {
+      int r[2];
+      uint4 raw[2][kPer / 8 > 0 ? kPer / 8 : 1];
+      uint2 raw4[2];
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) acc[i] = fmaf(wgt, v[i], acc[i]);
+      for (int j = 0; j < 2; ++j) {
+        r[j] = s0 + j < k ? s_row[wib][s0 + j] : -1;
+        if (r[j] >= 0) {
+          const __nv_bfloat16* row = o_part + (size_t)r[j] * HG * 128 + lane * kPer;
+          if constexpr (kPer % 8 == 0) {
+#pragma unroll
+            for (int q = 0; q < kPer / 8; ++q) raw[j][q] = reinterpret_cast<const uint4*>(row)[q];
+          } else {
+            raw4[j] = *reinterpret_cast<const uint2*>(row);
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (r[j] < 0) continue;
+        const float wgt = s_wgt[wib][s0 + j][my_head];
+        if constexpr (kPer % 8 == 0) {
+#pragma unroll
+          for (int q = 0; q < kPer / 8; ++q) {
+            const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw[j][q]);
+#pragma unroll
+            for (int z = 0; z < 4; ++z) {
+              const float2 f = __bfloat1622float2(h2[z]);
+              acc[q * 8 + 2 * z] = fmaf(wgt, f.x, acc[q * 8 + 2 * z]);
+              acc[q * 8 + 2 * z + 1] = fmaf(wgt, f.y, acc[q * 8 + 2 * z + 1]);
+            }
+          }
+        } else {
+          const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw4[j]);
+          const float2 f0 = __bfloat1622float2(h2[0]), f1 = __bfloat1622float2(h2[1]);
+          acc[0] = fmaf(wgt, f0.x, acc[0]);
+          acc[1] = fmaf(wgt, f0.y, acc[1]);
+          acc[2] = fmaf(wgt, f1.x, acc[2]);
+          acc[3] = fmaf(wgt, f1.y, acc[3]);
+        }
+      }
     }
     __syncwarp();  // the next row rewrites this warp's slot table
     const size_t orow0 = ((size_t)b * T + t) * Hq + g * HG;

@@ -16,8 +16,9 @@
 //   2. chunk scan  -- per list: exclusive prefix over qb (the chunk's first
 //                     position in the list) and the list length
 //   3. list scan   -- exclusive prefix over lists (and over lists padded to
-//                     whole tiles); work items in block-id-major order, which
-//                     is the order of decreasing expected list length
+//                     whole tiles); work items (b, g)-major, block id ascending
+//                     within a (b, g): the order of decreasing expected list
+//                     length
 //   4. scatter     -- one CTA per chunk again: an entry's position is its
 //                     chunk's offset plus the rows before it in the bitmap;
 //                     also the reverse map (b, g, t, slot) -> padded entry
@@ -145,10 +146,12 @@ __device__ __forceinline__ int block_scan_excl(int v, int* warp_sums, int* carry
   return excl;
 }
 
-// Work items of one kernel, in block-id-major order (the order of decreasing
-// expected list length): int4 {list, first entry, entries, padded offset of
-// the first entry}, at most per_item entries each. Called by one CTA of 1024
-// threads; `carry` is block-uniform scratch.
+// Work items of one kernel, (b, g)-major and block id ascending within a
+// (b, g) (the order of decreasing expected list length): int4 {list, first
+// entry, entries, padded offset of the first entry}, at most per_item entries
+// each. The CTAs running together then gather the query rows of one (b, g),
+// which L2 holds far better than the rows of every group. Called by one CTA
+// of 1024 threads; `carry` is block-uniform scratch.
 __device__ void emit_items(const int* __restrict__ count, const int* __restrict__ off,
                            const int* __restrict__ poff, int L, int BG, int n, int per_item,
                            int4* __restrict__ items, int max_items, int* __restrict__ n_items, int* err,
@@ -157,11 +160,10 @@ __device__ void emit_items(const int* __restrict__ count, const int* __restrict_
   if (tid == 0) *carry = 0;
   __syncthreads();
   for (int base = 0; base < L; base += 1024) {
-    const int j = base + tid;  // block-id-major index
+    const int j = base + tid;  // (b, g)-major index: list id
     int v = 0, lid = 0;
     if (j < L) {
-      const int c = j / BG, bg = j % BG;
-      lid = bg * n + c;
+      lid = j;
       v = (count[lid] + per_item - 1) / per_item;
     }
     const int first = block_scan_excl(v, warp_sums, carry);
