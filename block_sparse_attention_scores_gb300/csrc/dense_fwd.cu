@@ -268,19 +268,22 @@ __global__ void __launch_bounds__(kFThreads, 1)
       for (int c = 0; c <= qb; ++c, ++kc) {
         if (!mbar_wait(&sh.s_full[t], kc & 1, a.err, 1022 + t)) { ok = false; break; }
         tc_fence_after();
-        float sv[128];
+        float sv[128], mq[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tmem + lane_off + s_col + q * 32, *reinterpret_cast<float(*)[32]>(sv + 32 * q));
+        for (int q = 0; q < 4; ++q)
+          tmem_ld32_max(tmem + lane_off + s_col + q * 32, *reinterpret_cast<float(*)[32]>(sv + 32 * q), mq[q]);
         tmem_wait_ld();
-        if (c == qb) {  // the query's own block: keys after it are masked
+        float m_raw = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));  // the loads' own maximum
+        if (c == qb) {  // the query's own block: keys after it are masked, and the maximum is taken again
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int j = 0; j < 128; ++j)
+          for (int j = 0; j < 128; ++j) {
             if (j > row) sv[j] = -INFINITY;
+            m4[j & 3] = fmaxf(m4[j & 3], sv[j]);
+          }
+          m_raw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
-        float m4[4] = {sv[0], sv[1], sv[2], sv[3]};
-#pragma unroll
-        for (int j = 4; j < 128; ++j) m4[j & 3] = fmaxf(m4[j & 3], sv[j]);
-        const float m_blk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+        const float m_blk = m_raw * a.scale_log2;
         const bool need = m_blk > m_run + kHeadroom;
         if (__any_sync(0xffffffffu, need)) {
           // rescale l and (past the first block) O_t to the new maximum; PV_t of the previous block is done
@@ -508,22 +511,25 @@ __global__ void __launch_bounds__(kPThreads, 2)
         const int ab = ac & 1;
         if (!mbar_wait(&sh.acc_full[ab], (ac >> 1) & 1, a.err, 1122)) { ok = false; break; }
         tc_fence_after();
-        float xv[128];
+        float xv[128], mq[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(lane_addr + ab * 128 + q * 32, *reinterpret_cast<float(*)[32]>(xv + 32 * q));
+        for (int q = 0; q < 4; ++q)
+          tmem_ld32_max(lane_addr + ab * 128 + q * 32, *reinterpret_cast<float(*)[32]>(xv + 32 * q), mq[q]);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);
-        if (c == qb) {
+        float m_raw = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));  // the loads' own maximum
+        if (c == qb) {  // the own block: keys after the query are masked, the maximum taken again
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int j = 0; j < 128; ++j)
+          for (int j = 0; j < 128; ++j) {
             if (j > row) xv[j] = -INFINITY;
+            m4[j & 3] = fmaxf(m4[j & 3], xv[j]);
+          }
+          m_raw = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
         }
-        float m4[4] = {xv[0], xv[1], xv[2], xv[3]};
-#pragma unroll
-        for (int j = 4; j < 128; ++j) m4[j & 3] = fmaxf(m4[j & 3], xv[j]);
-        const float m_blk = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * a.scale_log2;
+        const float m_blk = m_raw * a.scale_log2;
         if (m_blk > m_run + kHeadroom) {
           l_run *= fast_exp2(m_run - m_blk);
           m_run = m_blk;

@@ -14,15 +14,15 @@
 // operand; every earlier KV block c < qb of k_idx (128 x 64) is a B operand.
 // Because Bk = 128 = UMMA N, the 128 fp32 columns of one accumulator are
 // exactly one block, so each epilogue thread (one TMEM lane = one query) takes
-// its block max with 127 fmax and inserts (max, c) into a register top-(k-1).
+// its block max (from TMEM loads that reduce as they read) and inserts
+// (max, c) into a register top-(k-1).
 // The own block needs no score: it is always kept.
 //
-// Warp roles (192 threads, 2 CTAs per SM or 4 (below), persistent over work items handed
+// Warp roles (192 threads, 2 CTAs per SM, persistent over work items handed
 // out largest-qb-first by an atomic counter):
 //   warp 0      TMA producer: q tile per item, k_idx tiles into a 4-stage ring
 //   warp 1      TMEM owner and UMMA issuer (one thread), 2 accumulators
-//               (FP8 with k <= 17: 1 accumulator, 4 CTAs per SM)
-//   warps 2..5  epilogue: tcgen05.ld, block max, running top-k, output
+//   warps 2..5  epilogue: tcgen05.ld.red (scores and their max), running top-k, output
 #include <cuda_fp8.h>
 
 #include "msa_internal.h"
@@ -36,12 +36,8 @@ constexpr int kStages = 4;
 constexpr int kTileBytes = 128 * 128;  // 128 rows x 64 bf16 (the FP8 path uses half of each tile)
 constexpr int kSmemBytes = (2 + kStages) * kTileBytes + 1024;
 constexpr int kSmem8 = (2 + kStages) * (kTileBytes / 2) + 1024;  // FP8: 8 KB tiles
-// CTAs per SM. FP8 with a short top-k list (k <= 17) runs four CTAs per SM
-// with one TMEM accumulator each: 16 epilogue warps per SM instead of 8, since
-// the epilogue, not the MMA, sets the pace; longer lists need the registers
-// of two CTAs per SM.
-template <int CAP, bool FP8>
-__host__ __device__ constexpr int topk_ctas() { return (FP8 && CAP <= 16) ? 4 : 2; }
+// CTAs per SM (each with two TMEM accumulators of 128 columns).
+constexpr int kCtasPerSm = 2;
 
 struct TopkArgs {
   int B, T, G, n, k;
@@ -98,11 +94,11 @@ __device__ __forceinline__ void topk_insert(float (&val)[CAP], int (&idx)[CAP], 
 // row's own scale is positive and common to all its blocks: it cannot change
 // the selection).
 template <int CAP, bool FP8>
-__global__ void __launch_bounds__(kThreads, topk_ctas<CAP, FP8>())
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     index_topk_kernel(TopkArgs a, const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k) {
   constexpr int kLoadBytes = FP8 ? kTileBytes / 2 : kTileBytes;  // bytes a q or k tile load brings
   constexpr int kTB = kLoadBytes;                                 // stage spacing in shared memory
-  constexpr int NACC = topk_ctas<CAP, FP8>() == 4 ? 1 : 2;        // TMEM accumulators (128 columns each)
+  constexpr int NACC = 2;                                         // TMEM accumulators (128 columns each)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sQ = smem;           // 2 q tiles
@@ -237,27 +233,23 @@ __global__ void __launch_bounds__(kThreads, topk_ctas<CAP, FP8>())
         idx[i] = -1;
       }
       bool ok = true;
+#pragma unroll 1
       for (int c = 0; c < qb; ++c, ++ac) {
         const int ab = ac % NACC;
         if (!mbar_wait(&sh.acc_full[ab], (ac / NACC) & 1, a.err, 122)) { ok = false; break; }
         tc_fence_after();
-        float m0 = -INFINITY, m1 = -INFINITY;
+        // the block max comes from the loads themselves (the scores are not otherwise needed)
+        float mq[4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float v0[32], v1[32];
-          tmem_ld32(lane_addr + ab * 128 + h * 64, v0);
-          tmem_ld32(lane_addr + ab * 128 + h * 64 + 32, v1);
+        for (int q = 0; q < 4; ++q) {
+          float v[32];
+          tmem_ld32_max(lane_addr + ab * 128 + q * 32, v, mq[q]);
           tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            m0 = fmaxf(m0, fmaxf(v0[i], v0[i + 1]));
-            m1 = fmaxf(m1, fmaxf(v1[i], v1[i + 1]));
-          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.acc_empty[ab]);
-        float mx = fmaxf(m0, m1);
+        float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
         if constexpr (FP8) mx *= a.k_scale[(size_t)b * a.n + c];
         topk_insert<CAP>(val, idx, mx, c);
       }
@@ -302,7 +294,7 @@ cudaError_t launch_cap(const Prob& p, const TopkArgs& args, const CUtensorMap& m
   constexpr int smem_bytes = FP8 ? kSmem8 : kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
   if (e != cudaSuccess) return e;
-  const int grid = min(args.num_items, topk_ctas<CAP, FP8>() * num_sms());
+  const int grid = min(args.num_items, kCtasPerSm * num_sms());
   timing_begin(MSA_TIME_INDEX_TOPK, st);
   kern<<<grid, kThreads, smem_bytes, st>>>(args, mq, mk);
   timing_end(MSA_TIME_INDEX_TOPK, st);
