@@ -254,24 +254,30 @@ __global__ void __launch_bounds__(kPxThreads, 1)
         const int lim = entry >= 0 ? (entry >> 8) - c * 128 : -1;
         if (!mbar_wait(&sh.s_full[sb], (tj >> 1) & 1, a.err, 422)) { ok = false; break; }
         tc_fence_after();
-        float x[128];
+        float x[128], mq[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-          tmem_ld32(tmem + lane_off + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(x + q * 32));
+          tmem_ld32_max(tmem + lane_off + sb * 128 + q * 32, *reinterpret_cast<float(*)[32]>(x + q * 32), mq[q]);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.s_empty[sb]);
-        float m = -INFINITY;
+        float mm, l = 0.f;
+        if (lim >= 127) {  // every key visible: the loads' own maximum (scale > 0 keeps it the maximum)
+          mm = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
 #pragma unroll
-        for (int i = 0; i < 128; ++i) {
-          x[i] = (i <= lim) ? x[i] * a.scale_log2 : -INFINITY;
-          m = fmaxf(m, x[i]);
+          for (int i = 0; i < 128; ++i) l += fast_exp2(fmaf(x[i], a.scale_log2, -mm));
+        } else {
+          float m = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            x[i] = (i <= lim) ? x[i] * a.scale_log2 : -INFINITY;
+            m = fmaxf(m, x[i]);
+          }
+          mm = (m == -INFINITY) ? 0.f : m;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) l += fast_exp2(x[i] - mm);
         }
-        const float mm = (m == -INFINITY) ? 0.f : m;
-        float l = 0.f;
-#pragma unroll
-        for (int i = 0; i < 128; ++i) l += fast_exp2(x[i] - mm);
         if (entry >= 0) {
           const int t = entry >> 8, slot = entry & 255;
           a.px_part[(((size_t)b * a.T + t) * a.G + g) * a.k + slot] = (mm + __log2f(l)) * kLn2;

@@ -374,12 +374,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float x[32];
-          tmem_ld32(tmem + lane_off + s_col + q * 32, x);
-          tmem_wait_ld();
-          if (full) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
+          if (full) {  // the loads' own maximum (tcgen05.ld.red)
+            tmem_ld32_max(tmem + lane_off + s_col + q * 32, x, m4[q]);
+            tmem_wait_ld();
           } else {
+            tmem_ld32(tmem + lane_off + s_col + q * 32, x);
+            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i)
               if (q * 32 + i <= lim) m4[i & 3] = fmaxf(m4[i & 3], x[i]);
