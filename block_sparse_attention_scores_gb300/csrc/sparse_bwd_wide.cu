@@ -527,6 +527,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the readers of the previous gs^T included)
         if (!mbar_wait(&sh.x_full, par, a.err, 633)) { ok = false; break; }
         tc_fence_after();
+        // the previous tile's gather buffer goes back to the producers as early as it can: every MMA on it
+        // is done (X^T of this tile was issued after them) and its partial stores, issued a stage ago, have
+        // read their staging; the next tile's gather is what the tensor core waits for
+        if (rel_gb >= 0) {
+          if (lane == 0) {
+            bulk_wait_read_all();
+            mbar_arrive(&sh.g_empty[rel_gb]);
+          }
+          __syncwarp();
+          rel_gb = -1;
+        }
         float xv[kHQ];
         tmem_ld_cols<kHQ>(tmem + lane_off + cP + hf * kHQ, xv);
         tmem_wait_ld();
@@ -545,16 +556,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.p_ready);
-        // the previous tile's gather buffer: every MMA on it is done (X^T of this tile was issued after
-        // them) and its partial stores have had a stage to read their staging
-        if (rel_gb >= 0) {
-          if (lane == 0) {
-            bulk_wait_read_all();
-            mbar_arrive(&sh.g_empty[rel_gb]);
-          }
-          __syncwarp();
-          rel_gb = -1;
-        }
         // ---- stage B: dS = P (dP - D) * scale, bf16. Packed into R's first 64 columns (the
         // TMEM A operand of dK) once every warp has loaded dP^T, and copied into the dO area
         // (the B operand of dQ^T) once dV has read dO
