@@ -1296,6 +1296,21 @@ cudaError_t launch_bwd_dense(const Prob& p, const void* Q, const void* K, const 
   if ((e = launch_dense_px(p, q_idx, k_idx, lse_px, ws, L, st)) != cudaSuccess) return e;
   BwdMaps mp;
   if (!make_bwd_maps(p, Q, K, V, dO, q_idx, k_idx, &mp)) return cudaErrorInvalidValue;
+  {
+    // a tile's queries are consecutive tokens: whole-tile boxes (128 / hg tokens) for Q, dO and q_idx
+    const uint32_t npos = 128 / p.hg;
+    const uint64_t dims[3] = {128, (uint64_t)p.Hq, (uint64_t)p.BT()};
+    const uint64_t strides[2] = {256, (uint64_t)p.Hq * 256};
+    const uint32_t box[3] = {64, (uint32_t)p.hg, npos};
+    if (!encode_tmap(&mp.mq, const_cast<void*>(Q), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap(&mp.mdo, const_cast<void*>(dO), 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    const uint64_t dims2[3] = {64, (uint64_t)p.G, (uint64_t)p.BT()};
+    const uint64_t strides2[2] = {128, (uint64_t)p.G * 128};
+    const uint32_t box2[3] = {64, 1, npos};
+    if (!encode_tmap(&mp.mqi, const_cast<void*>(q_idx), 3, dims2, strides2, box2, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+  }
   CUtensorMap mdq;
   {
     // the caller's fp32 dQ, added into per half tile: 32 d x hg heads x (64 / hg) queries

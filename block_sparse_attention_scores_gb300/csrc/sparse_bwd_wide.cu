@@ -304,6 +304,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const unsigned dg = __ballot_sync(0xffffffffu, mine && e_own >= 0 && (e_own >> 8) < key_last);
+        if constexpr (DENSE) {
+          // consecutive queries: producer 0 loads the whole tile with five boxes (Q and dO per 64-column
+          // chunk: 128 / hg tokens x hg heads, landing at row q * hg as the one-query boxes would; q_idx:
+          // one row per token); the other producers only write their rows' metadata
+          if (lane == 0) {
+            m.diag[p] = dg != 0u;
+            if (p == 0) {
+              mbar_arrive_expect_tx(&sh.g_full[gb], npos * (2 * hg * 256 + 128));
+              const int bt0 = b * a.T + item.y + j * npos;
+              tma_load_3d(buf + oQ, &map_q, &sh.g_full[gb], 0, g * hg, bt0);
+              tma_load_3d(buf + oQ + kChunk, &map_q, &sh.g_full[gb], 64, g * hg, bt0);
+              tma_load_3d(buf + oDO, &map_do, &sh.g_full[gb], 0, g * hg, bt0);
+              tma_load_3d(buf + oDO + kChunk, &map_do, &sh.g_full[gb], 64, g * hg, bt0);
+              tma_load_3d(buf + oQI, &map_qi, &sh.g_full[gb], 0, g, bt0);
+            } else {
+              mbar_arrive(&sh.g_full[gb]);
+            }
+          }
+          __syncwarp();
+        } else {
         if (lane == 0) {
           m.diag[p] = dg != 0u;
           mbar_arrive_expect_tx(&sh.g_full[gb], nq * (2 * hg * 256 + 128));
@@ -327,6 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
+        }
         if (j + 1 < ntiles) {
           rec = load_rec(b, g, e_next);
           e_next = j + 2 < ntiles ? load_entry(item, j + 2) : -1;
