@@ -453,12 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ss_w(tmem + cR, kT + 128 * ks, gT + (oDO >> 4) + 128 * ks, hi, id_dq, ks > 0);
           umma_commit(&sh.dq_full);
-          if (j + 1 < ntiles) {  // the next tile's S^T, as soon as this dQ^T has left R
-            if (!issue_s(tj + 1)) { ok = false; break; }
-            s_issued = true;
-          }
-          // index branch (gs^T written long before, in stage A): dk_idx += gs^T QI, dq_idx^T = KI^T gs^T
-          // into P, after dV has read P^T (same issuing thread: in order)
+          // index branch (gs^T, stored by the epilogue at the end of its stage C1, while dQ^T runs):
+          // dk_idx += gs^T QI, dq_idx^T = KI^T gs^T into P, after dV has read P^T (same issuing thread: in
+          // order). It goes before the next tile's S^T, which has slack, so that the warps reading dq_idx^T
+          // find it done
           if (!mbar_wait(&sh.gs_ready, par, a.err, 620)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
@@ -469,6 +467,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_bf16_ss_w2(tmem + cP, iT + 128 * ks, hi, gsB + ks * (2 * kGsAtom >> 4), hiGS, id_dqi, ks > 0);
 #undef KSTEP
           umma_commit(&sh.ph2_full);
+          if (j + 1 < ntiles) {  // the next tile's S^T, once this dQ^T has left R
+            if (!issue_s(tj + 1)) { ok = false; break; }
+            s_issued = true;
+          }
         }
         umma_commit(&sh.kv_empty);
       }
@@ -483,7 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = 64 * hf;                // this half's tile rows
     const int kk = quarter * 32 + lane;      // TMEM lane: key (S, dP, P, X), d (dQ^T), e (dq_idx^T)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool kl_writer = warp == 8;
+    // the per-tile KL write falls to a warp of TMEM lanes 64..127, which reads no dq_idx^T (the warps of
+    // lanes 0..63 set the tile's pace)
+    const bool kl_writer = warp == 10;
     uint32_t tj = 0;
     bool ok = true;
     int rel_gb = -1;  // gather buffer whose partial stores must finish reading before it is handed back
@@ -646,6 +650,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             gp[q2] = pack_bf16(gsv[0], gsv[1]);
           }
+          // gs^T into shared memory for the index MMAs, issued right after dQ^T (the previous tile's, the
+          // last readers of this image, were done before this tile's X^T)
+          // gs^T row kk: 16-byte chunks of 8 queries, swizzled like the TMA image of the same width
+          if constexpr (npos == 32) {
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc)
+              *reinterpret_cast<uint4*>(smem + oGS + kk * 64 + (((2 * hf + cc) ^ ((kk >> 1) & 3)) << 4)) =
+                  make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
+          } else {
+            *reinterpret_cast<uint4*>(smem + oGS + kk * 32 + ((hf ^ ((kk >> 2) & 1)) << 4)) =
+                make_uint4(gp[0], gp[1], gp[2], gp[3]);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sh.gs_ready);
         }
         // ---- stage D1: read out dQ^T (lane = d) as bf16 slot partials, staged where dS^T was
         // (dQ^T is its last reader); R goes back to the tensor core for the next tile's S^T
@@ -700,22 +719,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
           }
         }
-        // ---- stage C2: gs^T for the index MMAs (the previous tile's were done before this tile's
-        // X^T), and the KL sums
+        // ---- stage C2: the KL sums
         {
-          // gs^T row kk: 16-byte chunks of 8 queries, swizzled like the TMA image of the same width
-          if constexpr (npos == 32) {
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc)
-              *reinterpret_cast<uint4*>(smem + oGS + kk * 64 + (((2 * hf + cc) ^ ((kk >> 1) & 3)) << 4)) =
-                  make_uint4(gp[4 * cc], gp[4 * cc + 1], gp[4 * cc + 2], gp[4 * cc + 3]);
-          } else {
-            *reinterpret_cast<uint4*>(smem + oGS + kk * 32 + ((hf ^ ((kk >> 2) & 1)) << 4)) =
-                make_uint4(gp[0], gp[1], gp[2], gp[3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.gs_ready);
           // KL terms summed over the 128 keys: lanes by a butterfly, the four
           // key quarters by shared atomics into the tile's cleared sums
           if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
