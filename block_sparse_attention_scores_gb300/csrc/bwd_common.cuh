@@ -27,7 +27,7 @@ struct BwdArgs {
   float* dV;
   __nv_bfloat16* dq_part;  // [padded entries, hg, d], tile order
   __nv_bfloat16* dqi_part; // [padded entries, E], tile order
-  float* kl_part;          // [B,T,G,k]
+  float* kl_part;          // [B,T,G,k,4]: per slot, the four key quarters' KL sums
   float* dki_part;         // [B,G,T,E]
   // Full attention (every query t >= 128 c sees block c): the lists are not
   // stored but cut into segments of dense_seg queries; the outputs are the
@@ -76,10 +76,16 @@ __device__ __forceinline__ void decode_list(int l, int n, int G, int& b, int& g,
 }
 
 // Sum over the 32 lanes of NV per-lane values, with a butterfly that halves
-// the values a lane keeps at each step (NV - 1 shuffles instead of 5 NV), then
-// add each sum into acc[] (one shared atomic per value, distinct addresses).
+// the values a lane keeps at each step (NV - 1 shuffles instead of 5 NV). On
+// return the lanes with lane % kDup == 0 hold in v[0 .. kKeep) the sums of the
+// values [base, base + kKeep); the function returns base.
 template <int NV>
-__device__ __forceinline__ void lanes_sum_add(float (&v)[NV], int lane, float* acc) {
+struct LanesSum {
+  static constexpr int kKeep = NV >= 32 ? NV / 32 : 1;
+  static constexpr int kDup = NV >= 32 ? 1 : 32 / NV;  // lanes holding the same sums
+};
+template <int NV>
+__device__ __forceinline__ int lanes_sum(float (&v)[NV], int lane) {
   int base = 0;
 #pragma unroll
   for (int s = 0; s < 5; ++s) {
@@ -100,12 +106,7 @@ __device__ __forceinline__ void lanes_sum_add(float (&v)[NV], int lane, float* a
       v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
     }
   }
-  constexpr int kKeep = NV >= 32 ? NV / 32 : 1;
-  constexpr int kDup = NV >= 32 ? 1 : 32 / NV;  // lanes holding the same sums
-  if ((lane & (kDup - 1)) == 0) {
-#pragma unroll
-    for (int i = 0; i < kKeep; ++i) atomicAdd(&acc[base + i], v[i]);
-  }
+  return base;
 }
 
 }  // namespace bwdc

@@ -145,7 +145,7 @@ WsLayout ws_layout(const Prob& p, int which) {
     L.lse_px = take(rows * p.G * 4);
     L.dq_part = take((size_t)L.max_padded * p.hg * p.d * 2);
     L.dqi_part = take((size_t)L.max_padded * p.E * 2);
-    L.kl_part = take(rows * p.G * p.k * 4);
+    L.kl_part = take(rows * p.G * p.k * 16);
     L.dki_part = take((size_t)p.B * p.G * p.T * p.E * 4);
     L.o_part = L.dq_part;
     L.lse_part = take((size_t)L.max_padded * p.hg * 4);

@@ -42,7 +42,7 @@ struct WsLayout {
   size_t lse_px = 0;        // fp32  [B,T,G]        index-branch LSE over S(g,t)
   size_t dq_part = 0;       // bf16  [padded entries, hg, d] dQ partials, tile order
   size_t dqi_part = 0;      // bf16  [padded entries, E]     dq_idx partials, tile order
-  size_t kl_part = 0;       // fp32  [B,T,G,k]      KL partials per slot
+  size_t kl_part = 0;       // fp32  [B,T,G,k,4]    KL partials per slot and key quarter
   size_t dki_part = 0;      // fp32  [B,G,T,E]      dk_idx per group
   size_t q8 = 0;            // e4m3  [B,T,G,E]      FP8 index queries (MSA_WS_TOPK_FP8)
   size_t k8 = 0;            // e4m3  [B,T,E]        FP8 index keys

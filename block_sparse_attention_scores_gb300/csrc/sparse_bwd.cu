@@ -38,7 +38,8 @@ namespace {
 
 using bwdc::decode_list;
 using bwdc::fast_exp2;
-using bwdc::lanes_sum_add;
+using bwdc::LanesSum;
+using bwdc::lanes_sum;
 using bwdc::pack_bf16;
 constexpr float kLog2e = kBwdLog2e;
 constexpr float kLn2 = kBwdLn2;
@@ -351,9 +352,7 @@ struct BwdShared {
   uint64_t r_free[2], x_free;  // a tile's dQ^T / dq_idx^T read out of TMEM (by tile parity / every tile)
   uint64_t pv_free;            // dV += P^T dO of a tile complete: P^T may be overwritten
   uint64_t acc_free;
-  uint64_t kl_ready, kl_free;  // KL sums of a tile complete / read and cleared
   RowMeta meta[3];  // one per gather buffer
-  float kl_acc[kRows];  // per-query KL sum of the current tile (shared atomics of the 8 epilogue warps)
   int4 item[2];
   uint32_t tmem_base;
   int abort;
@@ -396,7 +395,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   BwdShared& sh = *reinterpret_cast<BwdShared*>(smem + L::oSh);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kRows; ++i) sh.kl_acc[i] = 0.f;
     for (int i = 0; i < 8; ++i) sh.meta[0].diag[i] = sh.meta[1].diag[i] = sh.meta[2].diag[i] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
@@ -421,8 +419,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(&sh.x_free, 8);
     mbar_init(&sh.pv_free, 1);
     mbar_init(&sh.acc_free, 8);
-    mbar_init(&sh.kl_ready, 8);
-    mbar_init(&sh.kl_free, 1);
     sh.abort = 0;
     fence_barrier_init();
   }
@@ -709,7 +705,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int col0 = 32 * hf;
     const int kk = quarter * 32 + lane;  // TMEM lane: key in block c (phase 1), d (dQ^T), e (dq_idx^T)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool kl_writer = warp == 2;   // a quarter-2 warp: no dq_idx^T rows to store
     uint32_t tj = 0;
     bool ok = true;
     // Tile whose phase-2 results (dQ^T, dq_idx^T) are still in TMEM: they are
@@ -717,7 +712,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // tile's dP^T while this readout runs.
     bool pend = false;
     uint32_t p_tj = 0;
-    int p_pos0 = 0, p_b = 0, p_g = 0;
+    int p_pos0 = 0;
     // Gather buffer whose staged partials are being stored: it goes back to
     // the producers once the stores have read it, checked one stage later so
     // the wait stays off the epilogue's path.
@@ -740,7 +735,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // stores have read it.
     auto epi2 = [&]() -> bool {
       const int pgb = p_tj % kNG;
-      const RowMeta& mp = sh.meta[pgb];
       if (!mbar_wait(&sh.ph2_full, p_tj & 1, a.err, 524)) return false;
       tc_fence_after();
       {
@@ -770,17 +764,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           if (quarter < 2) tma_store_2d(&map_dqi, stq, quarter * 32, p_pos0 + hf * kQ);
           bulk_commit();
         }
-      }
-      if (kl_writer) {
-        // every epilogue warp has added its KL terms: write the per-query sums
-        if (!mbar_wait(&sh.kl_ready, p_tj & 1, a.err, 526)) return false;
-        for (int q = lane; q < npos; q += 32) {
-          const int e = mp.ent[q * hg];
-          if (e >= 0) a.kl_part[(((size_t)p_b * a.T + (e >> 8)) * a.G + p_g) * a.k + (e & 255)] = sh.kl_acc[q];
-          sh.kl_acc[q] = 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.kl_free);
       }
       rel_gb = pgb;
       return true;
@@ -926,18 +909,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&sh.gs_ready);
-          // KL terms summed over the 128 keys: lanes by a butterfly, the four
-          // key quarters by shared atomics into the tile's cleared sums
-          if (!mbar_wait(&sh.kl_free, (tj & 1) ^ 1, a.err, 525)) { ok = false; break; }
-          lanes_sum_add<kQ>(term, lane, sh.kl_acc + hf * kQ);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.kl_ready);
+          // KL terms summed over this warp's 32 keys (a butterfly over the lanes); each key quarter
+          // writes its own sums, which the merge adds in order (the same bits in every run)
+          const int base = lanes_sum<kQ>(term, lane);
+          if ((lane & (LanesSum<kQ>::kDup - 1)) == 0) {
+#pragma unroll
+            for (int i = 0; i < LanesSum<kQ>::kKeep; ++i) {
+              const int e = m.ent[col0 + (base + i) * hg];
+              if (e >= 0)
+                a.kl_part[((((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)) * 4 + quarter] = term[i];
+            }
+          }
         }
         pend = true;  // this tile's dQ^T / dq_idx^T are read out after the next tile's stage A
         p_tj = tj;
         p_pos0 = item.w + j * npos;
-        p_b = b;
-        p_g = g;
       }
       if (!ok) break;
       if (pend) {
@@ -1045,7 +1031,10 @@ __global__ void bwd_merge_kernel(const int32_t* __restrict__ block_idx, const in
         if (r >= 0 && (long long)r >= max_padded) r = -1;
       }
       rv_own[u] = r;
-      if (r >= 0) kl_own += kl_part[(size_t)w * k + sidx];
+      if (r >= 0) {  // the slot's four key-quarter sums, in order
+        const float4 q4 = reinterpret_cast<const float4*>(kl_part)[(size_t)w * k + sidx];
+        kl_own += ((q4.x + q4.y) + q4.z) + q4.w;
+      }
     }
     float acc[kPer];
 #pragma unroll

@@ -53,7 +53,8 @@ namespace {
 
 using bwdc::decode_list;
 using bwdc::fast_exp2;
-using bwdc::lanes_sum_add;
+using bwdc::LanesSum;
+using bwdc::lanes_sum;
 using bwdc::pack_bf16;
 constexpr float kLog2e = kBwdLog2e;
 constexpr float kLn2 = kBwdLn2;
@@ -91,9 +92,8 @@ struct Shared {
   uint64_t g_full[2], g_empty[2];
   uint64_t s_full, x_full, s_read, x_read, dp_full, dp_read, p_ready, pv_done, ds_tmem, ds_smem, dk_done;
   uint64_t gs_ready, dq_full, ph2_full;
-  uint64_t r_free, x_free, acc_free, kl_ready, kl_free;
+  uint64_t r_free, x_free, acc_free;
   RowMeta meta[2];
-  float kl_acc[32];
   int4 item[2];
   uint32_t tmem_base;
   int abort;
@@ -159,7 +159,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Shared& sh = *reinterpret_cast<Shared*>(smem + oSh);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < npos; ++i) sh.kl_acc[i] = 0.f;
     for (int i = 0; i < 8; ++i) sh.meta[0].diag[i] = sh.meta[1].diag[i] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.it_full[i], 1);
@@ -186,8 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sh.r_free, 8);
     mbar_init(&sh.x_free, 4);  // the warps of TMEM lanes 0..63, which hold dq_idx^T
     mbar_init(&sh.acc_free, 8);
-    mbar_init(&sh.kl_ready, 8);
-    mbar_init(&sh.kl_free, 1);
     sh.abort = 0;
     fence_barrier_init();
   }
@@ -485,9 +482,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int col0 = 64 * hf;                // this half's tile rows
     const int kk = quarter * 32 + lane;      // TMEM lane: key (S, dP, P, X), d (dQ^T), e (dq_idx^T)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // the per-tile KL write falls to a warp of TMEM lanes 64..127, which reads no dq_idx^T (the warps of
-    // lanes 0..63 set the tile's pace)
-    const bool kl_writer = warp == 10;
     uint32_t tj = 0;
     bool ok = true;
     int rel_gb = -1;  // gather buffer whose partial stores must finish reading before it is handed back
@@ -719,17 +713,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_commit();
           }
         }
-        // ---- stage C2: the KL sums
+        // ---- stage C2: the KL terms summed over this warp's 32 keys (a butterfly over the lanes); each key
+        // quarter writes its own sums, which the merge adds in order (the same bits in every run)
         {
-          // KL terms summed over the 128 keys: lanes by a butterfly, the four
-          // key quarters by shared atomics into the tile's cleared sums
-          if (!mbar_wait(&sh.kl_free, par ^ 1, a.err, 628)) { ok = false; break; }
-          lanes_sum_add<kHQ>(term, lane, sh.kl_acc + hf * kHQ);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sh.kl_ready);
+          const int base = lanes_sum<kHQ>(term, lane);
+          if ((lane & (LanesSum<kHQ>::kDup - 1)) == 0) {
+#pragma unroll
+            for (int i = 0; i < LanesSum<kHQ>::kKeep; ++i) {
+              const int e = m.ent[hf * kHQ + base + i];
+              if (e < 0) continue;
+              if constexpr (DENSE)
+                atomicAdd(a.KL + ((size_t)b * a.G + g) * a.T + (e >> 8), term[i]);
+              else
+                a.kl_part[((((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)) * 4 + quarter] = term[i];
+            }
+          }
         }
         // ---- stage D2: dq_idx^T (TMEM lanes 0..63) as bf16 slot partials, staged where Q was (dK,
-        // its last reader, is done); the per-query KL sums
+        // its last reader, is done)
         {
           if (quarter < 2) {
             if (!mbar_wait(&sh.ph2_full, par, a.err, 630)) { ok = false; break; }
@@ -757,20 +758,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           rel_gb = gb;
-          if (kl_writer) {  // every epilogue warp has added its KL terms: write the per-query sums
-            if (!mbar_wait(&sh.kl_ready, par, a.err, 631)) { ok = false; break; }
-            for (int q = lane; q < npos; q += 32) {
-              const int e = m.ent[q];
-              if constexpr (DENSE) {
-                if (e >= 0) atomicAdd(a.KL + ((size_t)b * a.G + g) * a.T + (e >> 8), sh.kl_acc[q]);
-              } else {
-                if (e >= 0) a.kl_part[(((size_t)b * a.T + (e >> 8)) * a.G + g) * a.k + (e & 255)] = sh.kl_acc[q];
-              }
-              sh.kl_acc[q] = 0.f;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.kl_free);
-          }
         }
       }
       if (!ok) break;
