@@ -21,9 +21,11 @@
 //   dQ^T = K_c^T dS^T  (N = 128)       -> bf16 slot partial, TMA store
 //   gs   = w (p_px - p_main)           dk_idx += gs^T QI (TMEM, whole list)
 //   dq_idx^T = KI_c^T gs^T             -> bf16 slot partial, TMA store
+//   KL terms summed over each warp's 32 keys -> fp32 partial per (slot, key quarter)
 // Every MMA of a tile has N = 128 except the index ones, so the tensor pipe
 // runs near its per-instruction rate instead of at the N = 64 floor of a
-// 64-row tile.
+// 64-row tile. The merge adds slot partials (and a slot's four key-quarter KL
+// sums) in a fixed order, so every output is the same in every run.
 //
 // TMEM (512 columns): R [0, 128) holds S^T, then dP^T (once the epilogue has
 // loaded S^T), then dQ^T; P [128, 192) holds X^T, then P^T as packed bf16
@@ -31,11 +33,18 @@
 // read P^T); dV [192, 320), dK [320, 448), dk_idx [448, 512) accumulate over
 // the list.
 //
-// Shared memory: K, V, k_idx of the block (80 KB) and two gather buffers of
-// 68 KB (Q, dO: 128 rows x 256 B each; q_idx: one 128-byte row per query).
-// Inside a tile's buffer, dS^T goes where dO was (once dV has read it), gs^T
-// where Q was (once dK has read it), and the dQ / dq_idx partials are staged
-// there for their TMA stores.
+// Shared memory: K, V, k_idx of the block (80 KB), two gather buffers of
+// 68 KB (Q, dO: 128 rows x 256 B each; q_idx: one 128-byte row per query) and
+// the tile's gs^T image (8 KB). Inside a tile's buffer, dS^T goes where dO was
+// (once dV has read it), and the dQ partials (where dS^T was) and dq_idx
+// partials (where Q was) are staged for their TMA stores. A buffer goes back
+// to the producers once the next tile's X^T is complete.
+//
+// Full attention (DENSE): the lists are every query from the block on, built
+// from the item number in segments of 4096 queries; a tile's queries are
+// consecutive tokens, gathered with five whole-tile boxes; dQ is added into
+// the caller's fp32 dQ by TMA reduce-add, dq_idx, KL, dK, dV and dk_idx by
+// atomic adds.
 //
 // Warp roles (512 threads, one CTA per SM, persistent; registers split 64 /
 // 192 between the first two warpgroups and the last two):

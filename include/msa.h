@@ -180,7 +180,10 @@ MSA_API msa_status msa_sparse_fwd(const msa_shape *shape, const void *Q, const v
  * fully written: every key block is selected at least by its own queries, so
  * every dK/dV/dk_idx row receives its sum (rows of a block whose queries all
  * had invalid block_idx rows are unspecified, as is everything else when the
- * device error word is set).
+ * device error word is set). Every sum runs in a fixed order (per-slot and
+ * per-group partials, merged in order; no floating-point atomics), so the
+ * outputs, like those of msa_index_topk and msa_sparse_fwd, are the same bits
+ * in every run on the same inputs.
  */
 MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K, const void *V, const void *O,
                    const void *dO, const float *LSE, const void *q_idx, const void *k_idx,
@@ -311,7 +314,7 @@ MSA_API msa_status msa_selftest_wait_timeout(void *workspace, int32_t limit_us, 
 enum {
   MSA_TIME_INDEX_TOPK = 0, /* index_topk_kernel (msa_index_topk, msa_index_topk_fp8, the no-workspace call) */
   MSA_TIME_SPARSE_FWD = 1, /* sparse_fwd_kernel (msa_sparse_fwd, msa_sparse_fwd_mapped), not the map or merge */
-  MSA_TIME_BWD = 2,        /* bwd_kernel (msa_bwd, msa_bwd_mapped), not the pre-passes or merges */
+  MSA_TIME_BWD = 2,        /* the fused backward kernel (msa_bwd, msa_bwd_mapped), not the pre-passes or merges */
   MSA_TIME_DENSE_FWD = 3,  /* dense_fwd_kernel (msa_dense_fwd) */
   MSA_TIME_DENSE_BWD = 4   /* the backward kernel of msa_dense_bwd, not D or the index LSE */
 };
