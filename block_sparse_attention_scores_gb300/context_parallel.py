@@ -20,8 +20,11 @@ group-parallel one:
 Requirements: G % W == 0 and T % W == 0 (each shard a whole number of
 tokens; the per-rank T stays the full T, so the kernels' own T % 128 rule
 applies unchanged). ``compute`` is the per-rank hot path: ``cuda_compute``
-(the library's entry points on the rank's current GPU) in production; any
-function of the same signature for checking the exchange on CPU ranks.
+(the library's entry points on the rank's current GPU) in production,
+``cuda_compute_dense`` for the indexer warmup's full attention (itinai.ru
+"How to solve the memory problem with MiniMax Sparse Attention", "Training
+sparse attention"; no selection, so no block_idx); any function of the same
+signature for checking the exchange on CPU ranks.
 """
 from __future__ import annotations
 
@@ -131,7 +134,8 @@ def cp_step(s: LayerShape, shards: dict, compute, kl_weight: float = 1.0, group=
     t = {n: seq_to_heads(shards[n], *AXES[n], world, group) for n in ("Q", "K", "V", "dO", "q_idx")}
     t["k_idx"] = gather_seq(shards["k_idx"], world, group)
     out = compute(loc, t, kl_weight)
-    res = {n: heads_to_seq(out[n], *AXES[n], world, group) for n in OUTPUTS if n != "dk_idx"}
+    # the outputs the compute gives (full attention has no block_idx)
+    res = {n: heads_to_seq(out[n], *AXES[n], world, group) for n in OUTPUTS if n != "dk_idx" and n in out}
     res["dk_idx"] = reduce_scatter_seq(out["dk_idx"], world, group)
     return res
 
@@ -159,3 +163,26 @@ def cuda_compute(s: LayerShape, t: dict, kl_weight: float = 1.0) -> dict:
                        g["dQ"], g["dK"], g["dV"], g["dq_idx"], g["dk_idx"], g["KL"], ws, st)
     msa.msa_check_device_status(ws, st)
     return dict(block_idx=bi, O=O, LSE=LSE, **g)
+
+
+def cuda_compute_dense(s: LayerShape, t: dict, kl_weight: float = 1.0) -> dict:
+    """Full attention (the indexer warmup) on the current GPU: msa_dense_fwd ->
+    msa_dense_bwd over every visible token of the rank's groups (4 or 8 heads
+    per group). The outputs are those of cuda_compute without block_idx."""
+    import block_sparse_attention_scores_gb300 as msa
+
+    shape = msa.Shape(B=s.B, T=s.T, Hq=s.Hq, G=s.G, d=s.d, d_idx=s.d_idx, Bk=s.Bk, k=1)
+    dev = t["Q"].device
+    ws = msa.alloc_workspace(shape, msa.MSA_WS_DENSE, dev)
+    st = torch.cuda.current_stream(dev)
+    O = torch.empty_like(t["Q"])
+    LSE = torch.empty((s.B, s.T, s.Hq), dtype=torch.float32, device=dev)
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(dQ=torch.empty(t["Q"].shape, **f32), dK=torch.empty(t["K"].shape, **f32),
+             dV=torch.empty(t["V"].shape, **f32), dq_idx=torch.empty(t["q_idx"].shape, **f32),
+             dk_idx=torch.empty(t["k_idx"].shape, **f32), KL=torch.empty((s.B, s.G, s.T), **f32))
+    msa.msa_dense_fwd(shape, t["Q"], t["K"], t["V"], O, LSE, ws, st)
+    msa.msa_dense_bwd(shape, t["Q"], t["K"], t["V"], O, t["dO"], LSE, t["q_idx"], t["k_idx"], kl_weight,
+                      g["dQ"], g["dK"], g["dV"], g["dq_idx"], g["dk_idx"], g["KL"], ws, st)
+    msa.msa_check_device_status(ws, st)
+    return dict(O=O, LSE=LSE, **g)

@@ -9,6 +9,8 @@ dk_idx is reduce-scattered and the outputs return to the token-sharded
 layout. Reassembled, every output must equal the single-rank oracle on the
 whole layer: bit for bit where a group's arithmetic is untouched by the
 split, and to fp64 rounding for dk_idx, whose sum over groups is regrouped.
+The same holds for the indexer warmup's full attention (the oracle with no
+block list, every visible token), which returns no block_idx.
 """
 import os
 import socket
@@ -43,7 +45,22 @@ def _oracle_compute(loc, t, kl_weight):
     return out
 
 
-def _rank(rank, world, port, q):
+def _oracle_compute_dense(loc, t, kl_weight):
+    """Full attention on one group slice by the fp64 oracle (no block list)."""
+    import torch
+
+    import oracle
+
+    a = {n: t[n].numpy().view(np.uint16) for n in ("Q", "K", "V", "dO", "q_idx", "k_idx")}
+    s = oracle.shape(loc.B, loc.T, loc.Hq, loc.G, loc.d, loc.d_idx, loc.Bk, loc.k, kl_weight=kl_weight)
+    O, LSE = oracle.full_fwd(s, a["Q"], a["K"], a["V"], None)
+    g = oracle.full_bwd(s, a["Q"], a["K"], a["V"], a["dO"], a["q_idx"], a["k_idx"], None)
+    out = {n: torch.from_numpy(np.ascontiguousarray(v)) for n, v in g.items()}
+    out.update(O=torch.from_numpy(O), LSE=torch.from_numpy(LSE))
+    return out
+
+
+def _rank(rank, world, port, q, mode):
     import torch
     import torch.distributed as dist
 
@@ -62,7 +79,8 @@ def _rank(rank, world, port, q):
         back = cp.heads_to_seq(cp.seq_to_heads(x, 1, 2, world), 1, 2, world)
         assert torch.equal(back, x)
         s = cp.LayerShape(B=W.B, T=W.T, Hq=W.Hq, G=W.G, d=W.d, d_idx=W.d_idx, Bk=W.Bk, k=W.k)
-        res = cp.cp_step(s, shards, _oracle_compute, kl_weight=0.5)
+        compute = _oracle_compute if mode == "sparse" else _oracle_compute_dense
+        res = cp.cp_step(s, shards, compute, kl_weight=0.5)
         q.put((rank, {n: v.numpy() for n, v in res.items()}))
     except Exception as e:  # reported to the parent, which fails the test at once
         q.put((rank, f"{type(e).__name__}: {e}"))
@@ -71,7 +89,8 @@ def _rank(rank, world, port, q):
         dist.destroy_process_group()
 
 
-def test_context_parallel_two_ranks_equal_single_rank():
+@pytest.mark.parametrize("mode", ["sparse", "dense"])
+def test_context_parallel_two_ranks_equal_single_rank(mode):
     import torch.multiprocessing as mp
 
     import oracle
@@ -81,7 +100,7 @@ def test_context_parallel_two_ranks_equal_single_rank():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_rank, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_rank, args=(r, world, port, q, mode)) for r in range(world)]
     for p in procs:
         p.start()
     got = dict(q.get(timeout=300) for _ in range(world))
@@ -91,18 +110,20 @@ def test_context_parallel_two_ranks_equal_single_rank():
         p.join(timeout=60)
         assert p.exitcode == 0
     # reassemble the token shards
+    names = [n for n in cp.OUTPUTS if mode == "sparse" or n != "block_idx"]
+    assert sorted(got[0]) == sorted(names)
     full = {}
-    for n in cp.OUTPUTS:
+    for n in names:
         t_axis = 1 if n in ("dk_idx",) else cp.AXES[n][0]
         full[n] = np.concatenate([got[r][n] for r in range(world)], axis=t_axis)
 
     inp = synth.make_inputs(W)
     s = oracle.shape_of(W, kl_weight=0.5)
-    bi, _, _ = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])
+    bi = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])[0] if mode == "sparse" else None
     O, LSE = oracle.full_fwd(s, inp["Q"], inp["K"], inp["V"], bi)
     ref = oracle.full_bwd(s, *[inp[n] for n in ("Q", "K", "V", "dO", "q_idx", "k_idx")], bi)
     ref.update(block_idx=bi, O=O, LSE=LSE)
-    for n in cp.OUTPUTS:
+    for n in names:
         assert full[n].shape == np.asarray(ref[n]).shape, n
         if n == "dk_idx":
             np.testing.assert_allclose(full[n], ref[n], rtol=1e-12, atol=1e-14)

@@ -51,3 +51,42 @@ def test_group_slices_equal_whole_layer():
     dki = parts[0]["dk_idx"] + parts[1]["dk_idx"]
     torch.testing.assert_close(dki, full["dk_idx"], rtol=1e-4, atol=1e-5)
     assert float(full["dk_idx"].abs().max()) > 1e-3
+
+
+def test_full_attention_group_slices_equal_whole_layer():
+    """The same for the indexer warmup's full attention (cuda_compute_dense):
+    the forward is deterministic and per group, so O and LSE are bit-identical;
+    the backward adds its sums with atomics, so the gradients and KL match the
+    whole-layer call to fp32 rounding, dk_idx once the slices' sums are added."""
+    import __graft_entry__
+
+    __graft_entry__.build_library()
+    from block_sparse_attention_scores_gb300 import context_parallel as cp
+
+    w = synth.CONFIGS[1].with_(T=2048, name="cp_dense_b1_t2048_hq32_g8")
+    inp = synth.make_inputs(w)
+    d = {n: to_dev(inp[n]) for n in cp.INPUTS}
+    s = cp.LayerShape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=1)
+    full = cp.cuda_compute_dense(s, d)
+    world = 2
+    loc = cp.local_shape(s, world)
+    hg = w.Hq // w.G
+    parts = []
+    for r in range(world):
+        g0, g1 = cp.group_range(w.G, world, r)
+        t = dict(Q=d["Q"][:, :, g0 * hg:g1 * hg].contiguous(), dO=d["dO"][:, :, g0 * hg:g1 * hg].contiguous(),
+                 K=d["K"][:, :, g0:g1].contiguous(), V=d["V"][:, :, g0:g1].contiguous(),
+                 q_idx=d["q_idx"][:, :, g0:g1].contiguous(), k_idx=d["k_idx"])
+        parts.append(cp.cuda_compute_dense(loc, t))
+    torch.cuda.synchronize()
+    assert "block_idx" not in full
+    for n in ("O", "LSE", "dQ", "dK", "dV", "dq_idx", "KL"):
+        t_axis, h_axis = cp.AXES[n]
+        got = torch.cat([p[n] for p in parts], dim=h_axis)
+        if n in ("O", "LSE"):
+            assert torch.equal(got, full[n]), n
+        else:
+            torch.testing.assert_close(got, full[n], rtol=1e-4, atol=1e-5)
+    dki = parts[0]["dk_idx"] + parts[1]["dk_idx"]
+    torch.testing.assert_close(dki, full["dk_idx"], rtol=1e-4, atol=1e-5)
+    assert float(full["dk_idx"].abs().max()) > 1e-3
