@@ -42,6 +42,17 @@ def assert_close(name, got, want, max_abs=2e-2, min_cos=0.999):
     return err, cos
 
 
+def assert_kl_sum(got, want, rtol=1e-3):
+    """Sum of the per-row KL over the compared rows, to a relative error of rtol
+    (the per-row bound above is absolute; this one catches a small bias that
+    every row shares, e.g. a dropped term or a wrong logarithm base)."""
+    sg = float(np.sum(np.asarray(got, np.float64)))
+    sw = float(np.sum(np.asarray(want, np.float64)))
+    rel = abs(sg - sw) / max(abs(sw), 1e-30)
+    assert rel <= rtol, f"sum of KL {sg:.9g} against {sw:.9g}: relative error {rel:.3e} > {rtol}"
+    return rel
+
+
 def compare_block_idx(got, want, gap, tie_eps=1e-4):
     """Bit-exact block ids, except rows whose oracle k-th/(k+1)-th gap < tie_eps.
 

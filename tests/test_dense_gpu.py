@@ -15,7 +15,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import assert_close, to_dev, to_f64
+from helpers import assert_close, assert_kl_sum, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 NAMES = ("Q", "K", "V", "dO", "q_idx", "k_idx")
@@ -73,6 +73,7 @@ def test_dense_matches_oracle_full(msa, w, scale):
         # with its magnitude, which large logits raise to tens (dQ up to 45, dK 70 at scale 1)
         bound = 2e-2 * max(1.0, float(np.abs(ref[name]).max()))
         msg.append((name,) + assert_close(name, to_f64(got[name]), ref[name], max_abs=bound))
+    assert_kl_sum(to_f64(got["KL"]), ref["KL"])
     print(w.name + ": " + "  ".join(f"{n} err={e:.1e} cos={c:.6f}" for n, e, c in msg))
 
 
@@ -131,6 +132,7 @@ def _sampled(msa, w, rows_n, blocks, seed, group=None):
     res.append(("dQ",) + assert_close("dQ", gdQ, dQ))
     res.append(("dq_idx",) + assert_close("dq_idx", _pick(got["dq_idx"], b, t, g), dqi))
     res.append(("KL",) + assert_close("KL", _pick(got["KL"], b, g, t), KL))
+    assert_kl_sum(_pick(got["KL"], b, g, t), KL)
     bb = np.array([x[0] for x in blocks])
     cc = np.array([x[1] for x in blocks])
     dK, dV, dki = oracle.bwd_blocks(s, *[inp[n] for n in NAMES], None, blocks=bb * w.n_blocks + cc, group=group)

@@ -22,7 +22,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import assert_close, compare_block_idx, to_dev, to_f64
+from helpers import assert_close, assert_kl_sum, compare_block_idx, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,7 @@ def test_timed_path_t131072(msa):
     res.append(("dQ",) + assert_close("dQ", gdQ, dQ))
     res.append(("dq_idx",) + assert_close("dq_idx", to_f64(g["dq_idx"])[0, t_q, g_q], dqi))
     res.append(("KL",) + assert_close("KL", to_f64(g["KL"])[0, g_q, t_q], KL))
+    assert_kl_sum(to_f64(g["KL"])[0, g_q, t_q], KL)
 
     # ---- per-block backward: the longest list (selections summed over groups) and an early block
     counts = np.bincount(bi_h[bi_h >= 0].ravel(), minlength=w.n_blocks)

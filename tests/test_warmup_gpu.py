@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from helpers import assert_close, to_dev, to_f64
+from helpers import assert_close, assert_kl_sum, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -87,6 +87,7 @@ def test_warmup_step_matches_oracle_full(msa, w):
     msg.append(("LSE",) + assert_close("LSE", to_f64(got["LSE"]).reshape(LSE_ref.shape), LSE_ref))
     for name in ("dQ", "dK", "dV", "dq_idx", "dk_idx", "KL"):
         msg.append((name,) + assert_close(name, to_f64(got[name]), ref[name]))
+    assert_kl_sum(to_f64(got["KL"]), ref["KL"])
     print(w.name + ": " + "  ".join(f"{n} err={e:.1e} cos={c:.6f}" for n, e, c in msg))
 
 
@@ -125,6 +126,7 @@ def _sampled_parity(msa, w, bi, label, seed, blocks):
     res.append(("dQ",) + assert_close("dQ", gdQ, dQ))
     res.append(("dq_idx",) + assert_close("dq_idx", to_f64(got["dq_idx"])[b, t, g], dqi))
     res.append(("KL",) + assert_close("KL", to_f64(got["KL"])[b, g, t], KL))
+    assert_kl_sum(to_f64(got["KL"])[b, g, t], KL)
     bb = np.array([x[0] for x in blocks])
     cc = np.array([x[1] for x in blocks])
     dK, dV, dki = oracle.bwd_blocks(os_, *[inp[n] for n in names], bi, blocks=bb * w.n_blocks + cc)
