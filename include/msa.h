@@ -191,8 +191,9 @@ MSA_API msa_status msa_bwd(const msa_shape *shape, const void *Q, const void *K,
                    float *dk_idx, float *KL, void *workspace, size_t workspace_bytes, msa_stream_t stream);
 
 /*
- * Index top-k for callers that cannot allocate device memory. The paper has
- * no counterpart to this call; it computes exactly what msa_index_topk does.
+ * Index top-k for callers that cannot allocate device memory. The method's
+ * description has no counterpart to this call; it computes exactly what
+ * msa_index_topk does.
  *
  * Some callers cannot call cudaMalloc: a plugin inside a host application
  * that owns every byte of device memory and hands the plugin no allocator,

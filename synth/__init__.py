@@ -165,6 +165,12 @@ CONFIGS = {
     3: Workload("msa_b1_t131072_hq32_g8_k16", B=1, T=131072, Hq=32, G=8, seed=SEED_BASE + 3),
     4: Workload("msa_b1_t1048576_hq16_g4_k16", B=1, T=1048576, Hq=16, G=4, seed=SEED_BASE + 4),
 }
+# The same five by their sizes (the id above only fixes each one's seed).
+T1024 = CONFIGS[0]      # B=1, T=1024, Hq=8, G=2, k=4
+T8192 = CONFIGS[1]      # B=1, T=8192, Hq=32, G=8, k=16
+B4_T8192 = CONFIGS[2]   # B=4, T=8192, Hq=32, G=8, k=16
+T131072 = CONFIGS[3]    # B=1, T=131072, Hq=32, G=8, k=16
+T1048576 = CONFIGS[4]   # B=1, T=1048576, Hq=16, G=4, k=16
 
 
 def make_inputs(w: Workload, which=("Q", "K", "V", "dO", "q_idx", "k_idx")) -> dict:

@@ -30,7 +30,7 @@ def cosine(a, b):
 
 
 def assert_close(name, got, want, max_abs=2e-2, min_cos=0.999):
-    """The benchmark spec's tolerance for bf16 outputs with fp32 accumulation."""
+    """The parity bar for bf16 inputs with fp32 accumulation: max |err| <= 2e-2 and cosine >= 0.999."""
     got = np.asarray(got, np.float64)
     want = np.asarray(want, np.float64)
     assert got.shape == want.shape, (name, got.shape, want.shape)

@@ -1,29 +1,32 @@
-"""The bench's counted work (selected pairs and FLOPs) against the workload
-table the configurations were specified with, and against a direct count on
-a selection generated for a small shape."""
+"""The bench's counted work (selected pairs and FLOPs) against the table the
+five workloads were specified with, and against a direct count on a
+selection generated for a small shape."""
 import pytest
 
 import bench
 import synth
 
-# selected, causally visible (query, key) pairs per (b, g) for the five workloads
-N_SEL = {0: 360_960, 1: 14_290_944, 2: 14_290_944, 3: 258_146_304, 4: 2_078_932_992}
-# forward (index + main) and forward+backward FLOPs, to the table's precision
-FWD = {0: 1.61e9, 1: 2.69e11, 2: 1.07e12, 3: 1.30e13, 4: 2.99e14}
-FWD_BWD = {0: 5.59e9, 1: 8.98e11, 2: 3.59e12, 3: 2.44e13, 4: 3.44e14}
+# per workload: selected, causally visible (query, key) pairs per (b, g); forward (index + main) and
+# forward+backward FLOPs, to the table's precision
+COUNTS = [
+    (synth.T1024, 360_960, 1.61e9, 5.59e9),
+    (synth.T8192, 14_290_944, 2.69e11, 8.98e11),
+    (synth.B4_T8192, 14_290_944, 1.07e12, 3.59e12),
+    (synth.T131072, 258_146_304, 1.30e13, 2.44e13),
+    (synth.T1048576, 2_078_932_992, 2.99e14, 3.44e14),
+]
 
 
-@pytest.mark.parametrize("cfg", range(5))
-def test_selected_pairs_and_flops(cfg):
-    w = synth.CONFIGS[cfg]
-    assert bench.n_selected(w) == N_SEL[cfg]
+@pytest.mark.parametrize("w,n_sel,fwd,fwd_bwd", COUNTS, ids=[c[0].name for c in COUNTS])
+def test_selected_pairs_and_flops(w, n_sel, fwd, fwd_bwd):
+    assert bench.n_selected(w) == n_sel
     f = bench.counted_flops(w)
-    assert f["index"] + f["fwd"] == pytest.approx(FWD[cfg], rel=6e-3)
-    assert f["total"] == pytest.approx(FWD_BWD[cfg], rel=6e-3)
+    assert f["index"] + f["fwd"] == pytest.approx(fwd, rel=6e-3)
+    assert f["total"] == pytest.approx(fwd_bwd, rel=6e-3)
 
 
 def test_selected_pairs_equal_a_direct_count():
-    w = synth.CONFIGS[0].with_(T=2048, k=5)
+    w = synth.T1024.with_(T=2048, k=5)
     bi = synth.synthetic_block_idx(w)
     direct = 0
     for row_t in range(w.T):
@@ -40,7 +43,7 @@ def test_algorithmic_bytes_are_the_entry_points_tensor_sizes():
 
     import bench
 
-    for w in (synth.CONFIGS[0], synth.CONFIGS[1].with_(B=2, T=1024)):
+    for w in (synth.T1024, synth.T8192.with_(B=2, T=1024)):
         B, T, Hq, G, d, E, k = w.B, w.T, w.Hq, w.G, w.d, w.d_idx, w.k
         bf, f32, i32 = np.uint16, np.float32, np.int32
         t = dict(Q=((B, T, Hq, d), bf), K=((B, T, G, d), bf), V=((B, T, G, d), bf), O=((B, T, Hq, d), bf),

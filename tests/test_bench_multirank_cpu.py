@@ -24,7 +24,7 @@ def _worker(rank, world, port, q):
     try:
         ms = 10.0 + 5.0 * rank  # rank 1 is the slow one
         m = bench.dist_max(ms)
-        w = bench.rank_workload(bench.synth.CONFIGS[0], rank)
+        w = bench.rank_workload(bench.synth.T1024, rank)
         q.put((rank, m, w.seed, w.T, bench.aggregate_tokens_per_s(w, world, m)))
         dist.barrier()
     finally:

@@ -42,13 +42,13 @@ def _gpu(msa, w, inp, bi, kl_weight=1.0):
 
 
 SMALL = [
-    synth.CONFIGS[0],
-    synth.CONFIGS[0].with_(T=128, name="single_block"),
-    synth.CONFIGS[0].with_(T=512, k=1, name="k1_own_block_only"),
-    synth.CONFIGS[0].with_(T=640, k=8, name="k_gt_blocks_dense_causal"),
-    synth.CONFIGS[0].with_(B=2, T=768, Hq=3, G=3, k=3, name="b2_hg1"),
-    synth.CONFIGS[0].with_(T=1024, Hq=4, G=2, k=5, name="hg2"),
-    synth.CONFIGS[0].with_(T=1024, Hq=16, G=2, k=6, name="hg8"),
+    synth.T1024,
+    synth.T1024.with_(T=128, name="single_block"),
+    synth.T1024.with_(T=512, k=1, name="k1_own_block_only"),
+    synth.T1024.with_(T=640, k=8, name="k_gt_blocks_dense_causal"),
+    synth.T1024.with_(B=2, T=768, Hq=3, G=3, k=3, name="b2_hg1"),
+    synth.T1024.with_(T=1024, Hq=4, G=2, k=5, name="hg2"),
+    synth.T1024.with_(T=1024, Hq=16, G=2, k=6, name="hg8"),
 ]
 
 
@@ -68,7 +68,7 @@ def test_bwd_matches_oracle_full(msa, w):
 
 
 def test_bwd_kl_weight_scales_index_gradients_only(msa):
-    w = synth.CONFIGS[0].with_(T=512)
+    w = synth.T1024.with_(T=512)
     inp = synth.make_inputs(w)
     s = oracle.shape_of(w)
     bi, _, _ = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])
@@ -113,21 +113,20 @@ def _check_sampled(msa, w, bi, n_rows, blocks, seed):
     return out
 
 
-def test_bwd_config1_sampled(msa):
-    w = synth.CONFIGS[1]
+def test_bwd_t8192_sampled(msa):
+    w = synth.T8192
     inp = synth.make_inputs(w, ("q_idx", "k_idx"))
     bi, _, _ = oracle.full_topk(oracle.shape_of(w), inp["q_idx"], inp["k_idx"])
     res = _check_sampled(msa, w, bi, 256, [(0, 3), (0, 63)], seed=1)
-    print("config1: " + "  ".join(f"{n} err={e:.1e} cos={c:.6f}" for n, e, c in res))
+    print(w.name + ": " + "  ".join(f"{n} err={e:.1e} cos={c:.6f}" for n, e, c in res))
 
 
-@pytest.mark.parametrize("cfg_id,n_rows,blocks", [
-    (2, 128, [(3, 40)]),
-    (3, 96, [(0, 1000)]),
-    (4, 48, [(0, 8191)]),
-])
-def test_bwd_large_configs_sampled(msa, cfg_id, n_rows, blocks):
-    w = synth.CONFIGS[cfg_id]
+@pytest.mark.parametrize("w,n_rows,blocks,seed", [
+    (synth.B4_T8192, 128, [(3, 40)], 2),
+    (synth.T131072, 96, [(0, 1000)], 3),
+    (synth.T1048576, 48, [(0, 8191)], 4),
+], ids=["b4_t8192", "t131072", "t1048576"])
+def test_bwd_large_workloads_sampled(msa, w, n_rows, blocks, seed):
     bi = synth.synthetic_block_idx(w)
-    res = _check_sampled(msa, w, bi, n_rows, blocks, seed=cfg_id)
-    print(f"config{cfg_id}: " + "  ".join(f"{n} err={e:.1e} cos={c:.6f}" for n, e, c in res))
+    res = _check_sampled(msa, w, bi, n_rows, blocks, seed=seed)
+    print(f"{w.name}: " + "  ".join(f"{n} err={e:.1e} cos={c:.6f}" for n, e, c in res))

@@ -20,7 +20,7 @@ import pytest
 
 import synth
 
-W = synth.CONFIGS[0].with_(T=512, Hq=8, G=4, k=3, name="cp_b1_t512_hq8_g4_k3")
+W = synth.T1024.with_(T=512, Hq=8, G=4, k=3, name="cp_b1_t512_hq8_g4_k3")
 
 
 def _free_port():

@@ -25,7 +25,7 @@ def test_group_slices_equal_whole_layer():
     __graft_entry__.build_library()
     from block_sparse_attention_scores_gb300 import context_parallel as cp
 
-    w = synth.CONFIGS[1].with_(T=2048, name="cp_b1_t2048_hq32_g8_k16")
+    w = synth.T8192.with_(T=2048, name="cp_b1_t2048_hq32_g8_k16")
     inp = synth.make_inputs(w)
     d = {n: to_dev(inp[n]) for n in cp.INPUTS}
     s = cp.LayerShape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
@@ -63,7 +63,7 @@ def test_full_attention_group_slices_equal_whole_layer():
     __graft_entry__.build_library()
     from block_sparse_attention_scores_gb300 import context_parallel as cp
 
-    w = synth.CONFIGS[1].with_(T=2048, name="cp_dense_b1_t2048_hq32_g8")
+    w = synth.T8192.with_(T=2048, name="cp_dense_b1_t2048_hq32_g8")
     inp = synth.make_inputs(w)
     d = {n: to_dev(inp[n]) for n in cp.INPUTS}
     s = cp.LayerShape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=1)

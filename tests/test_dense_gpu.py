@@ -51,11 +51,11 @@ def _run_dense(msa, w, inp, scale=0.0, kl_weight=1.0):
 
 
 SMALL = [
-    (synth.CONFIGS[0].with_(T=128, name="one_block"), 0.0),
-    (synth.CONFIGS[0].with_(name="t1024_hg4"), 0.0),
-    (synth.CONFIGS[0].with_(B=2, T=768, Hq=16, G=2, name="b2_t768_hg8"), 0.0),
+    (synth.T1024.with_(T=128, name="one_block"), 0.0),
+    (synth.T1024.with_(name="t1024_hg4"), 0.0),
+    (synth.T1024.with_(B=2, T=768, Hq=16, G=2, name="b2_t768_hg8"), 0.0),
     # scale 1: logits about 16x the default, so the running maximum of a row moves by more than 2^8
-    (synth.CONFIGS[0].with_(T=1024, Hq=4, G=1, name="t1024_large_logits"), 1.0),
+    (synth.T1024.with_(T=1024, Hq=4, G=1, name="t1024_large_logits"), 1.0),
 ]
 
 
@@ -78,8 +78,8 @@ def test_dense_matches_oracle_full(msa, w, scale):
 
 
 @pytest.mark.parametrize("w", [
-    synth.CONFIGS[1].with_(B=2, name="b2_t8192"),
-    synth.CONFIGS[1].with_(T=16384, name="t16384"),
+    synth.T8192.with_(B=2, name="b2_t8192"),
+    synth.T8192.with_(T=16384, name="t16384"),
 ], ids=lambda w: w.name)
 def test_dense_equals_sparse_path_on_full_selection(msa, w):
     """Two independent GPU paths to the same full attention: query-outer dense
@@ -150,8 +150,8 @@ def _sampled(msa, w, rows_n, blocks, seed, group=None):
 
 @pytest.mark.parametrize("w,blocks", [
     # 4608 queries: segments [0, 4096) and [4096, 4608); block 30's queries lie in both, block 24's too
-    (synth.CONFIGS[0].with_(B=2, T=4608, name="b2_t4608_hg4"), [(0, 30), (1, 24), (1, 35)]),
-    (synth.CONFIGS[0].with_(T=4608, Hq=16, G=2, name="t4608_hg8"), [(0, 31), (0, 33)]),
+    (synth.T1024.with_(B=2, T=4608, name="b2_t4608_hg4"), [(0, 30), (1, 24), (1, 35)]),
+    (synth.T1024.with_(T=4608, Hq=16, G=2, name="t4608_hg8"), [(0, 31), (0, 33)]),
 ], ids=["b2_t4608_hg4", "t4608_hg8"])
 def test_dense_sampled_across_segments(msa, w, blocks):
     _sampled(msa, w, 64, blocks, seed=11)
@@ -161,5 +161,5 @@ def test_dense_full_size_sampled(msa):
     """T = 131072, Hq = 32, G = 8 (the headline layer): sampled rows, and the
     last KV block's dK, dV for one group (every group's queries of one block
     would cost the oracle a minute)."""
-    w = synth.CONFIGS[3]
+    w = synth.T131072
     _sampled(msa, w, 40, [(0, w.n_blocks - 1)], seed=13, group=3)

@@ -43,8 +43,8 @@ def _run(msa, w, inp):
     return {k: (v.view(torch.int16) if v.dtype == torch.bfloat16 else v).cpu().numpy() for k, v in res.items()}
 
 
-@pytest.mark.parametrize("w", [synth.CONFIGS[0], synth.CONFIGS[0].with_(T=4096, Hq=16, G=4, k=8, name="t4096_hg4"),
-                               synth.CONFIGS[0].with_(T=2048, Hq=4, G=2, k=8, name="t2048_hg2")],
+@pytest.mark.parametrize("w", [synth.T1024, synth.T1024.with_(T=4096, Hq=16, G=4, k=8, name="t4096_hg4"),
+                               synth.T1024.with_(T=2048, Hq=4, G=2, k=8, name="t2048_hg2")],
                          ids=["cfg0", "t4096_hg4", "t2048_hg2"])
 def test_two_runs_give_identical_bits(msa, w):
     inp = synth.make_inputs(w)

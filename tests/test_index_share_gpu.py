@@ -52,8 +52,8 @@ def _outputs(msa, s, w, d, bi, ws, mapped):
     return {k: _host(v) for k, v in out.items()}
 
 
-@pytest.mark.parametrize("w", [synth.CONFIGS[0], synth.CONFIGS[0].with_(T=4096, Hq=16, G=4, k=8, name="t4096_hg4"),
-                               synth.CONFIGS[0].with_(B=2, T=768, Hq=3, G=3, k=3, name="b2_hg1")],
+@pytest.mark.parametrize("w", [synth.T1024, synth.T1024.with_(T=4096, Hq=16, G=4, k=8, name="t4096_hg4"),
+                               synth.T1024.with_(B=2, T=768, Hq=3, G=3, k=3, name="b2_hg1")],
                          ids=["cfg0", "t4096_hg4", "b2_hg1"])
 def test_mapped_calls_match_unmapped(msa, w):
     inp = synth.make_inputs(w)
@@ -82,7 +82,7 @@ def test_mapped_calls_match_unmapped(msa, w):
 def test_mapped_calls_need_a_backward_workspace(msa):
     import torch
 
-    w = synth.CONFIGS[0]
+    w = synth.T1024
     s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
     small = msa.alloc_workspace(s, msa.MSA_WS_FWD)
     bi = torch.zeros((w.B, w.G, w.T, w.k), dtype=torch.int32, device="cuda")

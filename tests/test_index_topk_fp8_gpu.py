@@ -38,11 +38,11 @@ def _run(msa, w):
 
 
 @pytest.mark.parametrize("cfg", [
-    synth.CONFIGS[0],
-    synth.CONFIGS[0].with_(T=128, name="single_block"),
-    synth.CONFIGS[0].with_(B=2, T=768, G=3, Hq=3, k=5, name="b2_g3_hg1"),
-    synth.CONFIGS[0].with_(T=1536, G=2, Hq=16, k=33, name="k33"),
-    synth.CONFIGS[1],
+    synth.T1024,
+    synth.T1024.with_(T=128, name="single_block"),
+    synth.T1024.with_(B=2, T=768, G=3, Hq=3, k=5, name="b2_g3_hg1"),
+    synth.T1024.with_(T=1536, G=2, Hq=16, k=33, name="k33"),
+    synth.T8192,
 ], ids=["cfg0", "single_block", "b2_g3_hg1", "k33", "cfg1"])
 def test_index_topk_fp8_matches_oracle(msa, cfg):
     inp, got = _run(msa, cfg)
@@ -62,15 +62,15 @@ def test_index_topk_fp8_matches_oracle(msa, cfg):
 
 
 def test_fp8_workspace_kind(msa):
-    w = synth.CONFIGS[0]
+    w = synth.T1024
     s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
     need = msa.msa_workspace_size(s, msa.MSA_WS_TOPK_FP8)
     assert need >= w.B * w.T * (w.G + 1) * w.d_idx + w.B * w.n_blocks * 4
 
 
 @pytest.mark.parametrize("cfg", [
-    synth.CONFIGS[0].with_(T=4096, G=2, Hq=16, k=16, name="ties_k16"),
-    synth.CONFIGS[0].with_(T=8192, G=1, Hq=8, k=33, name="ties_k33"),
+    synth.T1024.with_(T=4096, G=2, Hq=16, k=16, name="ties_k16"),
+    synth.T1024.with_(T=8192, G=1, Hq=8, k=33, name="ties_k33"),
 ], ids=["k16", "k33"])
 def test_index_topk_fp8_exact_ties(msa, cfg):
     """tied_index_inputs through the FP8 path: the keys of every block share one
@@ -93,14 +93,14 @@ def test_index_topk_fp8_exact_ties(msa, cfg):
     assert bad == 0
 
 
-@pytest.mark.parametrize("cfg_id,n_per_group", [(3, 64), (4, 24)])
-def test_index_topk_fp8_large_configs_sampled(msa, cfg_id, n_per_group):
+@pytest.mark.parametrize("w,n_per_group,seed", [(synth.T131072, 64, 103), (synth.T1048576, 24, 104)],
+                         ids=["t131072", "t1048576"])
+def test_index_topk_fp8_large_workloads_sampled(msa, w, n_per_group, seed):
     """The full-size workloads (T = 131072 and T = 2^20), in the launch
     configuration the bench times: sampled rows (first and last positions,
     block edges, random positions) against the oracle's FP8 selection."""
-    w = synth.CONFIGS[cfg_id]
     inp, got = _run(msa, w)
-    rng = np.random.default_rng(100 + cfg_id)
+    rng = np.random.default_rng(seed)
     rows = []
     for b in range(w.B):
         for g in range(w.G):
@@ -112,5 +112,5 @@ def test_index_topk_fp8_large_configs_sampled(msa, cfg_id, n_per_group):
     valid_selection(got[:, :, : min(w.T, 4096)], min(w.T, 4096), w.Bk)
     want, gap, _ = oracle.index_topk_fp8(oracle.shape_of(w), inp["q_idx"], inp["k_idx"], rows=rows)
     n, ties, bad, bad_tie = compare_block_idx(got[b, g, t], want, gap)
-    print(f"config{cfg_id}: sampled rows={n} near_ties={ties} mismatches(outside ties)={bad} (in ties)={bad_tie}")
+    print(f"{w.name}: sampled rows={n} near_ties={ties} mismatches(outside ties)={bad} (in ties)={bad_tie}")
     assert bad == 0

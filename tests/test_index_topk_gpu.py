@@ -33,13 +33,13 @@ def _run(msa, w):
 
 
 @pytest.mark.parametrize("cfg", [
-    synth.CONFIGS[0],                                           # T=1024, G=2, k=4 (fewer blocks than k early on)
-    synth.CONFIGS[0].with_(T=128, name="single_block"),         # only the own block exists
-    synth.CONFIGS[0].with_(T=384, k=1, name="k1"),              # own block only
-    synth.CONFIGS[0].with_(T=640, k=8, name="k_gt_blocks"),     # k > number of blocks: all visible kept
-    synth.CONFIGS[0].with_(B=2, T=768, G=3, Hq=3, k=5, name="b2_g3_hg1"),
-    synth.CONFIGS[0].with_(T=2048, G=1, Hq=8, k=20, name="k20"),
-    synth.CONFIGS[0].with_(T=1536, G=2, Hq=16, k=33, name="k33"),
+    synth.T1024,                                           # T=1024, G=2, k=4 (fewer blocks than k early on)
+    synth.T1024.with_(T=128, name="single_block"),         # only the own block exists
+    synth.T1024.with_(T=384, k=1, name="k1"),              # own block only
+    synth.T1024.with_(T=640, k=8, name="k_gt_blocks"),     # k > number of blocks: all visible kept
+    synth.T1024.with_(B=2, T=768, G=3, Hq=3, k=5, name="b2_g3_hg1"),
+    synth.T1024.with_(T=2048, G=1, Hq=8, k=20, name="k20"),
+    synth.T1024.with_(T=1536, G=2, Hq=16, k=33, name="k33"),
 ])
 def test_index_topk_matches_oracle_full(msa, cfg):
     inp, got = _run(msa, cfg)
@@ -50,21 +50,21 @@ def test_index_topk_matches_oracle_full(msa, cfg):
     assert bad == 0
 
 
-def test_index_topk_config1_full(msa):
-    w = synth.CONFIGS[1]
+def test_index_topk_t8192_full(msa):
+    w = synth.T8192
     inp, got = _run(msa, w)
     valid_selection(got, w.T, w.Bk)
     want, gap, _ = oracle.full_topk(oracle.shape_of(w), inp["q_idx"], inp["k_idx"])
     n, ties, bad, bad_tie = compare_block_idx(got, want, gap)
-    print(f"config1: rows={n} near_ties={ties} mismatches(outside ties)={bad} mismatches(in ties)={bad_tie}")
+    print(f"{w.name}: rows={n} near_ties={ties} mismatches(outside ties)={bad} mismatches(in ties)={bad_tie}")
     assert bad == 0
 
 
 @pytest.mark.parametrize("cfg", [
-    synth.CONFIGS[0].with_(T=4096, G=2, Hq=2, k=5, name="ties_k5"),
-    synth.CONFIGS[0].with_(T=4096, G=2, Hq=16, k=16, name="ties_k16"),
-    synth.CONFIGS[0].with_(T=8192, G=1, Hq=8, k=33, name="ties_k33"),
-    synth.CONFIGS[0].with_(T=12288, G=1, Hq=8, k=64, name="ties_k64"),
+    synth.T1024.with_(T=4096, G=2, Hq=2, k=5, name="ties_k5"),
+    synth.T1024.with_(T=4096, G=2, Hq=16, k=16, name="ties_k16"),
+    synth.T1024.with_(T=8192, G=1, Hq=8, k=33, name="ties_k33"),
+    synth.T1024.with_(T=12288, G=1, Hq=8, k=64, name="ties_k64"),
 ], ids=["k5", "k16", "k33", "k64"])
 def test_index_topk_exact_ties(msa, cfg):
     """Pooled scores that tie exactly (tied_index_inputs): every row must match the
@@ -98,11 +98,11 @@ def _sampled_rows(w, n_per_group, seed):
     return np.concatenate(rows)
 
 
-@pytest.mark.parametrize("cfg_id,n_per_group", [(2, 96), (3, 64), (4, 24)])
-def test_index_topk_large_configs_sampled(msa, cfg_id, n_per_group):
-    w = synth.CONFIGS[cfg_id]
+@pytest.mark.parametrize("w,n_per_group,seed", [(synth.B4_T8192, 96, 2), (synth.T131072, 64, 3),
+                                               (synth.T1048576, 24, 4)], ids=["b4_t8192", "t131072", "t1048576"])
+def test_index_topk_large_workloads_sampled(msa, w, n_per_group, seed):
     inp, got = _run(msa, w)
-    rows = _sampled_rows(w, n_per_group, seed=cfg_id)
+    rows = _sampled_rows(w, n_per_group, seed=seed)
     b = rows // (w.G * w.T)
     g = (rows // w.T) % w.G
     t = rows % w.T
@@ -110,5 +110,5 @@ def test_index_topk_large_configs_sampled(msa, cfg_id, n_per_group):
     valid_selection(got[:, :, : min(w.T, 4096)], min(w.T, 4096), w.Bk)
     want, gap, _ = oracle.index_topk(oracle.shape_of(w), inp["q_idx"], inp["k_idx"], rows=rows)
     n, ties, bad, bad_tie = compare_block_idx(sub, want, gap)
-    print(f"config{cfg_id}: sampled rows={n} near_ties={ties} mismatches(outside ties)={bad} (in ties)={bad_tie}")
+    print(f"{w.name}: sampled rows={n} near_ties={ties} mismatches(outside ties)={bad} (in ties)={bad_tie}")
     assert bad == 0

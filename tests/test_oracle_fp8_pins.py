@@ -69,7 +69,7 @@ def test_rounding_agrees_with_torch_float8():
 
 
 def test_quantization_reaches_full_range_and_stays_close():
-    w = synth.CONFIGS[0].with_(T=512)
+    w = synth.T1024.with_(T=512)
     inp = synth.make_inputs(w, which=("q_idx", "k_idx"))
     s = oracle.shape_of(w)
     q_deq, k_deq, sq, sk = oracle.quantize_fp8(s, inp["q_idx"], inp["k_idx"])
@@ -87,7 +87,7 @@ def test_quantization_reaches_full_range_and_stays_close():
 
 
 def test_fp8_selection_equals_bf16_selection_on_the_e4m3_grid():
-    w = synth.CONFIGS[0].with_(T=768, k=3)
+    w = synth.T1024.with_(T=768, k=3)
     rng = np.random.default_rng(11)
     grid = np.array(sorted(v for v, _ in _e4m3_table() if 0.25 <= abs(v) <= 448))
     q = rng.choice(grid, size=(w.B, w.T, w.G, w.d_idx))
@@ -107,7 +107,7 @@ def test_fp8_selection_equals_bf16_selection_on_the_e4m3_grid():
 def test_all_zero_row_and_block_quantize_with_scale_one_and_tie_to_lowest_blocks():
     # amax = 0: scale 1 and zero codes; a zero query row scores 0 against every
     # block, so the tie rule alone decides: the own block plus the lowest ids
-    w = synth.CONFIGS[0].with_(T=1024, k=4)
+    w = synth.T1024.with_(T=1024, k=4)
     inp = synth.make_inputs(w, which=("q_idx", "k_idx"))
     q = inp["q_idx"].copy()
     k = inp["k_idx"].copy()

@@ -144,7 +144,7 @@ def _tied_closed_form(w, q_idx, k_idx):
 @pytest.mark.parametrize("k", [2, 4, 7])
 def test_topk_exact_tie_levels_match_tie_rule(k):
     # many exact ties at every rank, including larger values arriving after runs of equal ones
-    w = synth.CONFIGS[0].with_(T=1024, G=2, Hq=2, k=k, name="tied")
+    w = synth.T1024.with_(T=1024, G=2, Hq=2, k=k, name="tied")
     q_idx, k_idx = synth.tied_index_inputs(w)
     bi, gap, _ = oracle.full_topk(oracle.shape_of(w), q_idx, k_idx)
     assert np.array_equal(bi, _tied_closed_form(w, q_idx, k_idx))

@@ -37,13 +37,13 @@ def _gpu_fwd(msa, w, inp, bi):
 
 
 SMALL = [
-    synth.CONFIGS[0],
-    synth.CONFIGS[0].with_(T=128, name="single_block"),
-    synth.CONFIGS[0].with_(T=512, k=1, name="k1_own_block_only"),
-    synth.CONFIGS[0].with_(T=640, k=8, name="k_gt_blocks_dense_causal"),
-    synth.CONFIGS[0].with_(B=2, T=768, Hq=3, G=3, k=3, name="b2_hg1"),
-    synth.CONFIGS[0].with_(T=1024, Hq=4, G=2, k=5, name="hg2"),
-    synth.CONFIGS[0].with_(T=1024, Hq=16, G=2, k=6, name="hg8"),
+    synth.T1024,
+    synth.T1024.with_(T=128, name="single_block"),
+    synth.T1024.with_(T=512, k=1, name="k1_own_block_only"),
+    synth.T1024.with_(T=640, k=8, name="k_gt_blocks_dense_causal"),
+    synth.T1024.with_(B=2, T=768, Hq=3, G=3, k=3, name="b2_hg1"),
+    synth.T1024.with_(T=1024, Hq=4, G=2, k=5, name="hg2"),
+    synth.T1024.with_(T=1024, Hq=16, G=2, k=6, name="hg8"),
 ]
 
 
@@ -59,8 +59,8 @@ def test_sparse_fwd_matches_oracle_full(msa, w):
     print(f"{w.name}: O err={e1[0]:.2e} cos={e1[1]:.6f}  LSE err={e2[0]:.2e}")
 
 
-def test_sparse_fwd_config1_full(msa):
-    w = synth.CONFIGS[1]
+def test_sparse_fwd_t8192_full(msa):
+    w = synth.T8192
     inp = synth.make_inputs(w)
     s = oracle.shape_of(w)
     bi, _, _ = oracle.full_topk(s, inp["q_idx"], inp["k_idx"])
@@ -68,7 +68,7 @@ def test_sparse_fwd_config1_full(msa):
     O_ref, L_ref = oracle.full_fwd(s, inp["Q"], inp["K"], inp["V"], bi)
     e1 = assert_close("O", to_f64(O), O_ref)
     e2 = assert_close("LSE", to_f64(LSE), L_ref)
-    print(f"config1: O err={e1[0]:.2e} cos={e1[1]:.6f}  LSE err={e2[0]:.2e}")
+    print(f"{w.name}: O err={e1[0]:.2e} cos={e1[1]:.6f}  LSE err={e2[0]:.2e}")
 
 
 def _sample_rows(w, n, seed):
@@ -79,26 +79,26 @@ def _sample_rows(w, n, seed):
     return (b * w.T + t) * w.Hq + h
 
 
-@pytest.mark.parametrize("cfg_id,n", [(2, 512), (3, 512), (4, 256)])
-def test_sparse_fwd_large_configs_sampled(msa, cfg_id, n):
-    w = synth.CONFIGS[cfg_id]
+@pytest.mark.parametrize("w,n,seed", [(synth.B4_T8192, 512, 2), (synth.T131072, 512, 3), (synth.T1048576, 256, 4)],
+                         ids=["b4_t8192", "t131072", "t1048576"])
+def test_sparse_fwd_large_workloads_sampled(msa, w, n, seed):
     inp = synth.make_inputs(w, ("Q", "K", "V"))
     bi = synth.synthetic_block_idx(w)
     O, LSE = _gpu_fwd(msa, w, inp, bi)
-    rows = _sample_rows(w, n, cfg_id)
+    rows = _sample_rows(w, n, seed)
     O_ref, L_ref = oracle.sparse_fwd(oracle.shape_of(w), inp["Q"], inp["K"], inp["V"], bi, rows=rows)
     Og = to_f64(O.view(-1, w.d)[rows.tolist()])
     Lg = to_f64(LSE.view(-1)[rows.tolist()])
     e1 = assert_close("O", Og, O_ref)
     e2 = assert_close("LSE", Lg, L_ref)
-    print(f"config{cfg_id}: sampled rows={rows.size} O err={e1[0]:.2e} cos={e1[1]:.6f} LSE err={e2[0]:.2e}")
+    print(f"{w.name}: sampled rows={rows.size} O err={e1[0]:.2e} cos={e1[1]:.6f} LSE err={e2[0]:.2e}")
 
 
 def test_sparse_fwd_rejects_bad_block_idx(msa):
     """A row without its own block is reported through the device error word."""
     import torch
 
-    w = synth.CONFIGS[0].with_(T=256, k=2)
+    w = synth.T1024.with_(T=256, k=2)
     inp = synth.make_inputs(w, ("Q", "K", "V"))
     bi = synth.synthetic_block_idx(w)
     bi[0, 0, 200] = [0, -1]  # own block (1) missing

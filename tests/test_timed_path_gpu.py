@@ -40,7 +40,7 @@ def msa():
 def test_timed_path_t131072(msa):
     import torch
 
-    w = synth.CONFIGS[3]
+    w = synth.T131072
     inp = synth.make_inputs(w)
     s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
     ws = msa.alloc_workspace(s, msa.MSA_WS_BWD)

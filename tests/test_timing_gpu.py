@@ -17,7 +17,7 @@ def test_kernel_events_bracket_only_the_main_kernel():
     __graft_entry__.build_library()
     import block_sparse_attention_scores_gb300 as msa
 
-    w = synth.CONFIGS[0].with_(T=4096, k=8)
+    w = synth.T1024.with_(T=4096, k=8)
     inp = synth.make_inputs(w)
     s = msa.Shape(B=w.B, T=w.T, Hq=w.Hq, G=w.G, k=w.k)
     d = {n: to_dev(inp[n]) for n in inp}

@@ -52,11 +52,11 @@ def _run(msa, w, inp):
 
 
 @pytest.mark.parametrize("w", [
-    synth.CONFIGS[0].with_(T=128, k=1, name="one_block"),
-    synth.CONFIGS[0].with_(T=1024, k=8, name="t1024_k8"),
-    synth.CONFIGS[0].with_(T=1024, k=11, name="t1024_k11_padded"),
-    synth.CONFIGS[1].with_(B=2, k=64, name="t8192_k64"),
-    synth.CONFIGS[1].with_(T=16384, k=128, name="t16384_k128"),
+    synth.T1024.with_(T=128, k=1, name="one_block"),
+    synth.T1024.with_(T=1024, k=8, name="t1024_k8"),
+    synth.T1024.with_(T=1024, k=11, name="t1024_k11_padded"),
+    synth.T8192.with_(B=2, k=64, name="t8192_k64"),
+    synth.T8192.with_(T=16384, k=128, name="t16384_k128"),
 ], ids=lambda w: w.name)
 def test_warmup_selection_is_every_visible_block(msa, w):
     import torch
@@ -68,9 +68,9 @@ def test_warmup_selection_is_every_visible_block(msa, w):
 
 
 SMALL = [
-    _warm(synth.CONFIGS[0]),                                                  # T=1024, hg=4, k=8
-    _warm(synth.CONFIGS[0].with_(B=2, T=768, Hq=3, G=3, name="b2_hg1")),     # k=6
-    _warm(synth.CONFIGS[0].with_(T=1024, Hq=16, G=2, name="hg8")),
+    _warm(synth.T1024),                                                  # T=1024, hg=4, k=8
+    _warm(synth.T1024.with_(B=2, T=768, Hq=3, G=3, name="b2_hg1")),     # k=6
+    _warm(synth.T1024.with_(T=1024, Hq=16, G=2, name="hg8")),
 ]
 
 
@@ -141,9 +141,9 @@ def _sampled_parity(msa, w, bi, label, seed, blocks):
 
 @pytest.mark.parametrize("w,blocks", [
     # T=8192, all 64 blocks; block 0 is selected by every query of its batch
-    (_warm(synth.CONFIGS[1].with_(B=2)), [(0, 0), (1, 31), (1, 63)]),
+    (_warm(synth.T8192.with_(B=2)), [(0, 0), (1, 31), (1, 63)]),
     # T=16384, all 128 blocks; the last block keeps the oracle's per-block work small
-    (_warm(synth.CONFIGS[1].with_(T=16384, name="t16384")), [(0, 127)]),
+    (_warm(synth.T8192.with_(T=16384, name="t16384")), [(0, 127)]),
 ], ids=["t8192_k64", "t16384_k128"])
 def test_warmup_step_sampled(msa, w, blocks):
     """Dense causal attention and the dense-teacher KL at the largest sizes the
@@ -154,5 +154,5 @@ def test_warmup_step_sampled(msa, w, blocks):
 def test_wide_sparse_selection_sampled(msa):
     """A random selection of 96 blocks per row (between 64 and 128 slots) at
     T = 16384: the forward and backward merges' wide path."""
-    w = synth.CONFIGS[1].with_(T=16384, G=2, Hq=8, k=96, name="k96")
+    w = synth.T8192.with_(T=16384, G=2, Hq=8, k=96, name="k96")
     _sampled_parity(msa, w, synth.synthetic_block_idx(w), "sparse k96", seed=7, blocks=[(0, 124), (0, 127)])

@@ -17,8 +17,8 @@ from helpers import to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("w", [synth.CONFIGS[0].with_(T=2048, name="t2048"),
-                               synth.CONFIGS[0].with_(B=2, T=1536, G=3, Hq=6, k=6, name="b2_g3_k6")],
+@pytest.mark.parametrize("w", [synth.T1024.with_(T=2048, name="t2048"),
+                               synth.T1024.with_(B=2, T=1536, G=3, Hq=6, k=6, name="b2_g3_k6")],
                          ids=lambda w: w.name)
 def test_noalloc_topk_matches_workspace_topk_twice(w):
     import torch
